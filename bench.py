@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark: closed-form tree verify + commit of one GDN layer on a GB300.
+
+One step is one pass of the whole hot path over one batch: tree prep, the
+S0 contraction, the masked decayed A/C build, the triangular solve and the
+output (one verify call), then the commit of a root-to-leaf accepted path.
+Default workload: batched verify, B=16 streams, H=16 heads, dk=dv=128,
+T=64-node uniform random trees with depth 4..20, bf16 q/k/v, fp32 S0, fp32
+o (synthetic, seeded).  Metric: verified nodes/s (B*T per step) and us per
+layer verify.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl canopy|reference]
+  python bench.py --sweep          # crossover map vs the serial replay kernel
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronise on both sides, CUDA events on the launching stream, max
+over ranks.  Inputs rotate over enough independent sets that the data one
+step touches is not in L2 (129 MB) when the step starts.  Clocks are sampled
+with nvidia-smi during the timed region.  Under torchrun each rank runs the
+same per-GPU workload (replicas: the units are independent, no collective in
+the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = dict(name="batched verify B=16 T=64 H=16 dk=dv=128 random trees depth 4-20 bf16 q/k/v fp32 S0",
+                case=2, B=16, T=64, H=16, d=128)
+METRIC = "µs per GDN layer tree-verify and verified nodes/s (B=16,T=64); % HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def verify_bytes(B, T, H, d, in_bytes=2, o_bytes=4):
+    """Algorithmic bytes of one verify call: S0, q/k/v, g, beta and parent read;
+    o, U, l, depth and the ancestor mask written."""
+    W = (T + 31) // 32
+    return (B * H * d * d * 4 + B * T * H * d * in_bytes * 3 + B * T * H * 4 * 2 + B * T * 4
+            + B * T * H * d * o_bytes + B * T * H * d * 4 + B * T * H * 4 + B * T * 4 + B * T * W * 4)
+
+
+def commit_bytes(B, T, H, d):
+    """S0 read and S_new written (the path's k rows, u entries and gates are
+    negligible and not counted)."""
+    return 2 * B * H * d * d * 4
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = os.path.join("/tmp", f"canopy_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        self.f = open(self.out, "w")
+        self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                      "-i", str(self.gpu), "-lms", "100"], stdout=self.f,
+                                     stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.out):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.remove(self.out)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+
+def make_sets(nsets, rank, wl, bf16=True):
+    import torch
+
+    import synth
+    from gated_deltanet_linear_tree_gb300 import canopy
+    from synth import trees
+    sets = []
+    B, T, H, d = wl["B"], wl["T"], wl["H"], wl["d"]
+    for s in range(nsets):
+        inp = synth.config_inputs(wl["case"], rnd=1000 * rank + s, B=B, T=T, H=H, dk=d, dv=d)
+        dev = {}
+        for n in ("q", "k", "v"):
+            dev[n] = torch.from_numpy(inp[n]).to("cuda", torch.bfloat16 if bf16 else torch.float32)
+        for n in ("g", "beta", "S0"):
+            dev[n] = torch.from_numpy(inp[n]).cuda()
+        dev["parent"] = torch.from_numpy(inp["parent"]).cuda()
+        rng = np.random.default_rng(s)
+        acc = np.array([rng.choice(trees.leaves(inp["parent"][b])) for b in range(B)], dtype=np.int32)
+        dev["acc"] = torch.from_numpy(acc).cuda()
+        dev["ws"] = canopy.workspace(B, T, H, d)
+        dev["o"] = torch.empty((B, T, H, d), dtype=torch.float32, device="cuda")
+        dev["S_new"] = torch.empty_like(dev["S0"])
+        dev["host"] = inp
+        sets.append(dev)
+    return sets
+
+
+def step(canopy, s, T, solve="fwdsub"):
+    canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=solve,
+                  out=s["o"])
+    canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
+
+
+def set_bytes(s):
+    return sum(t.numel() * t.element_size() for k, t in s.items() if k != "host")
+
+
+def run_canopy(args, world, rank, local):
+    import torch
+
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    if rank == 0 or not os.path.exists(bld.LIB):
+        bld.build()
+    barrier(world)
+    canopy.load()
+    wl = WORKLOAD
+    B, T, H, d = wl["B"], wl["T"], wl["H"], wl["d"]
+    sets = make_sets(args.sets, rank, wl)
+    per_set = set_bytes(sets[0])
+    for i in range(args.warmup):
+        step(canopy, sets[i % len(sets)], T, args.solve)
+    torch.cuda.synchronize()
+    assert canopy.read_device_error(sets[0]["ws"]) == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        s = sets[i % len(sets)]
+        ev[i][0].record()
+        canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=args.solve,
+                      out=s["o"])
+        ev[i][1].record()
+        canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    t_verify = [e[0].elapsed_time(e[1]) for e in ev]
+    t_commit = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = max_over_ranks(total_ms, world)
+    errs = [canopy.read_device_error(s["ws"]) for s in sets]
+    assert not any(errs), errs
+
+    ms_step = total_ms / K
+    nodes = B * T * K * world
+    value = nodes / (total_ms / 1e3)
+    v_us = 1e3 * statistics.mean(t_verify)
+    c_us = 1e3 * statistics.mean(t_commit)
+    peak, peak_src = peaks()
+    vb = verify_bytes(B, T, H, d)
+    cb = commit_bytes(B, T, H, d)
+    achieved = vb / (v_us * 1e-6) / 1e9
+    tc_path = T <= 64
+    launches_per_step = (1 if tc_path else 4) + 1
+
+    e2e = run_e2e(canopy, sets, T, args, world)
+    line = {
+        "metric": METRIC, "value": value, "unit": "verified nodes/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes and distributions of the pages' "
+        "batched-verify case; no dataset or weights)",
+        "config": {"workload": wl["name"], "B": B, "T": T, "H": H, "dk": d, "dv": d, "o_dtype": "f32",
+                   "solve": args.solve, "step": "verify + commit of one accepted leaf per stream",
+                   "l2": f"inputs/outputs rotate over {len(sets)} sets of {per_set / 1e6:.1f} MB "
+                         f"({len(sets) * per_set / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_layer_verify": v_us, "us_per_commit": c_us,
+        "verify_p10_p50_p90_us": [1e3 * float(np.percentile(t_verify, p)) for p in (10, 50, 90)],
+        "roofline": {"bound": "hbm", "kernel": "verify (tensor-core fused)" if tc_path else "verify (fp32 SIMT)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
+        "roofline_commit": {"bound": "hbm", "achieved": cb / (c_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                            "frac": cb / (c_us * 1e-6) / 1e9 / peak, "algorithmic_bytes": cb},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sets[0]["host"], args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(canopy, sets, T, args, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads o and S_new back."""
+    import torch
+    K = max(10, min(args.e2e_steps, args.steps))
+    names = ("q", "k", "v", "g", "beta", "S0", "parent", "acc")
+    hosts = []
+    for s in sets[:2]:
+        hosts.append({n: s[n].cpu().pin_memory() for n in names})
+    dev = {n: torch.empty_like(sets[0][n]) for n in names}
+    ws = sets[0]["ws"]
+    o = torch.empty_like(sets[0]["o"])
+    S_new = torch.empty_like(sets[0]["S0"])
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S_new.shape, dtype=S_new.dtype).pin_memory()
+    h2d = sum(hosts[0][n].numel() * hosts[0][n].element_size() for n in names)
+    d2h = o.numel() * o.element_size() + S_new.numel() * S_new.element_size()
+
+    def one(h):
+        for n in names:
+            dev[n].copy_(h[n], non_blocking=True)
+        canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
+                      solve=args.solve, out=o)
+        canopy.commit(dev["acc"], dev["S0"], dev["k"], ws, T, out=S_new)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S_new, non_blocking=True)
+
+    for i in range(3):
+        one(hosts[i % 2])
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        one(hosts[i % 2])
+    b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    B = dev["parent"].shape[0]
+    return {"value": B * T * K * world / (ms / 1e3), "unit": "verified nodes/s", "steps": K,
+            "ms_per_step": ms / K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(inp, seconds):
+    """The fp64 oracle as it stands, on a bounded sample of the workload:
+    whole streams of the first input set, until `seconds` have passed."""
+    import oracle
+    B = inp["parent"].shape[0]
+    T = inp["parent"].shape[1]
+    t0 = time.perf_counter()
+    n = 0
+    b = 0
+    while True:
+        oracle.replay(inp["parent"][b % B], inp["q"][b % B], inp["k"][b % B], inp["v"][b % B], inp["g"][b % B],
+                      inp["beta"][b % B], inp["S0"][b % B], keep_states=False)
+        n += T
+        b += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "verified nodes/s", "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"{b} whole streams (T={T}, H={inp['q'].shape[2]}, dk=dv=128) of the "
+            f"workload, fp64 NumPy replay, single-threaded"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    wl = WORKLOAD
+    inp = synth.config_inputs(wl["case"], rnd=0)
+    B, T = inp["parent"].shape
+    t0 = time.perf_counter()
+    oracle.replay(inp["parent"][0][:8], inp["q"][0][:8], inp["k"][0][:8], inp["v"][0][:8], inp["g"][0][:8],
+                  inp["beta"][0][:8], inp["S0"][0], keep_states=False)
+    t_node = (time.perf_counter() - t0) / 8
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    m = int(max(1, min(T, budget / t_node)))
+
+    def one(i):
+        b = i % B
+        oracle.replay(inp["parent"][b][:m], inp["q"][b][:m], inp["k"][b][:m], inp["v"][b][:m], inp["g"][b][:m],
+                      inp["beta"][b][:m], inp["S0"][b], keep_states=False)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    value = m * args.steps / dt
+    sample = f"first {m} nodes of one stream's tree per step (H=16, dk=dv=128), fp64 NumPy replay"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "verified nodes/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl["name"]},
+            "cpu_baseline": {"value": value, "unit": "verified nodes/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "verified nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["canopy", "reference"], default="canopy")
+    ap.add_argument("--solve", choices=["fwdsub", "neumann"], default="fwdsub")
+    ap.add_argument("--sets", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_canopy(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+"""Thin ctypes binding of libcanopy.so (include/canopy.h).
+
+Argument marshalling only: every step of the path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch provides device memory
+and the current stream); the calls are enqueued on
+``torch.cuda.current_stream()`` and return without synchronising.  If the
+library has not been built, loading fails loudly: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcanopy.so")
+
+OK, ERR_ARG, ERR_TREE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
+F32, BF16 = 0, 1
+SOLVE = {"fwdsub": 0, "neumann": 1}
+DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+# name -> (restype, argtypes); mirrors include/canopy.h
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "canopy_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
+    "canopy_workspace_init": (_I, [_P, _S, _P]),
+    "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "canopy_commit": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
+    "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "canopy_read_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "canopy_status_string": (ctypes.c_char_p, [_I]),
+    "canopy_version": (_I, []),
+}
+
+_lib = None
+
+
+class CanopyError(RuntimeError):
+    pass
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (no CUDA call is made by loading)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise CanopyError(f"{path} is missing: build it with gated_deltanet_linear_tree_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        msg = load().canopy_status_string(status).decode()
+        raise CanopyError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise CanopyError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise CanopyError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise CanopyError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise CanopyError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise CanopyError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def workspace_bytes(B: int, T: int, H: int, d: int) -> int:
+    return int(load().canopy_workspace_bytes(B, T, H, d, d))
+
+
+def workspace(B: int, T: int, H: int, d: int, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(B, T, H, d)
+    if n == 0:
+        raise CanopyError("unsupported sizes for the workspace")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(load().canopy_workspace_init(_ptr(ws), n, _stream()), "canopy_workspace_init")
+    return ws
+
+
+def tree_prep(parent, g, ws):
+    B, T = parent.shape
+    H = g.shape[-1]
+    _need(parent, "parent", torch.int32)
+    _need(g, "g", torch.float32, (B, T, H))
+    _check(load().canopy_tree_prep(_ptr(parent), _ptr(g), T, B, H, _ptr(ws), _stream()), "canopy_tree_prep")
+
+
+def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None):
+    """o [B, T, H, dv] for every node of every stream's tree."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(q, "q")
+    _need(k, "k", q.dtype, q.shape)
+    _need(v, "v", q.dtype, (B, T, H, dv))
+    _need(g, "g", torch.float32, (B, T, H))
+    _need(beta, "beta", torch.float32, (B, T, H))
+    _need(S0, "S0", torch.float32, (B, H, dv, dk))
+    _need(parent, "parent", torch.int32, (B, T))
+    _need(ws, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    _need(out, "o", None, (B, T, H, dv))
+    st = load().canopy_tree_verify(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
+                                   _ptr(parent), T, B, H, dk, dv, SOLVE[solve], _ptr(out), _dt(out),
+                                   _ptr(ws), _stream())
+    _check(st, "canopy_tree_verify")
+    return out
+
+
+def commit(accepted, S0, k, ws, T: int, out=None):
+    """S_new [B, H, dv, dk] for the accepted node of every stream."""
+    B, H, dv, dk = S0.shape
+    _need(accepted, "accepted", torch.int32, (B,))
+    _need(S0, "S0", torch.float32)
+    _need(k, "k", None, (B, T, H, dk))
+    if out is None:
+        out = torch.empty_like(S0)
+    _need(out, "S_new", torch.float32, S0.shape)
+    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _dt(k), T, B, H, dk, dv,
+                              _ptr(ws), _stream())
+    _check(st, "canopy_commit")
+    return out
+
+
+def snapshot_bytes(B: int, T: int, H: int, d: int) -> int:
+    return int(load().canopy_snapshot_bytes(B, T, H, d, d))
+
+
+def serial_replay(q, k, v, g, beta, S0, parent, ws, snapshot=None, o_dtype=torch.float32, out=None):
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(q, "q")
+    _need(k, "k", q.dtype, q.shape)
+    _need(v, "v", q.dtype, (B, T, H, dv))
+    _need(g, "g", torch.float32, (B, T, H))
+    _need(beta, "beta", torch.float32, (B, T, H))
+    _need(S0, "S0", torch.float32, (B, H, dv, dk))
+    _need(parent, "parent", torch.int32, (B, T))
+    if snapshot is None:
+        snapshot = torch.empty(snapshot_bytes(B, T, H, dk), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    st = load().canopy_serial_replay(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
+                                     _ptr(parent), T, B, H, dk, dv, _ptr(out), _dt(out), _ptr(snapshot),
+                                     _ptr(ws), _stream())
+    _check(st, "canopy_serial_replay")
+    return out
+
+
+def read_device_error(ws) -> int:
+    """Synchronise the current stream, return and clear the device error word."""
+    err = ctypes.c_int32(0)
+    _check(load().canopy_read_device_error(_ptr(ws), ctypes.byref(err), _stream()), "canopy_read_device_error")
+    return int(err.value)

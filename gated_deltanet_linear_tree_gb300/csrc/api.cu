@@ -1,0 +1,151 @@
+// extern "C" entry points of libcanopy.so: argument checks, workspace
+// binding and kernel dispatch.  See include/canopy.h for the contract.
+#include <stdlib.h>
+
+#include "common.cuh"
+
+namespace canopy {
+cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
+                             cudaStream_t st);
+cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
+                             const Ws& ws, int bv, cudaStream_t st);
+cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
+                               const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
+                               cudaStream_t st);
+cudaError_t launch_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k, int in_bf16,
+                          int T, int B, int H, int d, const Ws& ws, cudaStream_t st);
+cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
+                          const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int d,
+                          void* o, int o_bf16, float* snap, int32_t* err, cudaStream_t st);
+}  // namespace canopy
+
+using namespace canopy;
+
+namespace {
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool sizes_ok(int B, int T, int H) { return B >= 1 && H >= 1 && T >= 1 && T <= kMaxT; }
+
+canopy_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CANOPY_OK : CANOPY_ERR_CUDA; }
+
+// Value-tile width of the tensor-core verify: 32 unless CANOPY_TC_BV=64.
+int tc_tile() {
+    static int bv = -1;
+    if (bv < 0) {
+        const char* s = getenv("CANOPY_TC_BV");
+        bv = (s && atoi(s) == 64) ? 64 : 32;
+    }
+    return bv;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t canopy_workspace_bytes(int B, int T, int H, int dk, int dv) {
+    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return 0;
+    return ws_layout(B, T, H, dv).total;
+}
+
+canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (!aligned16(workspace) || bytes == 0) return CANOPY_ERR_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+size_t canopy_snapshot_bytes(int B, int T, int H, int dk, int dv) {
+    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return 0;
+    return size_t(B) * T * H * dv * dk * 4;
+}
+
+canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, void* workspace,
+                               void* stream) {
+    if (!aligned16(parent) || !aligned16(g) || !aligned16(workspace)) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, H)) return CANOPY_ERR_UNSUPPORTED;
+    Ws ws = ws_bind(workspace, B, T, H, 128);
+    return cuda_status(launch_tree_prep(parent, g, T, B, H, ws, static_cast<cudaStream_t>(stream)));
+}
+
+canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
+                                 const float* g, const float* beta, const float* S0, const int32_t* parent, int T,
+                                 int B, int H, int dk, int dv, canopy_solve solve, void* o, canopy_dtype o_dtype,
+                                 void* workspace, void* stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
+        !aligned16(parent) || !aligned16(o) || !aligned16(workspace))
+        return CANOPY_ERR_ARG;
+    if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
+        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN))
+        return CANOPY_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws ws = ws_bind(workspace, B, T, H, dv);
+    const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
+    const bool tc = in_bf16 && dk == 128 && T <= 64;
+    if (solve == CANOPY_SOLVE_NEUMANN) {
+        return CANOPY_ERR_UNSUPPORTED;
+    }
+    if (tc) return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, tc_tile(), st));
+    cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, st);
+    if (e != cudaSuccess) return CANOPY_ERR_CUDA;
+    return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, st));
+}
+
+canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,
+                            canopy_dtype in_dtype, int T, int B, int H, int dk, int dv, const void* workspace,
+                            void* stream) {
+    if (!aligned16(accepted) || !aligned16(S0) || !aligned16(S_new) || !aligned16(k) || !aligned16(workspace))
+        return CANOPY_ERR_ARG;
+    if (in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) return CANOPY_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    Ws ws = ws_bind(const_cast<void*>(workspace), B, T, H, dv);
+    return cuda_status(launch_commit(accepted, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, H, dk, ws,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
+                                   const float* g, const float* beta, const float* S0, const int32_t* parent, int T,
+                                   int B, int H, int dk, int dv, void* o, canopy_dtype o_dtype, void* snapshot,
+                                   void* workspace, void* stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
+        !aligned16(parent) || !aligned16(o) || !aligned16(snapshot) || !aligned16(workspace))
+        return CANOPY_ERR_ARG;
+    if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16))
+        return CANOPY_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    Ws ws = ws_bind(workspace, B, T, H, dv);
+    return cuda_status(launch_serial(q, k, v, in_dtype == CANOPY_BF16, g, beta, S0, parent, T, B, H, dk, o,
+                                     o_dtype == CANOPY_BF16, static_cast<float*>(snapshot), ws.err,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+canopy_status canopy_read_device_error(void* workspace, int32_t* err_out, void* stream) {
+    if (!aligned16(workspace) || !err_out) return CANOPY_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* dev = static_cast<int32_t*>(workspace);  // the error word is the workspace's first word
+    int32_t host = 0;
+    if (cudaMemcpyAsync(&host, dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return CANOPY_ERR_CUDA;
+    if (cudaMemsetAsync(dev, 0, sizeof(int32_t), st) != cudaSuccess) return CANOPY_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CANOPY_ERR_CUDA;
+    *err_out = host;
+    return CANOPY_OK;
+}
+
+const char* canopy_status_string(canopy_status s) {
+    switch (s) {
+        case CANOPY_OK: return "ok";
+        case CANOPY_ERR_ARG: return "invalid argument";
+        case CANOPY_ERR_TREE: return "invalid tree";
+        case CANOPY_ERR_UNSUPPORTED: return "unsupported size or combination";
+        case CANOPY_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+int canopy_version(void) { return (0 << 16) | 1; }
+
+}  // extern "C"

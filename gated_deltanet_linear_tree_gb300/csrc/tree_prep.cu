@@ -1,0 +1,98 @@
+// Tree preparation kernel: parent array -> validation, depth, strict-ancestor
+// bitmask, DFS pre-order, and cumulative log gates l for every head.
+//
+// canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed form"
+// (A(i), path(i), depth, l_i = log alpha_i + l_parent(i)) and "Design
+// decisions" (DFS pre-order keeps subtrees contiguous; a T x T bitmask).
+// One CTA of 256 threads per stream; T <= 256.
+#include "common.cuh"
+
+namespace canopy {
+
+namespace prep {
+
+__global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restrict__ parent,
+                                                        const float* __restrict__ g, int T, int H, Ws ws) {
+    __shared__ int sPtr[kMaxT];
+    __shared__ int sLen[kMaxT];
+    __shared__ int sPar[kMaxT];
+    __shared__ float sS[kMaxT];
+    __shared__ uint64_t sM[kMaxT * 4];
+    __shared__ int sSize[kMaxT];
+    __shared__ int sPos[kMaxT];
+    const int b = blockIdx.x, i = threadIdx.x;
+    int bad = 0;
+    if (i < T) {
+        int par = parent[size_t(b) * T + i];
+        const bool ok = (i == 0) ? (par == -1) : (par >= 0 && par < i);
+        if (!ok) {
+            bad |= CANOPY_DEVERR_TREE;
+            par = (i == 0) ? -1 : 0;
+        }
+        sPtr[i] = par;
+        sPar[i] = par;
+        sS[i] = 0.f;
+    }
+    if (bad) raise_err(ws.err, bad);
+    __syncthreads();
+    jump_paths<4>(T, sPtr, sLen, sS, sM);
+
+    // depth and strict-ancestor mask
+    if (i < T) {
+        ws.depth[size_t(b) * T + i] = sLen[i] - 1;
+        for (int w = 0; w < ws.W; ++w) {
+            uint64_t word = sM[i * 4 + (w >> 1)];
+            if ((w >> 1) == (i >> 6)) word &= ~(1ull << (i & 63));
+            ws.mask[(size_t(b) * T + i) * ws.W + w] = uint32_t(word >> (32 * (w & 1)));
+        }
+    }
+
+    // cumulative log gates, summed root first along each path, every head
+    int badg = 0;
+    for (int e = i; e < T * H; e += blockDim.x) {
+        const int n = e / H, hh = e % H;
+        float s = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            uint64_t bits = sM[n * 4 + w];
+            while (bits) {
+                const int j = 64 * w + __ffsll(static_cast<long long>(bits)) - 1;
+                bits &= bits - 1;
+                float a = g[(size_t(b) * T + j) * H + hh];
+                if (!(a > 0.f) || !isfinite(a)) {
+                    badg = CANOPY_DEVERR_GATE;
+                    a = 1.f;
+                }
+                s += logf(a);
+            }
+        }
+        ws.l[(size_t(b) * T + n) * H + hh] = s;
+    }
+    if (badg) raise_err(ws.err, badg);
+
+    // DFS pre-order (children in index order): subtree sizes bottom-up, then
+    // each child takes the next free slot after its parent.
+    __syncthreads();
+    if (i == 0) {
+        for (int n = 0; n < T; ++n) sSize[n] = 1;
+        for (int n = T - 1; n >= 1; --n) sSize[sPar[n]] += sSize[n];
+        sPos[0] = 0;
+        for (int n = 0; n < T; ++n) sLen[n] = 1;  // reuse: next free offset below n
+        for (int n = 1; n < T; ++n) {
+            const int pn = sPar[n];
+            sPos[n] = sPos[pn] + sLen[pn];
+            sLen[pn] += sSize[n];
+        }
+    }
+    __syncthreads();
+    if (i < T) ws.order[size_t(b) * T + sPos[i]] = i;
+}
+
+}  // namespace prep
+
+cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
+                             cudaStream_t st) {
+    prep::tree_prep_kernel<<<B, 256, 0, st>>>(parent, g, T, H, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace canopy

@@ -1,0 +1,507 @@
+// Closed-form tree verify on tcgen05 tensor cores (bf16 q/k/v, fp32 S0,
+// fp32 accumulation in tensor memory), one 64-node block (T <= 64).
+//
+// Method: canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed
+// form" (Bole's Theorem 1).  One CTA owns (stream b, head h, value tile of BV
+// columns of the d_v x d_k state) and, for all T nodes:
+//   1. tree prep: parent -> path bitmask, depth, l_i = sum log alpha (log2
+//      units inside), by pointer jumping (common.cuh);
+//   2. X  = [Q;K] S0_tile^T   on tcgen05 (M = 128 rows = Q rows then K rows,
+//      N = BV, K = dk); S0 is split into bf16 hi + lo parts in shared memory
+//      so the product keeps ~16 mantissa bits of the fp32 state;
+//      AC = [Q;K] K^T         on tcgen05 (N = 64): rows 0..63 give Q K^T,
+//      rows 64..127 give K K^T;
+//   3. epilogue (one thread per TMEM lane): C_ij = [j in path(i)]
+//      2^(l2_i - l2_j) q_i.k_j written back to TMEM as tf32 (the A operand of
+//      step 5); gamma_i X_Q,i written back in place; G_ij = beta_i
+//      2^(l2_i - l2_j) k_i.k_j for j in A(i) and R_i = beta_i (v_i -
+//      gamma_i X_K,i) into shared memory;
+//   4. forward substitution (I + G) U = R, one thread per value column,
+//      right-looking, in fp32 registers; U goes to the workspace (for commit)
+//      and, as tf32, to shared memory as the B operand of step 5;
+//   5. O = gamma Q S0^T + C U: one tcgen05 tf32 MMA with A = C read from
+//      tensor memory, accumulated onto the gamma-scaled X_Q columns;
+//   6. o rows are read back from TMEM and stored.
+// Decay ratios are only ever 2^(l2_i - l2_j) with j on i's root path, so they
+// lie in (0, 1] and never overflow ("Hard constraints", log-space gates).
+#include "common.cuh"
+
+namespace canopy {
+
+namespace tc {
+
+constexpr int DK = 128;
+constexpr int DV = 128;
+constexpr int TP = 64;  // nodes per block
+
+template <int BV>
+struct Smem {
+    static constexpr int QK = 0;                    // [Q;K] bf16: 2 atoms x 128 rows x 128 B
+    static constexpr int S_ATOM = BV * 128;         // one 64-column bf16 atom of the S0 tile
+    static constexpr int S_PLANE = 2 * S_ATOM;      // hi or lo plane
+    static constexpr int S = 32768;                 // S0 hi then lo
+    static constexpr int SMALL = S + 2 * S_PLANE;
+    // reused once the first MMAs are done:
+    static constexpr int GT = 0;                    // G^T fp32 [64][64]
+    static constexpr int RT = 16384;                // R^T fp32 [BV][64], 16-byte chunks swizzled
+    static constexpr int UT = S;                    // U^T tf32 as a K-major SW128 operand [BV][64]
+    // small arrays
+    static constexpr int PAR = SMALL;               // int[64]   jump pointer
+    static constexpr int LEN = PAR + 256;           // int[64]   path length
+    static constexpr int L2 = LEN + 256;            // float[64] cumulative log2 gate
+    static constexpr int GAM = L2 + 256;            // float[64] gamma = 2^l2
+    static constexpr int BETA = GAM + 256;          // float[64]
+    static constexpr int MASK = BETA + 256;         // u64[64]   path(i) incl. i
+    static constexpr int BAR = MASK + 512;          // u64[2]
+    static constexpr int TMEMSLOT = BAR + 16;       // u32
+    static constexpr int FLAG = TMEMSLOT + 4;       // int
+    static constexpr int TOTAL = FLAG + 12;
+    static_assert(RT + BV * 64 * 4 <= S, "R^T must fit in the Q/K region");
+    static_assert(BV * 256 <= 2 * S_PLANE, "U^T must fit in the S0 region");
+};
+
+constexpr uint32_t kTmemCols = 128;  // X: [0, BV), AC: [BV, BV + 64)
+
+struct Params {
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    const float* S0;
+    const int32_t* parent;
+    void* o;
+    float* U;
+    float* l;
+    int32_t* depth;
+    uint32_t* mask;
+    int32_t* err;
+    int B, T, H, W, o_bf16;
+};
+
+__device__ inline float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ inline float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int BV>
+__global__ void __launch_bounds__(128, 4)
+    verify_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, Params p) {
+    using L = Smem<BV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    int* sPtr = reinterpret_cast<int*>(sm + L::PAR);
+    int* sLen = reinterpret_cast<int*>(sm + L::LEN);
+    float* sL2 = reinterpret_cast<float*>(sm + L::L2);
+    float* sGam = reinterpret_cast<float*>(sm + L::GAM);
+    float* sBeta = reinterpret_cast<float*>(sm + L::BETA);
+    uint64_t* sMask = reinterpret_cast<uint64_t*>(sm + L::MASK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
+    int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int T = p.T, H = p.H;
+    const int v0 = vt * BV;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        *sFlag = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(sTmem, kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+
+    // S0 value tile: BV rows x 128 fp32, contiguous; 16-byte coalesced loads.
+    constexpr int NS = BV / 4;
+    float4 s0r[NS];
+    {
+        const float4* src = reinterpret_cast<const float4*>(p.S0 + ((size_t(b) * H + h) * DV + v0) * DK);
+#pragma unroll
+        for (int u = 0; u < NS; ++u) s0r[u] = __ldg(src + u * 128 + tid);
+    }
+    // Parents and gates; padded nodes get no path, beta = 0 and gamma = 1.
+    uint32_t vw[BV / 2];
+    int bad = 0;
+    if (tid < TP) {
+        const int i = tid;
+        int par = -1;
+        float a = 1.f, be = 0.f;
+        if (i < T) {
+            par = p.parent[size_t(b) * T + i];
+            a = p.g[(size_t(b) * T + i) * H + h];
+            be = p.beta[(size_t(b) * T + i) * H + h];
+            const bool ok_par = (i == 0) ? (par == -1) : (par >= 0 && par < i);
+            if (!ok_par) {
+                bad |= CANOPY_DEVERR_TREE;
+                par = (i == 0) ? -1 : 0;
+            }
+            if (!gate_ok(a, be)) {
+                bad |= CANOPY_DEVERR_GATE;
+                a = 1.f;
+                be = 0.f;
+            }
+        }
+        sPtr[i] = par;
+        sL2[i] = (i < T) ? log2f(a) : 0.f;
+        sBeta[i] = be;
+    }
+    if (bad) raise_err(p.err, bad);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sTmem;
+
+    uint8_t* sQK = sm + L::QK;
+    if (tid == 0) {
+        mbar_expect_tx(&bars[0], 4 * 64 * 64 * 2);
+        tma_load_4d(sQK + 0, &tmQ, &bars[0], 0, h, 0, b);
+        tma_load_4d(sQK + 16384, &tmQ, &bars[0], 64, h, 0, b);
+        tma_load_4d(sQK + 8192, &tmK, &bars[0], 0, h, 0, b);
+        tma_load_4d(sQK + 24576, &tmK, &bars[0], 64, h, 0, b);
+    }
+
+    // Tree prep (threads 0..63 own nodes; the whole CTA takes the barriers).
+    jump_paths<1>(TP, sPtr, sLen, sL2, sMask);
+    if (tid < TP) {
+        const int i = tid;
+        if (i >= T) sMask[i] = 0ull;  // padded nodes: empty path
+        sGam[i] = exp2f(sL2[i]);
+        if (i < T) {
+            if (vt == 0) p.l[(size_t(b) * T + i) * H + h] = sL2[i] * 0.69314718055994531f;
+            if (vt == 0 && h == 0) {
+                p.depth[size_t(b) * T + i] = sLen[i] - 1;
+                const uint64_t strict = sMask[i] & ~(1ull << i);
+                for (int w = 0; w < p.W; ++w)
+                    p.mask[(size_t(b) * T + i) * p.W + w] = uint32_t(strict >> (32 * w));
+            }
+        }
+    }
+
+    // S0 tile -> bf16 hi and lo planes, K-major with the 128-byte swizzle.
+    {
+        uint8_t* sS = sm + L::S;
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            const int f = u * 128 + tid;
+            const int r = f >> 5, c4 = f & 31;
+            const int atom = c4 >> 4, chunk = (c4 & 15) >> 1;
+            const int off = atom * L::S_ATOM + r * 128 + ((chunk ^ (r & 7)) << 4) + ((c4 & 1) << 3);
+            const float x[4] = {s0r[u].x, s0r[u].y, s0r[u].z, s0r[u].w};
+            uint32_t hb[4], lb[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x[e]);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(x[e] - __bfloat162float(hi));
+                hb[e] = __bfloat16_as_ushort(hi);
+                lb[e] = __bfloat16_as_ushort(lo);
+            }
+            *reinterpret_cast<uint2*>(sS + off) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+            *reinterpret_cast<uint2*>(sS + L::S_PLANE + off) =
+                make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+        }
+    }
+    // V rows for the K-row threads (lane 64 + i holds node i): BV bf16;
+    // issued here so their latency overlaps the first MMAs.
+    {
+        const int i = tid - 64;
+        if (tid >= 64 && i < T) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.v + ((size_t(b) * T + i) * H + h) * DV + v0);
+#pragma unroll
+            for (int u = 0; u < BV / 8; ++u) {
+                uint4 x = __ldg(src + u);
+                vw[4 * u] = x.x;
+                vw[4 * u + 1] = x.y;
+                vw[4 * u + 2] = x.z;
+                vw[4 * u + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < BV / 2; ++u) vw[u] = 0;
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // First MMAs: X = [Q;K] (S0hi + S0lo)^T and AC = [Q;K] K^T.
+    if (tid == 0) {
+        if (!mbar_wait(&bars[0], 0)) {
+            *sFlag = 1;
+        } else {
+            tc_fence_after();
+            const uint32_t aQK = smem_u32(sQK);
+            const uint32_t aS = smem_u32(sm + L::S);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
+                    const uint64_t db = sdesc_sw128(aS + part * L::S_PLANE + (ks >> 2) * L::S_ATOM + (ks & 3) * 32);
+                    mma_bf16_ss(tmem, da, db, idesc_bf16(128, BV), (part | ks) != 0);
+                }
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
+                const uint64_t db = sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32);
+                mma_bf16_ss(tmem + BV, da, db, idesc_bf16(128, 64), ks != 0);
+            }
+            mma_commit(&bars[1]);
+        }
+    }
+    __syncthreads();
+    bool ok = (*sFlag == 0) && mbar_wait(&bars[1], 0);
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        if (tid == 0) {
+            raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
+            mbar_wait(&bars[0], 0);  // let copies in flight land before leaving
+        }
+        goto teardown;
+    }
+    tc_fence_after();
+
+    {
+        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+        float* sGt = reinterpret_cast<float*>(sm + L::GT);
+        float* sRt = reinterpret_cast<float*>(sm + L::RT);
+        if (warp < 2) {
+            // Q rows: C into TMEM (tf32), gamma-scaled X_Q in place.
+            const int i = tid;
+            const float li = sL2[i], gi = sGam[i];
+            const uint64_t m = sMask[i];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + BV + cb * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = cb * 16 + jj;
+                    const float c = ((m >> j) & 1ull) ? __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
+                    r[jj] = to_tf32(c);
+                }
+                tmem_st16(lane_base + BV + cb * 16, r);
+            }
+#pragma unroll
+            for (int cb = 0; cb < BV / 16; ++cb) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + cb * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) r[jj] = __float_as_uint(gi * __uint_as_float(r[jj]));
+                tmem_st16(lane_base + cb * 16, r);
+            }
+            tmem_wait_st();
+        } else {
+            // K rows: G^T and R^T into shared memory.
+            const int i = tid - 64;
+            const float li = sL2[i], bi = sBeta[i], gi = sGam[i];
+            const uint64_t ms = sMask[i] & ~(1ull << i);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + BV + cb * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = cb * 16 + jj;
+                    sGt[j * 64 + i] = ((ms >> j) & 1ull) ? bi * __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int cb = 0; cb < BV / 16; ++cb) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + cb * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int c = cb * 16 + jj;
+                    const float vv = (c & 1) ? bf16_hi(vw[c >> 1]) : bf16_lo(vw[c >> 1]);
+                    const float rr = bi * (vv - gi * __uint_as_float(r[jj]));
+                    sRt[c * 64 + ((((i >> 2) ^ (c & 15))) << 2) + (i & 3)] = rr;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // Forward substitution, one thread per value column.
+    if (tid < BV) {
+        const int c = tid;
+        const float* sGt = reinterpret_cast<const float*>(sm + L::GT);
+        const float* sRt = reinterpret_cast<const float*>(sm + L::RT);
+        uint8_t* sUt = sm + L::UT;
+        float acc[TP];
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+            const float4 x = *reinterpret_cast<const float4*>(sRt + c * 64 + ((ch ^ (c & 15)) << 2));
+            acc[4 * ch] = x.x;
+            acc[4 * ch + 1] = x.y;
+            acc[4 * ch + 2] = x.z;
+            acc[4 * ch + 3] = x.w;
+        }
+        const int Tp = (T + 15) & ~15;
+        float* Ucol = p.U + (size_t(b) * T * H + h) * DV + v0 + c;
+        uint32_t u4[4];
+#pragma unroll
+        for (int j = 0; j < TP; ++j) {
+            const float u = acc[j];
+            if (j < T) Ucol[size_t(j) * H * DV] = u;
+            u4[j & 3] = to_tf32(u);
+            if ((j & 3) == 3) {
+                const int atom = j >> 5, chunk = (j & 31) >> 2;
+                *reinterpret_cast<uint4*>(sUt + atom * (BV * 128) + c * 128 + ((chunk ^ (c & 7)) << 4)) =
+                    make_uint4(u4[0], u4[1], u4[2], u4[3]);
+            }
+            if (j + 1 < Tp) {
+#pragma unroll
+                for (int i4 = (j + 1) >> 2; i4 < TP / 4; ++i4) {
+                    if (i4 * 4 < Tp) {
+                        const float4 gg = *reinterpret_cast<const float4*>(sGt + j * 64 + i4 * 4);
+                        if (i4 * 4 + 0 > j) acc[i4 * 4 + 0] -= gg.x * u;
+                        if (i4 * 4 + 1 > j) acc[i4 * 4 + 1] -= gg.y * u;
+                        if (i4 * 4 + 2 > j) acc[i4 * 4 + 2] -= gg.z * u;
+                        if (i4 * 4 + 3 > j) acc[i4 * 4 + 3] -= gg.w * u;
+                    }
+                }
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // O = gamma X_Q + C U on the tensor cores (A = C from TMEM, B = U^T).
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t aU = smem_u32(sm + L::UT);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t db = sdesc_sw128(aU + (ks >> 2) * (BV * 128) + (ks & 3) * 32);
+            mma_tf32_ts(tmem, tmem + BV + ks * 8, db, idesc_tf32(128, BV), 1);
+        }
+        mma_commit(&bars[1]);
+    }
+    ok = mbar_wait(&bars[1], 1);
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        if (tid == 0) raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
+        goto teardown;
+    }
+    tc_fence_after();
+
+    if (warp < 2 && tid < T) {
+        const int i = tid;
+        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+        const size_t obase = ((size_t(b) * T + i) * H + h) * DV + v0;
+#pragma unroll
+        for (int cb = 0; cb < BV / 16; ++cb) {
+            uint32_t r[16];
+            tmem_ld16(lane_base + cb * 16, r);
+            tmem_wait_ld();
+            if (p.o_bf16) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const __nv_bfloat162 pr =
+                        __floats2bfloat162_rn(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                    w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + obase + cb * 16);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + obase + cb * 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                         __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            }
+        }
+    }
+
+teardown:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [B][T][H][128] bf16 -> boxes of 64 (dk) x 64 (nodes) with the 128-byte swizzle.
+static bool make_qk_map(CUtensorMap* m, const void* base, int B, int T, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {128, cuuint64_t(H), cuuint64_t(T), cuuint64_t(B)};
+    const cuuint64_t strides[3] = {128 * 2, cuuint64_t(H) * 128 * 2, cuuint64_t(T) * H * 128 * 2};
+    const cuuint32_t box[4] = {64, 1, 64, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BV>
+static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
+    CUtensorMap mq, mk;
+    if (!make_qk_map(&mq, q, prm.B, prm.T, prm.H) || !make_qk_map(&mk, k, prm.B, prm.T, prm.H))
+        return cudaErrorInvalidValue;
+    const int smem = tc::Smem<BV>::TOTAL + 1024;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc::verify_kernel<BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid(tc::DV / BV, prm.H, prm.B);
+    tc::verify_kernel<BV><<<grid, 128, smem, st>>>(mq, mk, prm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
+                             const Ws& ws, int bv, cudaStream_t st) {
+    tc::Params prm;
+    prm.v = static_cast<const __nv_bfloat16*>(v);
+    prm.g = g;
+    prm.beta = beta;
+    prm.S0 = S0;
+    prm.parent = parent;
+    prm.o = o;
+    prm.U = ws.U;
+    prm.l = ws.l;
+    prm.depth = ws.depth;
+    prm.mask = ws.mask;
+    prm.err = ws.err;
+    prm.B = B;
+    prm.T = T;
+    prm.H = H;
+    prm.W = ws.W;
+    prm.o_bf16 = o_bf16;
+    if (bv == 64) return launch_tc<64>(q, k, prm, st);
+    return launch_tc<32>(q, k, prm, st);
+}
+
+}  // namespace canopy

@@ -1,0 +1,149 @@
+/*
+ * canopy: closed-form tree verification for Gated DeltaNet layers on one
+ * NVIDIA GB300 (sm_103a).  C ABI of libcanopy.so.
+ *
+ * The method (canopy page, projects.dotslasha.me/p/canopy.md, "The tree
+ * closed form", which states Bole's Theorem 1): a draft tree of T nodes per
+ * stream, given as a parent array in any topological order, is verified by
+ * one ancestor-masked, decay-weighted unit-lower-triangular solve instead of
+ * forking a d_v x d_k state per branch; afterwards only the accepted node's
+ * state is rebuilt (commit).  In this library's orientation the state is
+ * S[dv][dk] and the rule ("The gated delta rule", TreeWY's form) is
+ *     S_i = g_i * S_parent(i) * (I - beta_i k_i k_i^T) + beta_i v_i k_i^T
+ *     o_i = S_i q_i                     (S_parent(0) = S0, no scale on q)
+ * with g_i the decay gate alpha_i in (0, 1].
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers; the caller owns and
+ *     allocates every buffer.  The library never allocates, frees or
+ *     synchronises inside a compute call; work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - All arrays are dense, row-major, with the last index fastest:
+ *       q, k     [B][T][H][dk]   bf16 or fp32 (in_dtype)
+ *       v        [B][T][H][dv]   bf16 or fp32 (in_dtype)
+ *       g, beta  [B][T][H]       fp32 (g = decay gate alpha, linear space)
+ *       S0       [B][H][dv][dk]  fp32
+ *       parent   [B][T]          int32, parent[b][0] = -1, 0 <= parent[b][i] < i
+ *       o        [B][T][H][dv]   fp32 or bf16 (o_dtype)
+ *   - Device pointers must be 16-byte aligned (vector and TMA loads).
+ *   - Argument errors are detected on the host and returned before anything
+ *     is enqueued.  Errors that depend on device data (a malformed tree, a
+ *     gate <= 0 or not finite, an accepted node out of range, an internal
+ *     wait that timed out) set bits in a sticky device error word inside the
+ *     workspace; the outputs of that call are then undefined.  Read and clear
+ *     the word with canopy_read_device_error().  No kernel traps or asserts.
+ *   - Sizes supported: 1 <= T <= 256, B >= 1, H >= 1, dk = dv = 128 for every
+ *     entry point; dk = dv = 32 additionally for the fp32 (tier A) and serial
+ *     paths.  Other values return CANOPY_ERR_UNSUPPORTED.
+ */
+#ifndef CANOPY_H
+#define CANOPY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CANOPY_OK = 0,
+    CANOPY_ERR_ARG = 1,          /* null/misaligned pointer, bad enum, B/H/T <= 0   */
+    CANOPY_ERR_TREE = 2,         /* reserved for host-side tree checks              */
+    CANOPY_ERR_UNSUPPORTED = 3,  /* a size or combination this build does not have  */
+    CANOPY_ERR_CUDA = 4          /* a CUDA runtime call failed (launch, copy, ...)  */
+} canopy_status;
+
+typedef enum { CANOPY_F32 = 0, CANOPY_BF16 = 1 } canopy_dtype;
+
+/* Solve strategy for (I + diag(beta) A) U = R (canopy page, "Design
+ * decisions", two solve strategies behind one interface). */
+typedef enum {
+    CANOPY_SOLVE_FWDSUB = 0,   /* blocked forward substitution, 64-node blocks   */
+    CANOPY_SOLVE_NEUMANN = 1   /* finite Neumann series, d rounds (Bole's solve) */
+} canopy_solve;
+
+/* Bits of the device error word. */
+#define CANOPY_DEVERR_TREE     0x1  /* parent[b][0] != -1 or parent[b][i] not in [0,i) */
+#define CANOPY_DEVERR_GATE     0x2  /* g <= 0, g or beta not finite                     */
+#define CANOPY_DEVERR_ACCEPTED 0x4  /* commit: accepted node not in [-1, T)             */
+#define CANOPY_DEVERR_TIMEOUT  0x8  /* an internal bounded wait gave up                 */
+
+/* Size in bytes of the workspace one verify/commit pair needs.  It holds the
+ * pseudo-values U fp32 [B][T][H][dv], the cumulative log gates
+ * l fp32 [B][T][H] (l_i = sum of log g over path(i)), node depths int32
+ * [B][T], the strict-ancestor bitmask uint32 [B][T][ceil(T/32)], the DFS
+ * pre-order int32 [B][T], the device error word, and the scratch of the fp32
+ * path.  Returns 0 for unsupported sizes. */
+size_t canopy_workspace_bytes(int B, int T, int H, int dk, int dv);
+
+/* Zero the workspace (including the error word); call once after allocating
+ * it.  Enqueued on `stream`. */
+canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Tree preparation (canopy page, "The tree closed form" and "Design
+ * decisions", tree order and tiling): validates every parent array and
+ * writes depth, the strict-ancestor bitmask, the DFS pre-order and the
+ * cumulative log gates l into the workspace.  The verify entry point does the
+ * same work inside its own kernels; this call exposes it on its own.
+ *   parent device int32 [B][T]; g device fp32 [B][T][H]. */
+canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
+                               int T, int B, int H, void* workspace, void* stream);
+
+/* Closed-form tree verify (canopy page, "The tree closed form"):
+ *   A_ij = [j in A(i)] exp(l_i - l_j) k_i.k_j,  C_ij = [j in path(i)] exp(l_i - l_j) q_i.k_j
+ *   (I + diag(beta) A) U = diag(beta) (V - diag(gamma) K S0^T),  gamma_i = exp(l_i)
+ *   O = diag(gamma) Q S0^T + C U
+ * Writes o (device, o_dtype) and, into the workspace, U, l, depth, mask.
+ * in_dtype CANOPY_BF16 selects the tensor-core path (tcgen05, bf16 operands,
+ * fp32 accumulation); CANOPY_F32 selects the fp32 path.  S0 is read only. */
+canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
+                                 const float* g, const float* beta, const float* S0,
+                                 const int32_t* parent, int T, int B, int H, int dk, int dv,
+                                 canopy_solve solve, void* o, canopy_dtype o_dtype,
+                                 void* workspace, void* stream);
+
+/* Commit (canopy page, "The tree closed form", last line, and "What the
+ * commit kernel stores"): for every stream b with accepted node a = accepted[b],
+ *   S_new = gamma_a S0 + sum_{j in path(a)} exp(l_a - l_j) u_j k_j^T      (fp32)
+ * using U, l and the ancestor mask that the preceding verify call left in
+ * the workspace (same parent, g and T).  a = -1 means nothing accepted:
+ * S_new = S0.  S_new may alias S0 (the update is elementwise in S0).
+ *   accepted device int32 [B]; S0, S_new device fp32 [B][H][dv][dk];
+ *   k device [B][T][H][dk] in in_dtype (the verify call's k). */
+canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new,
+                            const void* k, canopy_dtype in_dtype, int T, int B, int H,
+                            int dk, int dv, const void* workspace, void* stream);
+
+/* Bytes of the per-node snapshot buffer of the serial replay:
+ * fp32 [B][T][H][dv][dk]. */
+size_t canopy_snapshot_bytes(int B, int T, int H, int dk, int dv);
+
+/* Serial parent-pointer replay, the crossover opponent (canopy page,
+ * "Design decisions", serial baseline: SGLang's snapshot path).  For each
+ * node in index order it takes the parent's state (S0 for the root) from the
+ * snapshot buffer, applies one step of the rule in fp32, writes the node's
+ * snapshot when a later node other than i+1 will read it, and writes o_i.
+ * Same inputs and output as canopy_tree_verify; snapshot is device memory of
+ * canopy_snapshot_bytes(); workspace receives only the error word. */
+canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
+                                   const float* g, const float* beta, const float* S0,
+                                   const int32_t* parent, int T, int B, int H, int dk, int dv,
+                                   void* o, canopy_dtype o_dtype, void* snapshot,
+                                   void* workspace, void* stream);
+
+/* Synchronise `stream`, copy the device error word to *err_out and clear it.
+ * Returns CANOPY_ERR_CUDA if the stream reported an error. */
+canopy_status canopy_read_device_error(void* workspace, int32_t* err_out, void* stream);
+
+/* Human-readable name of a status. */
+const char* canopy_status_string(canopy_status s);
+
+/* Version of this library as (major << 16) | minor. */
+int canopy_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CANOPY_H */

@@ -31,8 +31,9 @@ def replay(parent, q, k, v, alpha, beta, S0, keep_states: bool = True):
     S0 = np.asarray(S0, np.float64)
     T, H, dk = q.shape
     dv = v.shape[-1]
-    needed = np.zeros(T, dtype=bool)
-    needed[p[1:]] = True
+    last_child = np.full(T, -1)
+    for i in range(1, T):
+        last_child[p[i]] = i
     states = {}
     S_all = np.empty((T, H, dv, dk)) if keep_states else None
     o = np.empty((T, H, dv))
@@ -44,8 +45,10 @@ def replay(parent, q, k, v, alpha, beta, S0, keep_states: bool = True):
         Si = ai * (Sp - bi * Spk[:, :, None] * k[i][:, None, :]) \
             + bi * v[i][:, :, None] * k[i][:, None, :]
         o[i] = np.einsum("hvd,hd->hv", Si, q[i])                 # S_i q_i
-        if needed[i]:
-            states[i] = Si
+        if last_child[i] >= 0:
+            states[i] = Si                       # kept until its last child is done
+        if p[i] >= 0 and last_child[p[i]] == i:
+            del states[p[i]]
         if keep_states:
             S_all[i] = Si
     return o, S_all

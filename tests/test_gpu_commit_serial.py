@@ -1,0 +1,158 @@
+"""GPU parity for commit and the serial replay, device error reporting, and the
+verify/commit round trip (canopy page, "M5: Commit kernel and the full
+round")."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import trees
+from tests.gpu_helpers import TOL_BF16, TOL_F32, oracle_outputs, rel_err, run_verify, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(T, fam, B=3, H=4, d=128, bf16=True, seed=0):
+    rng = np.random.default_rng(seed + 31 * T)
+    parents = [trees.family(fam, T, rng) for _ in range(B)]
+    return synth.make_inputs(parents, H, d, d, bf16, case=91, rnd=seed)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("T,fam", [(16, "top4"), (64, "random"), (64, "chain"), (100, "random"),
+                                   (256, "skewed")])
+def test_commit_matches_replay_state(lib, T, fam, bf16):
+    inp = _inputs(T, fam, bf16=bf16)
+    _, S_ref = oracle_outputs(inp, keep_states=True)
+    dev = to_device(inp, bf16)
+    B = inp["parent"].shape[0]
+    o, ws, err = run_verify(lib, dev)
+    assert err == 0
+    rng = np.random.default_rng(T)
+    for trial in range(3):
+        acc = np.array([rng.choice(trees.leaves(inp["parent"][b])) if trial < 2 else rng.integers(0, T)
+                        for b in range(B)], dtype=np.int32)
+        S_new = lib.commit(torch.from_numpy(acc).cuda(), dev["S0"], dev["k"], ws, T)
+        assert lib.read_device_error(ws) == 0
+        ref = np.stack([S_ref[b, acc[b]] for b in range(B)])
+        assert rel_err(S_new.cpu().numpy(), ref) <= (TOL_BF16 if bf16 else TOL_F32)
+
+
+def test_commit_nothing_accepted_and_in_place(lib):
+    inp = _inputs(32, "random")
+    dev = to_device(inp, True)
+    o, ws, err = run_verify(lib, dev)
+    acc = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+    S_new = lib.commit(acc, dev["S0"], dev["k"], ws, 32)
+    assert torch.equal(S_new, dev["S0"])
+    # in place: S_new aliases S0
+    _, S_ref = oracle_outputs(inp, keep_states=True)
+    acc = torch.tensor([5, 9, 31], dtype=torch.int32, device="cuda")
+    S = dev["S0"].clone()
+    lib.commit(acc, S, dev["k"], ws, 32, out=S)
+    ref = np.stack([S_ref[b, a] for b, a in enumerate([5, 9, 31])])
+    assert rel_err(S.cpu().numpy(), ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("T,fam", [(1, "chain"), (8, "top2"), (64, "random"), (64, "chain"), (65, "skewed"),
+                                   (256, "random"), (256, "top8")])
+def test_serial_replay_matches_oracle(lib, T, fam, bf16):
+    inp = _inputs(T, fam, bf16=bf16)
+    o_ref, _ = oracle_outputs(inp)
+    dev = to_device(inp, bf16)
+    B, T_, H, d = dev["q"].shape
+    ws = lib.workspace(B, T, H, d)
+    o = lib.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws)
+    assert lib.read_device_error(ws) == 0
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_F32          # fp32 state on the given inputs
+
+
+def test_serial_tiny_case(lib):
+    inp = synth.config_inputs(0)
+    o_ref, _ = oracle_outputs(inp)
+    dev = to_device(inp, False)
+    ws = lib.workspace(1, 8, 2, 32)
+    o = lib.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws)
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("T", [16, 64, 128])
+def test_device_error_flags(lib, T):
+    """Bad trees and gates are reported through the error word, never by a
+    trap; the kernels sanitise what they read, so nothing is out of bounds."""
+    inp = _inputs(T, "random", B=2)
+    dev = to_device(inp, True)
+    bad = dev["parent"].clone()
+    bad[1, T - 1] = T - 1                                  # parent[i] = i
+    dev2 = dict(dev, parent=bad)
+    _, ws, err = run_verify(lib, dev2)
+    assert err & 0x1
+    bad0 = dev["parent"].clone()
+    bad0[0, 0] = 0                                         # root with a parent
+    _, ws, err = run_verify(lib, dict(dev, parent=bad0))
+    assert err & 0x1
+    g = dev["g"].clone()
+    g[0, T // 2, 1] = 0.0                                  # gate 0: log undefined
+    _, ws, err = run_verify(lib, dict(dev, g=g))
+    assert err & 0x2
+    _, ws, err = run_verify(lib, dev)
+    assert err == 0
+    acc = torch.tensor([T, -5], dtype=torch.int32, device="cuda")
+    lib.commit(acc, dev["S0"], dev["k"], ws, T)
+    assert lib.read_device_error(ws) & 0x4
+    s = lib.workspace(2, T, 4, 128)
+    lib.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], bad, s)
+    assert lib.read_device_error(s) & 0x1
+
+
+def _round_trip(lib, B, T, H, rounds, bf16, check_streams):
+    """Verify a fresh tree, accept a random root-to-leaf path, commit it into
+    S0 in fp32; the oracle carries its own fp64 state from the same S0."""
+    S_dev = None
+    S_orc = None
+    worst_o = worst_s = 0.0
+    for r in range(rounds):
+        inp = synth.config_inputs(4, rnd=r, B=B, T=T, H=H, bf16=bf16)
+        if r == 0:
+            S_orc = inp["S0"].astype(np.float64)
+            S_dev = torch.from_numpy(inp["S0"]).cuda()
+        inp["S0"] = S_orc
+        dev = to_device(inp, bf16)
+        dev["S0"] = S_dev
+        ws = lib.workspace(B, T, H, 128)
+        o = lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], S_dev, dev["parent"], ws)
+        rng = synth.stream_seed(4, r, 999)
+        acc = np.array([rng.choice(trees.leaves(inp["parent"][b])) for b in range(B)], dtype=np.int32)
+        lib.commit(torch.from_numpy(acc).cuda(), S_dev, dev["k"], ws, T, out=S_dev)
+        assert lib.read_device_error(ws) == 0
+        on = o.cpu().numpy()
+        for b in check_streams(r):
+            o_ref, _ = oracle.replay(inp["parent"][b], inp["q"][b], inp["k"][b], inp["v"][b], inp["g"][b],
+                                     inp["beta"][b], S_orc[b], keep_states=False)
+            worst_o = max(worst_o, rel_err(on[b], o_ref))
+        # the oracle's own state: replay only the accepted path
+        for b in range(B):
+            path = oracle.root_path(inp["parent"][b], int(acc[b]))
+            chain = np.arange(-1, len(path) - 1, dtype=np.int32)
+            _, S_path = oracle.replay(chain, inp["q"][b][path], inp["k"][b][path], inp["v"][b][path],
+                                      inp["g"][b][path], inp["beta"][b][path], S_orc[b], keep_states=True)
+            S_orc[b] = S_path[-1]
+        worst_s = max(worst_s, rel_err(S_dev.cpu().numpy(), S_orc))
+    return worst_o, worst_s
+
+
+def test_round_trip_100_rounds(lib):
+    """Batched round trip: B=16, H=16, T=128, 100 rounds; the state checked
+    every round for every stream, o checked on one rotating stream per round."""
+    wo, ws_ = _round_trip(lib, 16, 128, 16, 100, True, lambda r: [r % 16])
+    print("100 rounds: worst o err", wo, "worst state err", ws_)
+    assert wo <= TOL_BF16 and ws_ <= TOL_BF16
+
+
+def test_round_trip_fp32_20_rounds(lib):
+    wo, ws_ = _round_trip(lib, 4, 64, 4, 20, False, lambda r: range(4))
+    print("fp32 20 rounds: worst o err", wo, "worst state err", ws_)
+    assert wo <= TOL_F32 and ws_ <= TOL_F32

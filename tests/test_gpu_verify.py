@@ -1,0 +1,161 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Tolerances (canopy page, "Hard constraints", oracle parity; restated as
+max |o - o_ref| / rms(o_ref) over one call's whole output): 1e-2 on the
+bf16-input tensor-core path, 1e-4 on the fp32 path.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import trees
+from tests.gpu_helpers import TOL_BF16, TOL_F32, oracle_outputs, rel_err, run_verify, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(T, fam, B=2, H=4, d=128, bf16=True, seed=0):
+    rng = np.random.default_rng(seed + 7919 * T)
+    parents = [trees.family(fam, T, rng) for _ in range(B)]
+    return synth.make_inputs(parents, H, d, d, bf16, case=90, rnd=seed)
+
+
+def test_case0_tiny_fp32(lib):
+    inp = synth.config_inputs(0)
+    o_ref, _ = oracle_outputs(inp)
+    o, ws, err = run_verify(lib, to_device(inp, bf16=False))
+    assert err == 0
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_F32
+
+
+def test_case1_qwen_layer_batch1(lib):
+    inp = synth.config_inputs(1)
+    o_ref, _ = oracle_outputs(inp)
+    o, ws, err = run_verify(lib, to_device(inp, bf16=True))
+    assert err == 0
+    e = rel_err(o.cpu().numpy(), o_ref)
+    print("case1 bf16 err", e)
+    assert e <= TOL_BF16
+
+
+def test_case2_batched_both_tiers(lib):
+    inp = synth.config_inputs(2)
+    o_ref, _ = oracle_outputs(inp)
+    o, ws, err = run_verify(lib, to_device(inp, bf16=True))
+    assert err == 0
+    eb = rel_err(o.cpu().numpy(), o_ref)
+    o32, _, err = run_verify(lib, to_device(inp, bf16=False))
+    assert err == 0
+    ea = rel_err(o32.cpu().numpy(), o_ref)
+    print("case2 errors: bf16 tensor-core", eb, "fp32", ea)
+    assert eb <= TOL_BF16
+    assert ea <= TOL_F32
+
+
+TC_T = [1, 2, 3, 8, 15, 16, 17, 31, 33, 48, 63, 64]
+BIG_T = [65, 100, 127, 128, 129, 200, 255, 256]
+
+
+@pytest.mark.parametrize("fam", ["chain", "top2", "top4", "top8", "skewed", "random"])
+@pytest.mark.parametrize("T", TC_T + BIG_T)
+def test_shapes_bf16(lib, fam, T):
+    inp = _inputs(T, fam)
+    o_ref, _ = oracle_outputs(inp)
+    o, _, err = run_verify(lib, to_device(inp, bf16=True))
+    assert err == 0
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("fam", ["chain", "top4", "random"])
+@pytest.mark.parametrize("T", [1, 3, 17, 64, 65, 256])
+def test_shapes_fp32(lib, fam, T):
+    inp = _inputs(T, fam, bf16=False)
+    o_ref, _ = oracle_outputs(inp)
+    o, _, err = run_verify(lib, to_device(inp, bf16=False))
+    assert err == 0
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_F32
+
+
+def test_small_gates_chain_stays_finite(lib):
+    """64-node chain with alpha = 0.05 (the page's stability case) and a
+    random tree with alpha down to 0.01."""
+    for T, fam, amin in ((64, "chain", 0.05), (64, "random", 0.01), (256, "chain", 0.05)):
+        inp = _inputs(T, fam)
+        inp["g"] = np.full_like(inp["g"], amin) if fam == "chain" else \
+            np.random.default_rng(3).uniform(amin, 1.0, inp["g"].shape).astype(np.float32)
+        o_ref, _ = oracle_outputs(inp)
+        o, _, err = run_verify(lib, to_device(inp, bf16=True))
+        on = o.cpu().numpy()
+        assert err == 0 and np.isfinite(on).all()
+        assert rel_err(on, o_ref) <= TOL_BF16
+
+
+def test_bf16_output(lib):
+    """o written as bf16: compared with the oracle rounded to bf16 (the
+    rounding of the result is outside the method)."""
+    inp = synth.config_inputs(2)
+    o_ref, _ = oracle_outputs(inp)
+    o, _, err = run_verify(lib, to_device(inp, bf16=True), o_dtype=torch.bfloat16)
+    assert err == 0
+    ref_b = torch.from_numpy(o_ref).to(torch.bfloat16).to(torch.float64).numpy()
+    assert rel_err(o.float().cpu().numpy(), ref_b) <= TOL_BF16
+
+
+def test_relabelling_gives_permuted_outputs(lib):
+    inp = _inputs(64, "random", B=1)
+    p = inp["parent"][0]
+    o1, _, _ = run_verify(lib, to_device(inp, bf16=True))
+    for order in (trees.dfs_preorder(p), trees.level_order(p)):
+        inp2 = dict(inp)
+        inp2["parent"] = trees.relabel(p, order)[None]
+        for n in ("q", "k", "v", "g", "beta"):
+            inp2[n] = np.ascontiguousarray(inp[n][:, order])
+        o2, _, err = run_verify(lib, to_device(inp2, bf16=True))
+        assert err == 0
+        assert rel_err(o2.cpu().numpy(), o1.cpu().numpy()[:, order]) <= TOL_BF16
+
+
+def test_identical_siblings(lib):
+    p = np.array([-1, 0, 1, 2, 2, 1, 5, 5], dtype=np.int32)
+    inp = synth.make_inputs([p], 4, 128, 128, True)
+    for src, dst in ((2, 5), (3, 6), (4, 7)):
+        for n in ("q", "k", "v", "g", "beta"):
+            inp[n][:, dst] = inp[n][:, src]
+    o, _, err = run_verify(lib, to_device(inp, bf16=True))
+    o = o.cpu().numpy()
+    assert err == 0
+    for src, dst in ((2, 5), (3, 6), (4, 7)):
+        assert np.abs(o[:, src] - o[:, dst]).max() <= 1e-5 * np.abs(o).max()
+
+
+def test_beta_zero(lib):
+    inp = _inputs(40, "random")
+    inp["beta"][:] = 0
+    o, ws, err = run_verify(lib, to_device(inp, bf16=True))
+    assert err == 0
+    l = np.stack([oracle.cumulative_log_gate(inp["parent"][b], inp["g"][b]) for b in range(2)])
+    expect = np.exp(l)[..., None] * np.einsum("bhvd,bthd->bthv", inp["S0"].astype(np.float64),
+                                              inp["q"].astype(np.float64))
+    assert rel_err(o.cpu().numpy(), expect) <= TOL_BF16
+
+
+def test_deterministic_and_guarded(lib):
+    inp = synth.config_inputs(2)
+    dev = to_device(inp, bf16=True)
+    B, T, H, d = dev["q"].shape
+    n = B * T * H * d
+    buf = torch.full((n + 128,), 7.25, dtype=torch.float32, device="cuda")
+    ws = lib.workspace(B, T, H, d)
+    outs = []
+    for _ in range(2):
+        out = buf[64:64 + n].view(B, T, H, d)
+        lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws, out=out)
+        torch.cuda.synchronize()
+        outs.append(out.clone())
+    assert lib.read_device_error(ws) == 0
+    assert torch.equal(outs[0], outs[1])
+    assert (buf[:64] == 7.25).all() and (buf[64 + n:] == 7.25).all()

@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol the
+header declares; host-side argument checks answer before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_linear_tree_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "canopy.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    from gated_deltanet_linear_tree_gb300 import canopy
+    canopy._lib = None
+    return canopy.load(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)          # drop comments
+    return sorted(set(re.findall(r"\b(canopy_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    from gated_deltanet_linear_tree_gb300 import canopy
+    assert sorted(canopy.SIGNATURES) == names
+
+
+def test_workspace_sizes(lib):
+    n = lib.canopy_workspace_bytes(16, 64, 16, 128, 128)
+    # U + l + depth + mask + order + scratch, each region 256-byte aligned
+    assert n >= 16 * 64 * 16 * 128 * 4 * 3 + 2 * 16 * 16 * 64 * 64 * 4
+    assert lib.canopy_workspace_bytes(16, 257, 16, 128, 128) == 0
+    assert lib.canopy_workspace_bytes(16, 64, 16, 64, 64) == 0
+    assert lib.canopy_workspace_bytes(0, 64, 16, 128, 128) == 0
+    assert lib.canopy_workspace_bytes(1, 8, 2, 32, 32) > 0
+    assert lib.canopy_snapshot_bytes(16, 64, 16, 128, 128) == 16 * 64 * 16 * 128 * 128 * 4
+
+
+def test_status_strings_and_version(lib):
+    assert lib.canopy_status_string(0) == b"ok"
+    assert lib.canopy_status_string(3).startswith(b"unsupported")
+    assert lib.canopy_version() >= 1
+
+
+def _verify(lib, ptrs, T=64, B=1, H=1, d=128, in_dt=1, solve=0, o_dt=0):
+    q, k, v, g, be, S0, par, o, ws = ptrs
+    return lib.canopy_tree_verify(q, k, v, in_dt, g, be, S0, par, T, B, H, d, d, solve, o, o_dt, ws, None)
+
+
+def test_host_argument_errors(lib):
+    # Every case returns before any CUDA call: fake pointers are never dereferenced.
+    good = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+    null = list(good)
+    null[0] = None
+    assert _verify(lib, null) == 1                                  # null pointer
+    mis = list(good)
+    mis[2] = ctypes.c_void_p(0x10008)
+    assert _verify(lib, mis) == 1                                   # misaligned
+    assert _verify(lib, good, T=257) == 3                           # T too large
+    assert _verify(lib, good, T=0) == 1
+    assert _verify(lib, good, d=64) == 3                            # unsupported head size
+    assert _verify(lib, good, in_dt=7) == 1                         # bad enum
+    assert _verify(lib, good, solve=5) == 1
+    assert lib.canopy_commit(None, good[1], good[2], good[3], 1, 64, 1, 1, 128, 128, good[4], None) == 1
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], 1, 300, 1, 1, 128, 128, good[4], None) == 3
+    assert lib.canopy_tree_prep(good[0], good[1], 0, 1, 1, good[2], None) == 3
+    err = ctypes.c_int32(0)
+    assert lib.canopy_read_device_error(None, ctypes.byref(err), None) == 1
+    assert lib.canopy_workspace_init(None, 16, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from gated_deltanet_linear_tree_gb300 import canopy
+    saved = canopy._lib
+    canopy._lib = None
+    try:
+        with pytest.raises(canopy.CanopyError):
+            canopy.load(str(tmp_path / "missing.so"))
+    finally:
+        canopy._lib = saved
