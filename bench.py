@@ -377,6 +377,77 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# crossover sweep: closed-form verify vs the serial replay kernel
+
+def run_sweep(args):
+    """For every (B, T, family) cell: median (p10, p90) µs of the closed-form
+    verify and of the serial replay, each call timed alone with CUDA events
+    after an L2 flush, the two kernels interleaved; the ratio serial/closed is
+    the crossover map."""
+    import torch
+
+    import synth
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    from synth import configs, trees
+    bld.build()
+    canopy.load()
+    H, d = 16, 128
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    Bs = [int(x) for x in args.sweep_b.split(",")] if args.sweep_b else configs.SWEEP_B
+    Ts = [int(x) for x in args.sweep_t.split(",")] if args.sweep_t else configs.SWEEP_T
+    fams = args.sweep_fam.split(",") if args.sweep_fam else configs.SWEEP_FAMILIES
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    solves = ["fwdsub", "neumann"]
+    for B in Bs:
+        for T in Ts:
+            for fam in fams:
+                rng = np.random.default_rng(1000 * B + T)
+                parents = [trees.family(fam, T, rng) for _ in range(B)]
+                inp = synth.make_inputs(parents, H, d, d, True, case=3, rnd=T)
+                dev = {n: torch.from_numpy(inp[n]).to("cuda", torch.bfloat16) for n in ("q", "k", "v")}
+                for n in ("g", "beta", "S0"):
+                    dev[n] = torch.from_numpy(inp[n]).cuda()
+                dev["parent"] = torch.from_numpy(inp["parent"]).cuda()
+                ws = canopy.workspace(B, T, H, d)
+                snap = torch.empty(canopy.snapshot_bytes(B, T, H, d), dtype=torch.uint8, device="cuda")
+                o = torch.empty((B, T, H, d), dtype=torch.float32, device="cuda")
+                calls = {"serial": lambda: canopy.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                                                dev["S0"], dev["parent"], ws, snapshot=snap, out=o)}
+                for sv in solves:
+                    if sv == "neumann" and T > 64:
+                        continue
+                    calls[sv] = (lambda sv=sv: canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                                             dev["S0"], dev["parent"], ws, solve=sv, out=o))
+                times = {k: [] for k in calls}
+                for it in range(args.sweep_warmup + args.sweep_reps):
+                    for name, fn in calls.items():
+                        flush.fill_(float(it))
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        fn()
+                        b.record()
+                        if it >= args.sweep_warmup:
+                            times[name].append((a, b))
+                torch.cuda.synchronize()
+                assert canopy.read_device_error(ws) == 0
+                rec = {"B": B, "T": T, "family": fam, "depth": int(max(trees.tree_depth(p) for p in parents))}
+                for name, evs in times.items():
+                    us = [1e3 * a.elapsed_time(b) for a, b in evs]
+                    rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
+                                 "p90": float(np.percentile(us, 90))}
+                rec["speedup_fwdsub"] = rec["serial"]["p50"] / rec["fwdsub"]["p50"]
+                if "neumann" in rec:
+                    rec["speedup_neumann"] = rec["serial"]["p50"] / rec["neumann"]["p50"]
+                line = json.dumps(rec)
+                print(line, flush=True)
+                if out:
+                    out.write(line + "\n")
+    if out:
+        out.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -388,7 +459,17 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="crossover map vs the serial replay kernel")
+    ap.add_argument("--sweep-b", default="")
+    ap.add_argument("--sweep-t", default="")
+    ap.add_argument("--sweep-fam", default="")
+    ap.add_argument("--sweep-reps", type=int, default=50)
+    ap.add_argument("--sweep-warmup", type=int, default=10)
+    ap.add_argument("--sweep-out", default="")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -9,7 +9,7 @@ cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B
                              cudaStream_t st);
 cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                              const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                             const Ws& ws, int bv, cudaStream_t st);
+                             const Ws& ws, int bv, int neumann, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
                                cudaStream_t st);
@@ -63,7 +63,7 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int
                                void* stream) {
     if (!aligned16(parent) || !aligned16(g) || !aligned16(workspace)) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, H)) return CANOPY_ERR_UNSUPPORTED;
-    Ws ws = ws_bind(workspace, B, T, H, 128);
+    Ws ws = ws_bind(workspace, B, T, H, 32);  // tree-prep regions do not depend on dv
     return cuda_status(launch_tree_prep(parent, g, T, B, H, ws, static_cast<cudaStream_t>(stream)));
 }
 
@@ -83,10 +83,10 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     Ws ws = ws_bind(workspace, B, T, H, dv);
     const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
     const bool tc = in_bf16 && dk == 128 && T <= 64;
-    if (solve == CANOPY_SOLVE_NEUMANN) {
-        return CANOPY_ERR_UNSUPPORTED;
-    }
-    if (tc) return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, tc_tile(), st));
+    if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
+    if (tc)
+        return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, tc_tile(),
+                                            solve == CANOPY_SOLVE_NEUMANN, st));
     cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, st));

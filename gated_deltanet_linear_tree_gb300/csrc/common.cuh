@@ -28,11 +28,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int H, int dv) {
     const size_t BT = size_t(B) * T;
     w.err = 0;  // first, so its offset does not depend on the sizes
     size_t o = 256;
-    w.U = o;     o = ws_align(o + BT * H * dv * 4);
+    // tree-prep outputs next: their offsets do not depend on dv
     w.l = o;     o = ws_align(o + BT * H * 4);
     w.depth = o; o = ws_align(o + BT * 4);
     w.mask = o;  o = ws_align(o + BT * w.W * 4);
     w.order = o; o = ws_align(o + BT * 4);
+    w.U = o;     o = ws_align(o + BT * H * dv * 4);
     // scratch of the fp32 path: G and C as [B][H][T][T], gamma*Q S0^T and R as [B][T][H][dv]
     w.gs = o;    o = ws_align(o + size_t(B) * H * T * T * 4);
     w.cs = o;    o = ws_align(o + size_t(B) * H * T * T * 4);

@@ -43,8 +43,9 @@ struct Smem {
     static constexpr int SMALL = S + 2 * S_PLANE;
     // reused once the first MMAs are done:
     static constexpr int GT = 0;                    // G^T fp32 [64][64]
-    static constexpr int RT = 16384;                // R^T fp32 [BV][64], 16-byte chunks swizzled
-    static constexpr int UT = S;                    // U^T tf32 as a K-major SW128 operand [BV][64]
+    static constexpr int RT = 16384;                // R^T fp32 [BV][64] (fwdsub) or Z^T tf32 operand (Neumann)
+    static constexpr int CS = S;                    // C fp32 [64][64], word index swizzled by row
+    static constexpr int UR = (BV == 32) ? 24576 : S + 16384;  // U fp32 [64][BV], chunks swizzled by row
     // small arrays
     static constexpr int PAR = SMALL;               // int[64]   jump pointer
     static constexpr int LEN = PAR + 256;           // int[64]   path length
@@ -55,12 +56,19 @@ struct Smem {
     static constexpr int BAR = MASK + 512;          // u64[2]
     static constexpr int TMEMSLOT = BAR + 16;       // u32
     static constexpr int FLAG = TMEMSLOT + 4;       // int
-    static constexpr int TOTAL = FLAG + 12;
+    static constexpr int DMAX = FLAG + 4;           // int: tree depth
+    static constexpr int TOTAL = DMAX + 8;
     static_assert(RT + BV * 64 * 4 <= S, "R^T must fit in the Q/K region");
-    static_assert(BV * 256 <= 2 * S_PLANE, "U^T must fit in the S0 region");
+    static_assert(BV == 32 ? (UR + 64 * BV * 4 <= S) : (UR + 64 * BV * 4 <= S + 2 * S_PLANE), "U placement");
+    static_assert(CS + 64 * 64 * 4 <= (BV == 32 ? S + 2 * S_PLANE : UR), "C placement");
 };
 
-constexpr uint32_t kTmemCols = 128;  // X: [0, BV), AC: [BV, BV + 64)
+// TMEM columns: X [0, BV), AC [BV, BV + 64); the Neumann variant adds
+// Y [BV + 64, 2 BV + 64) for the per-round products G Z.
+template <int BV, bool NEU>
+__host__ __device__ constexpr uint32_t tmem_cols() {
+    return (NEU && BV == 64) ? 256u : 128u;
+}
 
 struct Params {
     const __nv_bfloat16* v;
@@ -80,7 +88,39 @@ struct Params {
 __device__ inline float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ inline float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// One element (column c, node i) of a K-major tf32 B operand [BV][64] in the
+// 128-byte swizzle layout: node i sits in atom i/32, 16-byte chunk (i%32)/4.
 template <int BV>
+__device__ inline void store_zt(uint8_t* base, int c, int i, float x) {
+    const int atom = i >> 5, chunk = (i & 31) >> 2;
+    *reinterpret_cast<uint32_t*>(base + atom * (BV * 128) + c * 128 + ((chunk ^ (c & 7)) << 4) + ((i & 3) << 2)) =
+        to_tf32(x);
+}
+
+// Store one output row (BV values) as fp32 or bf16.
+template <int BV>
+__device__ inline void store_o(const Params& p, int b, int i, int h, int v0, const float (&x)[BV]) {
+    const size_t obase = ((size_t(b) * p.T + i) * p.H + h) * DV + v0;
+    if (p.o_bf16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + obase);
+#pragma unroll
+        for (int e = 0; e < BV / 8; ++e) {
+            uint32_t w[4];
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(x[8 * e + 2 * f], x[8 * e + 2 * f + 1]);
+                w[f] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + obase);
+#pragma unroll
+        for (int e = 0; e < BV / 4; ++e) dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+    }
+}
+
+template <int BV, bool NEU>
 __global__ void __launch_bounds__(128, 4)
     verify_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, Params p) {
     using L = Smem<BV>;
@@ -96,6 +136,7 @@ __global__ void __launch_bounds__(128, 4)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
     int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
+    int* sDmax = reinterpret_cast<int*>(sm + L::DMAX);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -107,9 +148,10 @@ __global__ void __launch_bounds__(128, 4)
         mbar_init(&bars[1], 1);
         fence_mbar_init();
         *sFlag = 0;
+        *sDmax = 0;
     }
     if (warp == 0) {
-        tmem_alloc(sTmem, kTmemCols);
+        tmem_alloc(sTmem, tmem_cols<BV, NEU>());
         tmem_relinquish();
         tc_fence_before();
     }
@@ -169,6 +211,7 @@ __global__ void __launch_bounds__(128, 4)
         if (i >= T) sMask[i] = 0ull;  // padded nodes: empty path
         sGam[i] = exp2f(sL2[i]);
         if (i < T) {
+            if (NEU) atomicMax(sDmax, sLen[i] - 1);
             if (vt == 0) p.l[(size_t(b) * T + i) * H + h] = sL2[i] * 0.69314718055994531f;
             if (vt == 0 && h == 0) {
                 p.depth[size_t(b) * T + i] = sLen[i] - 1;
@@ -263,13 +306,12 @@ __global__ void __launch_bounds__(128, 4)
 
     {
         const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-        float* sGt = reinterpret_cast<float*>(sm + L::GT);
-        float* sRt = reinterpret_cast<float*>(sm + L::RT);
         if (warp < 2) {
-            // Q rows: C into TMEM (tf32), gamma-scaled X_Q in place.
+            // Q rows: C row i into shared memory (fp32), words swizzled by row.
             const int i = tid;
-            const float li = sL2[i], gi = sGam[i];
+            const float li = sL2[i];
             const uint64_t m = sMask[i];
+            float* sC = reinterpret_cast<float*>(sm + L::CS);
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t r[16];
@@ -278,23 +320,14 @@ __global__ void __launch_bounds__(128, 4)
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int j = cb * 16 + jj;
-                    const float c = ((m >> j) & 1ull) ? __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
-                    r[jj] = to_tf32(c);
+                    sC[i * 64 + (j ^ (i & 31))] =
+                        ((m >> j) & 1ull) ? __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
                 }
-                tmem_st16(lane_base + BV + cb * 16, r);
             }
-#pragma unroll
-            for (int cb = 0; cb < BV / 16; ++cb) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + cb * 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) r[jj] = __float_as_uint(gi * __uint_as_float(r[jj]));
-                tmem_st16(lane_base + cb * 16, r);
-            }
-            tmem_wait_st();
-        } else {
-            // K rows: G^T and R^T into shared memory.
+        } else if constexpr (!NEU) {
+            // K rows: G^T and R^T into shared memory for the substitution.
+            float* sGt = reinterpret_cast<float*>(sm + L::GT);
+            float* sRt = reinterpret_cast<float*>(sm + L::RT);
             const int i = tid - 64;
             const float li = sL2[i], bi = sBeta[i], gi = sGam[i];
             const uint64_t ms = sMask[i] & ~(1ull << i);
@@ -324,107 +357,179 @@ __global__ void __launch_bounds__(128, 4)
             }
         }
     }
-    tc_fence_before();
-    __syncthreads();
 
-    // Forward substitution, one thread per value column.
-    if (tid < BV) {
-        const int c = tid;
-        const float* sGt = reinterpret_cast<const float*>(sm + L::GT);
-        const float* sRt = reinterpret_cast<const float*>(sm + L::RT);
-        uint8_t* sUt = sm + L::UT;
-        float acc[TP];
+    if constexpr (!NEU) {
+        __syncthreads();
+        // Forward substitution, one thread per value column (K-row warps).
+        if (tid >= 64 && tid < 64 + BV) {
+            const int c = tid - 64;
+            const float* sGt = reinterpret_cast<const float*>(sm + L::GT);
+            const float* sRt = reinterpret_cast<const float*>(sm + L::RT);
+            float* sU = reinterpret_cast<float*>(sm + L::UR);
+            float acc[TP];
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-            const float4 x = *reinterpret_cast<const float4*>(sRt + c * 64 + ((ch ^ (c & 15)) << 2));
-            acc[4 * ch] = x.x;
-            acc[4 * ch + 1] = x.y;
-            acc[4 * ch + 2] = x.z;
-            acc[4 * ch + 3] = x.w;
-        }
-        const int Tp = (T + 15) & ~15;
-        float* Ucol = p.U + (size_t(b) * T * H + h) * DV + v0 + c;
-        uint32_t u4[4];
-#pragma unroll
-        for (int j = 0; j < TP; ++j) {
-            const float u = acc[j];
-            if (j < T) Ucol[size_t(j) * H * DV] = u;
-            u4[j & 3] = to_tf32(u);
-            if ((j & 3) == 3) {
-                const int atom = j >> 5, chunk = (j & 31) >> 2;
-                *reinterpret_cast<uint4*>(sUt + atom * (BV * 128) + c * 128 + ((chunk ^ (c & 7)) << 4)) =
-                    make_uint4(u4[0], u4[1], u4[2], u4[3]);
+            for (int ch = 0; ch < 16; ++ch) {
+                const float4 x = *reinterpret_cast<const float4*>(sRt + c * 64 + ((ch ^ (c & 15)) << 2));
+                acc[4 * ch] = x.x;
+                acc[4 * ch + 1] = x.y;
+                acc[4 * ch + 2] = x.z;
+                acc[4 * ch + 3] = x.w;
             }
-            if (j + 1 < Tp) {
+            const int Tp = (T + 15) & ~15;
+            float* Ucol = p.U + (size_t(b) * T * H + h) * DV + v0 + c;
 #pragma unroll
-                for (int i4 = (j + 1) >> 2; i4 < TP / 4; ++i4) {
-                    if (i4 * 4 < Tp) {
-                        const float4 gg = *reinterpret_cast<const float4*>(sGt + j * 64 + i4 * 4);
-                        if (i4 * 4 + 0 > j) acc[i4 * 4 + 0] -= gg.x * u;
-                        if (i4 * 4 + 1 > j) acc[i4 * 4 + 1] -= gg.y * u;
-                        if (i4 * 4 + 2 > j) acc[i4 * 4 + 2] -= gg.z * u;
-                        if (i4 * 4 + 3 > j) acc[i4 * 4 + 3] -= gg.w * u;
+            for (int j = 0; j < TP; ++j) {
+                const float u = acc[j];
+                if (j < T) Ucol[size_t(j) * H * DV] = u;
+                sU[j * BV + ((((c >> 2) ^ (j & (BV / 4 - 1)))) << 2) + (c & 3)] = u;
+                if (j + 1 < Tp) {
+#pragma unroll
+                    for (int i4 = (j + 1) >> 2; i4 < TP / 4; ++i4) {
+                        if (i4 * 4 < Tp) {
+                            const float4 gg = *reinterpret_cast<const float4*>(sGt + j * 64 + i4 * 4);
+                            if (i4 * 4 + 0 > j) acc[i4 * 4 + 0] -= gg.x * u;
+                            if (i4 * 4 + 1 > j) acc[i4 * 4 + 1] -= gg.y * u;
+                            if (i4 * 4 + 2 > j) acc[i4 * 4 + 2] -= gg.z * u;
+                            if (i4 * 4 + 3 > j) acc[i4 * 4 + 3] -= gg.w * u;
+                        }
                     }
                 }
             }
         }
+    } else {
+        // Finite Neumann series (Bole's solve): U = sum_{m=0..d} (-G)^m R.
+        // Each round is one tcgen05 tf32 MMA, A = [.; G] read from TMEM (the
+        // K rows of the AC block, overwritten with G), B = Z^T from shared
+        // memory; rows 64..127 of the product are G Z_{m-1}, so
+        // Z_m = -G Z_{m-1}.  d rounds for a tree of depth d.
+        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+        uint8_t* sZt = sm + L::RT;
+        float acc[BV];  // K rows: U row
+        const int i = tid - 64;
+        if (warp >= 2) {
+            const float li = sL2[i], bi = sBeta[i], gi = sGam[i];
+            const uint64_t ms = sMask[i] & ~(1ull << i);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + BV + cb * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = cb * 16 + jj;
+                    const float gv = ((ms >> j) & 1ull) ? bi * __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
+                    r[jj] = to_tf32(gv);
+                }
+                tmem_st16(lane_base + BV + cb * 16, r);
+            }
+#pragma unroll
+            for (int cb = 0; cb < BV / 16; ++cb) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + cb * 16, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int c = cb * 16 + jj;
+                    const float vv = (c & 1) ? bf16_hi(vw[c >> 1]) : bf16_lo(vw[c >> 1]);
+                    acc[c] = bi * (vv - gi * __uint_as_float(r[jj]));
+                    store_zt<BV>(sZt, c, i, acc[c]);
+                }
+            }
+            tmem_wait_st();
+        }
+        const int rounds = *sDmax;
+        uint32_t parity = 1;
+        for (int m = 1; m <= rounds; ++m) {
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t aZ = smem_u32(sZt);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t db = sdesc_sw128(aZ + (ks >> 2) * (BV * 128) + (ks & 3) * 32);
+                    mma_tf32_ts(tmem + BV + 64, tmem + BV + ks * 8, db, idesc_tf32(128, BV), ks != 0);
+                }
+                mma_commit(&bars[1]);
+            }
+            ok = mbar_wait(&bars[1], parity);
+            parity ^= 1;
+            ok = __syncthreads_and(ok);
+            if (!ok) {
+                if (tid == 0) raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
+                goto teardown;
+            }
+            tc_fence_after();
+            if (warp >= 2) {
+                const bool last = (m == rounds);
+#pragma unroll
+                for (int cb = 0; cb < BV / 16; ++cb) {
+                    uint32_t r[16];
+                    tmem_ld16(lane_base + BV + 64 + cb * 16, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int c = cb * 16 + jj;
+                        const float z = -__uint_as_float(r[jj]);
+                        acc[c] += z;
+                        if (!last) store_zt<BV>(sZt, c, i, z);
+                    }
+                }
+            }
+        }
+        if (warp >= 2) {
+            float* sU = reinterpret_cast<float*>(sm + L::UR);
+#pragma unroll
+            for (int c = 0; c < BV; ++c) sU[i * BV + ((((c >> 2) ^ (i & (BV / 4 - 1)))) << 2) + (c & 3)] = acc[c];
+            if (i < T) {
+                float4* dst = reinterpret_cast<float4*>(p.U + ((size_t(b) * T + i) * H + h) * DV + v0);
+#pragma unroll
+                for (int e = 0; e < BV / 4; ++e)
+                    dst[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+            }
+        }
     }
-    fence_proxy_async_smem();
     __syncthreads();
 
-    // O = gamma X_Q + C U on the tensor cores (A = C from TMEM, B = U^T).
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t aU = smem_u32(sm + L::UT);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t db = sdesc_sw128(aU + (ks >> 2) * (BV * 128) + (ks & 3) * 32);
-            mma_tf32_ts(tmem, tmem + BV + ks * 8, db, idesc_tf32(128, BV), 1);
-        }
-        mma_commit(&bars[1]);
-    }
-    ok = mbar_wait(&bars[1], 1);
-    ok = __syncthreads_and(ok);
-    if (!ok) {
-        if (tid == 0) raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
-        goto teardown;
-    }
-    tc_fence_after();
-
-    if (warp < 2 && tid < T) {
+    // Output on CUDA cores in fp32: o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
+    if (warp < 2) {
         const int i = tid;
         const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-        const size_t obase = ((size_t(b) * T + i) * H + h) * DV + v0;
+        const float gi = sGam[i];
+        const float* sC = reinterpret_cast<const float*>(sm + L::CS);
+        const float* sU = reinterpret_cast<const float*>(sm + L::UR);
+        float acc[BV];
 #pragma unroll
         for (int cb = 0; cb < BV / 16; ++cb) {
             uint32_t r[16];
             tmem_ld16(lane_base + cb * 16, r);
             tmem_wait_ld();
-            if (p.o_bf16) {
-                uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const __nv_bfloat162 pr =
-                        __floats2bfloat162_rn(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                    w[e] = *reinterpret_cast<const uint32_t*>(&pr);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + obase + cb * 16);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + obase + cb * 16);
+            for (int e = 0; e < 16; ++e) acc[cb * 16 + e] = gi * __uint_as_float(r[e]);
+        }
+        uint64_t bits = sMask[i];
+        while (bits) {
+            const int j = __ffsll(static_cast<long long>(bits)) - 1;
+            bits &= bits - 1;
+            const float cij = sC[i * 64 + (j ^ (i & 31))];
+            const float* ur = sU + j * BV;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                         __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            for (int ch = 0; ch < BV / 4; ++ch) {
+                const float4 u = *reinterpret_cast<const float4*>(ur + ((ch ^ (j & (BV / 4 - 1))) << 2));
+                acc[4 * ch] += cij * u.x;
+                acc[4 * ch + 1] += cij * u.y;
+                acc[4 * ch + 2] += cij * u.z;
+                acc[4 * ch + 3] += cij * u.w;
             }
         }
+        if (i < T) store_o<BV>(p, b, i, h, v0, acc);
     }
 
 teardown:
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, tmem_cols<BV, NEU>());
 }
 
 }  // namespace tc
@@ -463,7 +568,7 @@ static bool make_qk_map(CUtensorMap* m, const void* base, int B, int T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BV>
+template <int BV, bool NEU>
 static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
     CUtensorMap mq, mk;
     if (!make_qk_map(&mq, q, prm.B, prm.T, prm.H) || !make_qk_map(&mk, k, prm.B, prm.T, prm.H))
@@ -471,18 +576,18 @@ static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm
     const int smem = tc::Smem<BV>::TOTAL + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc::verify_kernel<BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(tc::verify_kernel<BV, NEU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     dim3 grid(tc::DV / BV, prm.H, prm.B);
-    tc::verify_kernel<BV><<<grid, 128, smem, st>>>(mq, mk, prm);
+    tc::verify_kernel<BV, NEU><<<grid, 128, smem, st>>>(mq, mk, prm);
     return cudaGetLastError();
 }
 
 cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                              const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                             const Ws& ws, int bv, cudaStream_t st) {
+                             const Ws& ws, int bv, int neumann, cudaStream_t st) {
     tc::Params prm;
     prm.v = static_cast<const __nv_bfloat16*>(v);
     prm.g = g;
@@ -500,8 +605,9 @@ cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const 
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
-    if (bv == 64) return launch_tc<64>(q, k, prm, st);
-    return launch_tc<32>(q, k, prm, st);
+    if (neumann) return launch_tc<32, true>(q, k, prm, st);
+    if (bv == 64) return launch_tc<64, false>(q, k, prm, st);
+    return launch_tc<32, false>(q, k, prm, st);
 }
 
 }  // namespace canopy

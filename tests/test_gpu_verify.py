@@ -95,14 +95,18 @@ def test_small_gates_chain_stays_finite(lib):
 
 
 def test_bf16_output(lib):
-    """o written as bf16: compared with the oracle rounded to bf16 (the
-    rounding of the result is outside the method)."""
+    """o written as bf16: the rounding of the result to bf16 (at most half an
+    ulp, 2^-8 of the value) is allowed on top of the tolerance, as the
+    KBench verify task's bound adds a bf16 half-ulp."""
     inp = synth.config_inputs(2)
     o_ref, _ = oracle_outputs(inp)
     o, _, err = run_verify(lib, to_device(inp, bf16=True), o_dtype=torch.bfloat16)
     assert err == 0
-    ref_b = torch.from_numpy(o_ref).to(torch.bfloat16).to(torch.float64).numpy()
-    assert rel_err(o.float().cpu().numpy(), ref_b) <= TOL_BF16
+    ob = o.float().cpu().numpy().astype(np.float64)
+    excess = np.maximum(np.abs(ob - o_ref) - 2.0 ** -8 * np.abs(o_ref), 0.0)
+    assert excess.max() / np.sqrt((o_ref ** 2).mean()) <= TOL_BF16
+    # and the plain metric is within the tolerance plus the largest rounding step
+    assert rel_err(ob, o_ref) <= TOL_BF16 + 2.0 ** -8 * np.abs(o_ref).max() / np.sqrt((o_ref ** 2).mean())
 
 
 def test_relabelling_gives_permuted_outputs(lib):
