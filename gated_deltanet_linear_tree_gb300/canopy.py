@@ -32,6 +32,7 @@ SIGNATURES = {
     "canopy_commit": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "canopy_serial_replay_static": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
     "canopy_read_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "canopy_status_string": (ctypes.c_char_p, [_I]),
     "canopy_version": (_I, []),
@@ -172,6 +173,28 @@ def serial_replay(q, k, v, g, beta, S0, parent, ws, snapshot=None, o_dtype=torch
                                      _ptr(parent), T, B, H, dk, dv, _ptr(out), _dt(out), _ptr(snapshot),
                                      _ptr(ws), _stream())
     _check(st, "canopy_serial_replay")
+    return out
+
+
+def serial_replay_static(q, k, v, g, beta, S0, parent, err=None, o_dtype=torch.float32, out=None):
+    """Serial replay whose snapshots live in the library's fixed device array
+    (no workspace, no snapshot buffer); err is an optional int32 CUDA tensor
+    of one element that receives the device error bits (OR-ed)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(q, "q")
+    _need(k, "k", q.dtype, q.shape)
+    _need(v, "v", q.dtype, (B, T, H, dv))
+    _need(g, "g", torch.float32, (B, T, H))
+    _need(beta, "beta", torch.float32, (B, T, H))
+    _need(S0, "S0", torch.float32, (B, H, dv, dk))
+    _need(parent, "parent", torch.int32, (B, T))
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+    errp = _ptr(err) if err is not None else None
+    st = load().canopy_serial_replay_static(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
+                                            _ptr(parent), T, B, H, dk, dv, _ptr(out), _dt(out), errp, _stream())
+    _check(st, "canopy_serial_replay_static")
     return out
 
 

@@ -132,6 +132,32 @@ canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, 
                                    void* o, canopy_dtype o_dtype, void* snapshot,
                                    void* workspace, void* stream);
 
+/* Serial replay for callers that cannot allocate device memory.  The paper
+ * has no counterpart: this is a deployment variant of canopy_serial_replay.
+ * Hosts that own every device allocation through their own pool, or loops
+ * that cannot pay for cudaMalloc's device synchronisation, cannot hand the
+ * library a snapshot buffer; this call keeps its per-node snapshots in a
+ * fixed 32 MiB device array inside the library instead, reserved on every
+ * GPU that loads the library and held until the process exits.
+ *   - Same inputs and output o as canopy_serial_replay; no workspace and no
+ *     snapshot argument.  err is an optional device int32 (may be NULL):
+ *     device-side input errors (CANOPY_DEVERR_*) are OR-ed into it, so zero
+ *     it before the call if you read it afterwards.
+ *   - Limit: B*T*H*dk*dv*4 <= 33,554,176 bytes (32 MiB less 256 bytes), e.g.
+ *     B=1, T=31, H=16 at dk=dv=128; larger calls return
+ *     CANOPY_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the array's address there
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero (every snapshot is written before
+ *     it is read), but calls that overlap on the GPU race with each other.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine. */
+canopy_status canopy_serial_replay_static(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
+                                          const float* g, const float* beta, const float* S0,
+                                          const int32_t* parent, int T, int B, int H, int dk, int dv,
+                                          void* o, canopy_dtype o_dtype, int32_t* err, void* stream);
+
 /* Synchronise `stream`, copy the device error word to *err_out and clear it.
  * Returns CANOPY_ERR_CUDA if the stream reported an error. */
 canopy_status canopy_read_device_error(void* workspace, int32_t* err_out, void* stream);
