@@ -5,23 +5,21 @@
 // form" (Bole's Theorem 1).  One CTA owns (stream b, head h, value tile of BV
 // columns of the d_v x d_k state) and, for all T nodes:
 //   1. tree prep: parent -> path bitmask, depth, l_i = sum log alpha (log2
-//      units inside), by pointer jumping (common.cuh);
-//   2. X  = [Q;K] S0_tile^T   on tcgen05 (M = 128 rows = Q rows then K rows,
+//      units inside), by pointer jumping (common.cuh); nodes grouped by depth;
+//   2. X  = [Q;K] S0_tile^T on tcgen05 (M = 128 rows = Q rows then K rows,
 //      N = BV, K = dk); S0 is split into bf16 hi + lo parts in shared memory
 //      so the product keeps ~16 mantissa bits of the fp32 state;
-//      AC = [Q;K] K^T         on tcgen05 (N = 64): rows 0..63 give Q K^T,
-//      rows 64..127 give K K^T;
-//   3. epilogue (one thread per TMEM lane): C_ij = [j in path(i)]
-//      2^(l2_i - l2_j) q_i.k_j written back to TMEM as tf32 (the A operand of
-//      step 5); gamma_i X_Q,i written back in place; G_ij = beta_i
-//      2^(l2_i - l2_j) k_i.k_j for j in A(i) and R_i = beta_i (v_i -
-//      gamma_i X_K,i) into shared memory;
-//   4. forward substitution (I + G) U = R, one thread per value column,
-//      right-looking, in fp32 registers; U goes to the workspace (for commit)
-//      and, as tf32, to shared memory as the B operand of step 5;
-//   5. O = gamma Q S0^T + C U: one tcgen05 tf32 MMA with A = C read from
-//      tensor memory, accumulated onto the gamma-scaled X_Q columns;
-//   6. o rows are read back from TMEM and stored.
+//      AC = [Q;K] K^T on tcgen05 (N = 64): rows 0..63 give Q K^T, rows
+//      64..127 give K K^T;
+//   3. epilogue (one thread per TMEM lane): C_ij = 2^(l2_i - l2_j) q_i.k_j and
+//      G_ij = beta_i 2^(l2_i - l2_j) k_i.k_j on the root-path entries only,
+//      R_i = beta_i (v_i - gamma_i X_K,i), all into shared memory;
+//   4. the triangular solve (I + G) U = R in fp32, either level by level over
+//      the tree (forward substitution; one warp per node, lanes over value
+//      columns, sums over the ancestor bits) or as the finite Neumann series
+//      on tcgen05 (Bole's solve, d rounds of Z <- -G Z);
+//   5. O = gamma X_Q + C U in fp32, one warp per node, lanes over columns,
+//      summing over path(i).
 // Decay ratios are only ever 2^(l2_i - l2_j) with j on i's root path, so they
 // lie in (0, 1] and never overflow ("Hard constraints", log-space gates).
 #include "common.cuh"
@@ -32,21 +30,26 @@ namespace tc {
 
 constexpr int DK = 128;
 constexpr int DV = 128;
-constexpr int TP = 64;  // nodes per block
+constexpr int TP = 64;   // nodes per block
+constexpr int RS = 65;   // padded row stride (floats) of the T x T tables
 
 template <int BV>
 struct Smem {
+    // phase A (until the first MMAs complete)
     static constexpr int QK = 0;                    // [Q;K] bf16: 2 atoms x 128 rows x 128 B
     static constexpr int S_ATOM = BV * 128;         // one 64-column bf16 atom of the S0 tile
     static constexpr int S_PLANE = 2 * S_ATOM;      // hi or lo plane
     static constexpr int S = 32768;                 // S0 hi then lo
-    static constexpr int SMALL = S + 2 * S_PLANE;
-    // reused once the first MMAs are done:
-    static constexpr int GT = 0;                    // G^T fp32 [64][64]
-    static constexpr int RT = 16384;                // R^T fp32 [BV][64] (fwdsub) or Z^T tf32 operand (Neumann)
-    static constexpr int CS = S;                    // C fp32 [64][64], word index swizzled by row
-    static constexpr int UR = (BV == 32) ? 24576 : S + 16384;  // U fp32 [64][BV], chunks swizzled by row
+    static constexpr int A_END = S + 2 * S_PLANE;
+    // phase B (reuses phase A's space)
+    static constexpr int GS = 0;                    // G fp32 [64][RS]; later gamma X_Q fp32 [64][BV+1]
+    static constexpr int CS = GS + TP * RS * 4;     // C fp32 [64][RS]
+    static constexpr int RR = CS + TP * RS * 4;     // R fp32 [64][BV+1]
+    static constexpr int UR = RR + TP * (BV + 1) * 4;  // U fp32 [64][BV]
+    static constexpr int ZT = 33792;                // Neumann: Z^T tf32 operand [BV][64] (1024-aligned)
+    static constexpr int B_END = UR + TP * BV * 4;
     // small arrays
+    static constexpr int SMALL = ((A_END > B_END ? A_END : B_END) + 255) & ~255;
     static constexpr int PAR = SMALL;               // int[64]   jump pointer
     static constexpr int LEN = PAR + 256;           // int[64]   path length
     static constexpr int L2 = LEN + 256;            // float[64] cumulative log2 gate
@@ -57,10 +60,12 @@ struct Smem {
     static constexpr int TMEMSLOT = BAR + 16;       // u32
     static constexpr int FLAG = TMEMSLOT + 4;       // int
     static constexpr int DMAX = FLAG + 4;           // int: tree depth
-    static constexpr int TOTAL = DMAX + 8;
-    static_assert(RT + BV * 64 * 4 <= S, "R^T must fit in the Q/K region");
-    static_assert(BV == 32 ? (UR + 64 * BV * 4 <= S) : (UR + 64 * BV * 4 <= S + 2 * S_PLANE), "U placement");
-    static_assert(CS + 64 * 64 * 4 <= (BV == 32 ? S + 2 * S_PLANE : UR), "C placement");
+    static constexpr int CNT = DMAX + 8;            // int[64]: nodes per depth level
+    static constexpr int START = CNT + 256;         // int[65]: first slot of each level in LVL
+    static constexpr int LVL = START + 272;         // int[64]: nodes sorted by depth
+    static constexpr int TOTAL = LVL + 256;
+    static_assert(ZT + BV * 256 <= SMALL, "Z^T placement");
+    static_assert(TP * (BV + 1) * 4 <= TP * RS * 4 || BV == 64, "gamma X_Q placement");
 };
 
 // TMEM columns: X [0, BV), AC [BV, BV + 64); the Neumann variant adds
@@ -97,26 +102,25 @@ __device__ inline void store_zt(uint8_t* base, int c, int i, float x) {
         to_tf32(x);
 }
 
-// Store one output row (BV values) as fp32 or bf16.
-template <int BV>
-__device__ inline void store_o(const Params& p, int b, int i, int h, int v0, const float (&x)[BV]) {
-    const size_t obase = ((size_t(b) * p.T + i) * p.H + h) * DV + v0;
-    if (p.o_bf16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + obase);
+// Raw 64-column AC row of this thread's TMEM lane into a padded smem row.
+__device__ inline void ac_row_to_smem(uint32_t lane_base, int acol, float* row) {
 #pragma unroll
-        for (int e = 0; e < BV / 8; ++e) {
-            uint32_t w[4];
+    for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld16(lane_base + acol + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tmem_ld16(lane_base + acol + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tmem_wait_ld();
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(x[8 * e + 2 * f], x[8 * e + 2 * f + 1]);
-                w[f] = *reinterpret_cast<const uint32_t*>(&pr);
-            }
-            dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    } else {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + obase);
-#pragma unroll
-        for (int e = 0; e < BV / 4; ++e) dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+        for (int jj = 0; jj < 32; ++jj) row[32 * half + jj] = __uint_as_float(r[jj]);
+    }
+}
+
+// Bounded wait on an mbarrier phase by warp 0 only; the result is shared
+// through sFlag and agreed on at the barrier that follows.
+__device__ inline void warp0_wait(uint64_t* bar, uint32_t parity, int warp, int* sFlag) {
+    if (warp == 0) {
+        const bool ok = mbar_wait(bar, parity);
+        if (!ok && (threadIdx.x & 31) == 0) *sFlag = 1;
     }
 }
 
@@ -124,6 +128,7 @@ template <int BV, bool NEU>
 __global__ void __launch_bounds__(128, 4)
     verify_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, Params p) {
     using L = Smem<BV>;
+    constexpr int NCC = BV / 32;  // value columns per lane
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -137,8 +142,15 @@ __global__ void __launch_bounds__(128, 4)
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
     int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
     int* sDmax = reinterpret_cast<int*>(sm + L::DMAX);
+    int* sCnt = reinterpret_cast<int*>(sm + L::CNT);
+    int* sStart = reinterpret_cast<int*>(sm + L::START);
+    int* sLvl = reinterpret_cast<int*>(sm + L::LVL);
+    float* sG = reinterpret_cast<float*>(sm + L::GS);
+    float* sC = reinterpret_cast<float*>(sm + L::CS);
+    float* sR = reinterpret_cast<float*>(sm + L::RR);
+    float* sU = reinterpret_cast<float*>(sm + L::UR);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int T = p.T, H = p.H;
     const int v0 = vt * BV;
@@ -169,6 +181,7 @@ __global__ void __launch_bounds__(128, 4)
     int bad = 0;
     if (tid < TP) {
         const int i = tid;
+        sCnt[i] = 0;
         int par = -1;
         float a = 1.f, be = 0.f;
         if (i < T) {
@@ -206,12 +219,14 @@ __global__ void __launch_bounds__(128, 4)
 
     // Tree prep (threads 0..63 own nodes; the whole CTA takes the barriers).
     jump_paths<1>(TP, sPtr, sLen, sL2, sMask);
+    int rank = 0;
     if (tid < TP) {
         const int i = tid;
         if (i >= T) sMask[i] = 0ull;  // padded nodes: empty path
         sGam[i] = exp2f(sL2[i]);
         if (i < T) {
-            if (NEU) atomicMax(sDmax, sLen[i] - 1);
+            atomicMax(sDmax, sLen[i] - 1);
+            rank = atomicAdd(&sCnt[sLen[i] - 1], 1);
             if (vt == 0) p.l[(size_t(b) * T + i) * H + h] = sL2[i] * 0.69314718055994531f;
             if (vt == 0 && h == 0) {
                 p.depth[size_t(b) * T + i] = sLen[i] - 1;
@@ -221,6 +236,32 @@ __global__ void __launch_bounds__(128, 4)
             }
         }
     }
+    __syncthreads();
+    // Nodes grouped by depth level (order within a level is irrelevant: the
+    // nodes of one level never depend on each other).
+    if (warp == 0) {
+        // exclusive scan of the level counts by one warp (levels < 64)
+        const int dmax = *sDmax;
+        int c0 = (lane <= dmax) ? sCnt[lane] : 0;
+        int c1 = (lane + 32 <= dmax) ? sCnt[lane + 32] : 0;
+        int x0 = c0, x1 = c1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y0 = __shfl_up_sync(0xffffffffu, x0, off);
+            const int y1 = __shfl_up_sync(0xffffffffu, x1, off);
+            if (lane >= off) {
+                x0 += y0;
+                x1 += y1;
+            }
+        }
+        const int tot0 = __shfl_sync(0xffffffffu, x0, 31);
+        const int tot1 = __shfl_sync(0xffffffffu, x1, 31);  // every lane takes part in the shuffle
+        sStart[lane] = x0 - c0;
+        sStart[lane + 32] = tot0 + x1 - c1;
+        if (lane == 0) sStart[64] = tot0 + tot1;
+    }
+    __syncthreads();
+    if (tid < T) sLvl[sStart[sLen[tid] - 1] + rank] = tid;
 
     // S0 tile -> bf16 hi and lo planes, K-major with the 128-byte swizzle.
     {
@@ -231,18 +272,15 @@ __global__ void __launch_bounds__(128, 4)
             const int r = f >> 5, c4 = f & 31;
             const int atom = c4 >> 4, chunk = (c4 & 15) >> 1;
             const int off = atom * L::S_ATOM + r * 128 + ((chunk ^ (r & 7)) << 4) + ((c4 & 1) << 3);
-            const float x[4] = {s0r[u].x, s0r[u].y, s0r[u].z, s0r[u].w};
-            uint32_t hb[4], lb[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(x[e]);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(x[e] - __bfloat162float(hi));
-                hb[e] = __bfloat16_as_ushort(hi);
-                lb[e] = __bfloat16_as_ushort(lo);
-            }
-            *reinterpret_cast<uint2*>(sS + off) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(s0r[u].x, s0r[u].y);
+            const __nv_bfloat162 h23 = __floats2bfloat162_rn(s0r[u].z, s0r[u].w);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            const __nv_bfloat162 l01 = __floats2bfloat162_rn(s0r[u].x - f01.x, s0r[u].y - f01.y);
+            const __nv_bfloat162 l23 = __floats2bfloat162_rn(s0r[u].z - f23.x, s0r[u].w - f23.y);
+            *reinterpret_cast<uint2*>(sS + off) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
             *reinterpret_cast<uint2*>(sS + L::S_PLANE + off) =
-                make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+                make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
         }
     }
     // V rows for the K-row threads (lane 64 + i holds node i): BV bf16;
@@ -268,34 +306,38 @@ __global__ void __launch_bounds__(128, 4)
     __syncthreads();
 
     // First MMAs: X = [Q;K] (S0hi + S0lo)^T and AC = [Q;K] K^T.
-    if (tid == 0) {
-        if (!mbar_wait(&bars[0], 0)) {
-            *sFlag = 1;
-        } else {
-            tc_fence_after();
-            const uint32_t aQK = smem_u32(sQK);
-            const uint32_t aS = smem_u32(sm + L::S);
+    if (warp == 0) {
+        const bool ok = mbar_wait(&bars[0], 0);
+        if (lane == 0) {
+            if (!ok) {
+                *sFlag = 1;
+            } else {
+                tc_fence_after();
+                const uint32_t aQK = smem_u32(sQK);
+                const uint32_t aS = smem_u32(sm + L::S);
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
+                        const uint64_t db =
+                            sdesc_sw128(aS + part * L::S_PLANE + (ks >> 2) * L::S_ATOM + (ks & 3) * 32);
+                        mma_bf16_ss(tmem, da, db, idesc_bf16(128, BV), (part | ks) != 0);
+                    }
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
-                    const uint64_t db = sdesc_sw128(aS + part * L::S_PLANE + (ks >> 2) * L::S_ATOM + (ks & 3) * 32);
-                    mma_bf16_ss(tmem, da, db, idesc_bf16(128, BV), (part | ks) != 0);
+                    const uint64_t db = sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32);
+                    mma_bf16_ss(tmem + BV, da, db, idesc_bf16(128, 64), ks != 0);
                 }
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
-                const uint64_t db = sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32);
-                mma_bf16_ss(tmem + BV, da, db, idesc_bf16(128, 64), ks != 0);
+                mma_commit(&bars[1]);
             }
-            mma_commit(&bars[1]);
         }
+        __syncwarp();
+        if (*sFlag == 0) warp0_wait(&bars[1], 0, warp, sFlag);
     }
     __syncthreads();
-    bool ok = (*sFlag == 0) && mbar_wait(&bars[1], 0);
-    ok = __syncthreads_and(ok);
-    if (!ok) {
+    if (*sFlag) {
         if (tid == 0) {
             raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
             mbar_wait(&bars[0], 0);  // let copies in flight land before leaving
@@ -307,52 +349,40 @@ __global__ void __launch_bounds__(128, 4)
     {
         const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
         if (warp < 2) {
-            // Q rows: C row i into shared memory (fp32), words swizzled by row.
+            // Q rows: C row i (raw Q K^T, then the decay on the path entries,
+            // the only ones the output reads).
             const int i = tid;
             const float li = sL2[i];
-            const uint64_t m = sMask[i];
-            float* sC = reinterpret_cast<float*>(sm + L::CS);
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + BV + cb * 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = cb * 16 + jj;
-                    sC[i * 64 + (j ^ (i & 31))] =
-                        ((m >> j) & 1ull) ? __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
-                }
+            float* crow = sC + i * RS;
+            ac_row_to_smem(lane_base, BV, crow);
+            for (uint64_t bits = sMask[i]; bits; bits &= bits - 1) {
+                const int j = __ffsll(static_cast<long long>(bits)) - 1;
+                crow[j] *= exp2f(li - sL2[j]);
             }
-        } else if constexpr (!NEU) {
-            // K rows: G^T and R^T into shared memory for the substitution.
-            float* sGt = reinterpret_cast<float*>(sm + L::GT);
-            float* sRt = reinterpret_cast<float*>(sm + L::RT);
+        } else {
             const int i = tid - 64;
             const float li = sL2[i], bi = sBeta[i], gi = sGam[i];
             const uint64_t ms = sMask[i] & ~(1ull << i);
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + BV + cb * 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = cb * 16 + jj;
-                    sGt[j * 64 + i] = ((ms >> j) & 1ull) ? bi * __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
+            if constexpr (!NEU) {
+                // K rows: G row i on the strict ancestors, and R row i.
+                float* grow = sG + i * RS;
+                ac_row_to_smem(lane_base, BV, grow);
+                for (uint64_t bits = ms; bits; bits &= bits - 1) {
+                    const int j = __ffsll(static_cast<long long>(bits)) - 1;
+                    grow[j] *= bi * exp2f(li - sL2[j]);
                 }
-            }
+                float* rrow = sR + i * (BV + 1);
 #pragma unroll
-            for (int cb = 0; cb < BV / 16; ++cb) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + cb * 16, r);
-                tmem_wait_ld();
+                for (int cb = 0; cb < BV / 16; ++cb) {
+                    uint32_t r[16];
+                    tmem_ld16(lane_base + cb * 16, r);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int c = cb * 16 + jj;
-                    const float vv = (c & 1) ? bf16_hi(vw[c >> 1]) : bf16_lo(vw[c >> 1]);
-                    const float rr = bi * (vv - gi * __uint_as_float(r[jj]));
-                    sRt[c * 64 + ((((i >> 2) ^ (c & 15))) << 2) + (i & 3)] = rr;
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int c = cb * 16 + jj;
+                        const float vv = (c & 1) ? bf16_hi(vw[c >> 1]) : bf16_lo(vw[c >> 1]);
+                        rrow[c] = bi * (vv - gi * __uint_as_float(r[jj]));
+                    }
                 }
             }
         }
@@ -360,41 +390,53 @@ __global__ void __launch_bounds__(128, 4)
 
     if constexpr (!NEU) {
         __syncthreads();
-        // Forward substitution, one thread per value column (K-row warps).
-        if (tid >= 64 && tid < 64 + BV) {
-            const int c = tid - 64;
-            const float* sGt = reinterpret_cast<const float*>(sm + L::GT);
-            const float* sRt = reinterpret_cast<const float*>(sm + L::RT);
-            float* sU = reinterpret_cast<float*>(sm + L::UR);
-            float acc[TP];
+        // Level-synchronous forward substitution over the tree (canopy page,
+        // "The tree closed form", level-synchronous solve): the nodes of one
+        // depth level depend only on shallower nodes, so each level is one
+        // parallel step.  A warp takes a node, its lanes the value columns;
+        // u_i = R_i - sum_{j in A(i)} G_ij u_j runs over the ancestor bits.
+        const int dmax = *sDmax;
+        for (int lv = 0; lv <= dmax; ++lv) {
+            const int s1 = sStart[lv + 1];
+            for (int idx = sStart[lv] + warp; idx < s1; idx += 4) {
+                const int i = sLvl[idx];
+                const float* grow = sG + i * RS;
+                float a0[NCC], a1[NCC];
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const float4 x = *reinterpret_cast<const float4*>(sRt + c * 64 + ((ch ^ (c & 15)) << 2));
-                acc[4 * ch] = x.x;
-                acc[4 * ch + 1] = x.y;
-                acc[4 * ch + 2] = x.z;
-                acc[4 * ch + 3] = x.w;
-            }
-            const int Tp = (T + 15) & ~15;
-            float* Ucol = p.U + (size_t(b) * T * H + h) * DV + v0 + c;
+                for (int q = 0; q < NCC; ++q) {
+                    a0[q] = sR[i * (BV + 1) + lane + 32 * q];
+                    a1[q] = 0.f;
+                }
+                uint64_t bits = sMask[i] & ~(1ull << i);
+                while (bits) {
+                    const int j0 = __ffsll(static_cast<long long>(bits)) - 1;
+                    bits &= bits - 1;
+                    const float g0 = grow[j0];
+                    const float* u0 = sU + j0 * BV + lane;
+                    if (bits) {
+                        const int j1 = __ffsll(static_cast<long long>(bits)) - 1;
+                        bits &= bits - 1;
+                        const float g1 = grow[j1];
+                        const float* u1 = sU + j1 * BV + lane;
 #pragma unroll
-            for (int j = 0; j < TP; ++j) {
-                const float u = acc[j];
-                if (j < T) Ucol[size_t(j) * H * DV] = u;
-                sU[j * BV + ((((c >> 2) ^ (j & (BV / 4 - 1)))) << 2) + (c & 3)] = u;
-                if (j + 1 < Tp) {
-#pragma unroll
-                    for (int i4 = (j + 1) >> 2; i4 < TP / 4; ++i4) {
-                        if (i4 * 4 < Tp) {
-                            const float4 gg = *reinterpret_cast<const float4*>(sGt + j * 64 + i4 * 4);
-                            if (i4 * 4 + 0 > j) acc[i4 * 4 + 0] -= gg.x * u;
-                            if (i4 * 4 + 1 > j) acc[i4 * 4 + 1] -= gg.y * u;
-                            if (i4 * 4 + 2 > j) acc[i4 * 4 + 2] -= gg.z * u;
-                            if (i4 * 4 + 3 > j) acc[i4 * 4 + 3] -= gg.w * u;
+                        for (int q = 0; q < NCC; ++q) {
+                            a0[q] -= g0 * u0[32 * q];
+                            a1[q] -= g1 * u1[32 * q];
                         }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < NCC; ++q) a0[q] -= g0 * u0[32 * q];
                     }
                 }
+                float* ug = p.U + ((size_t(b) * T + i) * H + h) * DV + v0 + lane;
+#pragma unroll
+                for (int q = 0; q < NCC; ++q) {
+                    const float u = a0[q] + a1[q];
+                    sU[i * BV + lane + 32 * q] = u;
+                    ug[32 * q] = u;
+                }
             }
+            __syncthreads();
         }
     } else {
         // Finite Neumann series (Bole's solve): U = sum_{m=0..d} (-G)^m R.
@@ -403,7 +445,7 @@ __global__ void __launch_bounds__(128, 4)
         // memory; rows 64..127 of the product are G Z_{m-1}, so
         // Z_m = -G Z_{m-1}.  d rounds for a tree of depth d.
         const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-        uint8_t* sZt = sm + L::RT;
+        uint8_t* sZt = sm + L::ZT;
         float acc[BV];  // K rows: U row
         const int i = tid - 64;
         if (warp >= 2) {
@@ -443,20 +485,23 @@ __global__ void __launch_bounds__(128, 4)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t aZ = smem_u32(sZt);
+            if (warp == 0) {
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t aZ = smem_u32(sZt);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t db = sdesc_sw128(aZ + (ks >> 2) * (BV * 128) + (ks & 3) * 32);
-                    mma_tf32_ts(tmem + BV + 64, tmem + BV + ks * 8, db, idesc_tf32(128, BV), ks != 0);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t db = sdesc_sw128(aZ + (ks >> 2) * (BV * 128) + (ks & 3) * 32);
+                        mma_tf32_ts(tmem + BV + 64, tmem + BV + ks * 8, db, idesc_tf32(128, BV), ks != 0);
+                    }
+                    mma_commit(&bars[1]);
                 }
-                mma_commit(&bars[1]);
+                __syncwarp();
+                warp0_wait(&bars[1], parity, warp, sFlag);
             }
-            ok = mbar_wait(&bars[1], parity);
             parity ^= 1;
-            ok = __syncthreads_and(ok);
-            if (!ok) {
+            __syncthreads();
+            if (*sFlag) {
                 if (tid == 0) raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
                 goto teardown;
             }
@@ -478,10 +523,10 @@ __global__ void __launch_bounds__(128, 4)
                 }
             }
         }
+        __syncthreads();  // the last round's Z^T reads are done before sU overwrites
         if (warp >= 2) {
-            float* sU = reinterpret_cast<float*>(sm + L::UR);
 #pragma unroll
-            for (int c = 0; c < BV; ++c) sU[i * BV + ((((c >> 2) ^ (i & (BV / 4 - 1)))) << 2) + (c & 3)] = acc[c];
+            for (int c = 0; c < BV; ++c) sU[i * BV + c] = acc[c];
             if (i < T) {
                 float4* dst = reinterpret_cast<float4*>(p.U + ((size_t(b) * T + i) * H + h) * DV + v0);
 #pragma unroll
@@ -489,41 +534,67 @@ __global__ void __launch_bounds__(128, 4)
                     dst[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
             }
         }
+        __syncthreads();
     }
-    __syncthreads();
 
-    // Output on CUDA cores in fp32: o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
+    // gamma X_Q rows into shared memory (over G, no longer needed) so that
+    // the output can run with lanes over columns.
     if (warp < 2) {
         const int i = tid;
         const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
         const float gi = sGam[i];
-        const float* sC = reinterpret_cast<const float*>(sm + L::CS);
-        const float* sU = reinterpret_cast<const float*>(sm + L::UR);
-        float acc[BV];
+        float* xrow = sG + i * (BV + 1);
 #pragma unroll
         for (int cb = 0; cb < BV / 16; ++cb) {
             uint32_t r[16];
             tmem_ld16(lane_base + cb * 16, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[cb * 16 + e] = gi * __uint_as_float(r[e]);
+            for (int jj = 0; jj < 16; ++jj) xrow[cb * 16 + jj] = gi * __uint_as_float(r[jj]);
+        }
+    }
+    __syncthreads();
+
+    // Output on CUDA cores in fp32, one warp per node, lanes over columns:
+    // o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
+    for (int i = warp; i < T; i += 4) {
+        const float* crow = sC + i * RS;
+        float a0[NCC], a1[NCC];
+#pragma unroll
+        for (int q = 0; q < NCC; ++q) {
+            a0[q] = sG[i * (BV + 1) + lane + 32 * q];
+            a1[q] = 0.f;
         }
         uint64_t bits = sMask[i];
         while (bits) {
-            const int j = __ffsll(static_cast<long long>(bits)) - 1;
+            const int j0 = __ffsll(static_cast<long long>(bits)) - 1;
             bits &= bits - 1;
-            const float cij = sC[i * 64 + (j ^ (i & 31))];
-            const float* ur = sU + j * BV;
+            const float c0 = crow[j0];
+            const float* u0 = sU + j0 * BV + lane;
+            if (bits) {
+                const int j1 = __ffsll(static_cast<long long>(bits)) - 1;
+                bits &= bits - 1;
+                const float c1 = crow[j1];
+                const float* u1 = sU + j1 * BV + lane;
 #pragma unroll
-            for (int ch = 0; ch < BV / 4; ++ch) {
-                const float4 u = *reinterpret_cast<const float4*>(ur + ((ch ^ (j & (BV / 4 - 1))) << 2));
-                acc[4 * ch] += cij * u.x;
-                acc[4 * ch + 1] += cij * u.y;
-                acc[4 * ch + 2] += cij * u.z;
-                acc[4 * ch + 3] += cij * u.w;
+                for (int q = 0; q < NCC; ++q) {
+                    a0[q] += c0 * u0[32 * q];
+                    a1[q] += c1 * u1[32 * q];
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < NCC; ++q) a0[q] += c0 * u0[32 * q];
             }
         }
-        if (i < T) store_o<BV>(p, b, i, h, v0, acc);
+        const size_t ob = ((size_t(b) * T + i) * H + h) * DV + v0 + lane;
+#pragma unroll
+        for (int q = 0; q < NCC; ++q) {
+            const float x = a0[q] + a1[q];
+            if (p.o_bf16)
+                static_cast<__nv_bfloat16*>(p.o)[ob + 32 * q] = __float2bfloat16_rn(x);
+            else
+                static_cast<float*>(p.o)[ob + 32 * q] = x;
+        }
     }
 
 teardown:
