@@ -2,24 +2,30 @@
 // fp32 accumulation in tensor memory), one 64-node block (T <= 64).
 //
 // Method: canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed
-// form" (Bole's Theorem 1).  One CTA owns (stream b, head h, value tile of BV
-// columns of the d_v x d_k state) and, for all T nodes:
-//   1. tree prep: parent -> path bitmask, depth, l_i = sum log alpha (log2
-//      units inside), by pointer jumping (common.cuh); nodes grouped by depth;
-//   2. X  = [Q;K] S0_tile^T on tcgen05 (M = 128 rows = Q rows then K rows,
-//      N = BV, K = dk); S0 is split into bf16 hi + lo parts in shared memory
-//      so the product keeps ~16 mantissa bits of the fp32 state;
-//      AC = [Q;K] K^T on tcgen05 (N = 64): rows 0..63 give Q K^T, rows
-//      64..127 give K K^T;
-//   3. epilogue (one thread per TMEM lane): C_ij = 2^(l2_i - l2_j) q_i.k_j and
-//      G_ij = beta_i 2^(l2_i - l2_j) k_i.k_j on the root-path entries only,
-//      R_i = beta_i (v_i - gamma_i X_K,i), all into shared memory;
-//   4. the triangular solve (I + G) U = R in fp32, either level by level over
-//      the tree (forward substitution; one warp per node, lanes over value
-//      columns, sums over the ancestor bits) or as the finite Neumann series
-//      on tcgen05 (Bole's solve, d rounds of Z <- -G Z);
-//   5. O = gamma X_Q + C U in fp32, one warp per node, lanes over columns,
-//      summing over path(i).
+// form" (Bole's Theorem 1):
+//     (I + G) U = R,  R = diag(beta) (V - diag(gamma) K S0^T),
+//     O = diag(gamma) Q S0^T + C U.
+// Here the solve is carried by the inverse W = (I + G)^-1, which has the
+// ancestor sparsity of G, and by M = C W:
+//     U = W R,   O = diag(gamma) Q S0^T + M R.
+// One CTA (256 threads) owns one (stream b, head h) and all 128 value columns:
+//   1. tree prep: parent -> path bitmask, depth, l_i = sum log2 alpha, by
+//      pointer jumping;
+//   2. AC = [Q;K] K^T on tcgen05 (M = 128: Q rows then K rows, N = 64);
+//      C_ij = 2^(l2_i - l2_j) q_i.k_j and G_ij = beta_i 2^(l2_i - l2_j) k_i.k_j
+//      on the root-path entries into shared memory;
+//   3. W = (I + G)^-1 and M = C W by substitution along each node's root
+//      path (rows are independent: W (I + G) = I, M (I + G) = C), in fp32;
+//      the finite Neumann series variant builds W on tcgen05 instead;
+//   4. [M; W] is written to tensor memory as tf32 hi + lo parts (the A
+//      operand of step 6);
+//   5. X = [Q;K] S0^T on tcgen05 (N = 128), issued with step 2; S0 is split
+//      into bf16 hi + lo in shared memory so the product keeps ~16 mantissa
+//      bits of fp32;
+//   6. R = beta (V - gamma X_K) goes to shared memory as tf32 hi + lo; the
+//      X_Q rows are scaled by gamma and the X_K rows zeroed in place; then
+//      X += [M; W] R by three tf32 MMAs (hi*hi + hi*lo + lo*hi), which keeps
+//      fp32 accuracy: rows 0..63 become o, rows 64..127 become U.
 // Decay ratios are only ever 2^(l2_i - l2_j) with j on i's root path, so they
 // lie in (0, 1] and never overflow ("Hard constraints", log-space gates).
 #include "common.cuh"
@@ -30,50 +36,56 @@ namespace tc {
 
 constexpr int DK = 128;
 constexpr int DV = 128;
-constexpr int TP = 64;   // nodes per block
-constexpr int RS = 65;   // padded row stride (floats) of the T x T tables
+constexpr int TP = 64;       // nodes per block
+constexpr int RS = 65;       // padded row stride (floats) of the T x T tables
+constexpr int NT = 256;      // threads per CTA
+constexpr uint32_t kTmemCols = 256;  // X [0,128), A hi [128,192), A lo [192,256)
+constexpr uint32_t kTmemColsNeu = 512;  // + Neumann products G P at [256,320)
+constexpr int YC = 256;
+constexpr int XC = 0, AH = 128, AL = 192;
 
-template <int BV>
 struct Smem {
-    // phase A (until the first MMAs complete)
-    static constexpr int QK = 0;                    // [Q;K] bf16: 2 atoms x 128 rows x 128 B
-    static constexpr int S_ATOM = BV * 128;         // one 64-column bf16 atom of the S0 tile
-    static constexpr int S_PLANE = 2 * S_ATOM;      // hi or lo plane
-    static constexpr int S = 32768;                 // S0 hi then lo
-    static constexpr int A_END = S + 2 * S_PLANE;
-    // phase B (reuses phase A's space)
-    static constexpr int GS = 0;                    // G fp32 [64][RS]; later gamma X_Q fp32 [64][BV+1]
-    static constexpr int CS = GS + TP * RS * 4;     // C fp32 [64][RS]
-    static constexpr int RR = CS + TP * RS * 4;     // R fp32 [64][BV+1]
-    static constexpr int UR = RR + TP * (BV + 1) * 4;  // U fp32 [64][BV]
-    static constexpr int ZT = 33792;                // Neumann: Z^T tf32 operand [BV][64] (1024-aligned)
-    static constexpr int B_END = UR + TP * BV * 4;
+    // phase 1: Q/K and S0 hi/lo (until the first products complete)
+    static constexpr int QK = 0;                 // [Q;K] bf16: 2 atoms x 128 rows x 128 B
+    static constexpr int S = 32768;              // S0: 2 planes x 2 atoms x 128 rows x 128 B
+    static constexpr int S_ATOM = 128 * 128;
+    static constexpr int S_PLANE = 2 * S_ATOM;
+    static constexpr int P1_END = S + 2 * S_PLANE;
+    // phase 2: the T x T tables (over phase 1) and V (loaded by TMA once
+    // phase 1 is done)
+    static constexpr int CT = 0;                 // C fp32 [64][RS]
+    static constexpr int GT = CT + TP * RS * 4;  // G
+    static constexpr int WT = GT + TP * RS * 4;  // W
+    static constexpr int MT = WT + TP * RS * 4;  // M
+    static constexpr int VT = 67584;             // V bf16: 2 tiles [64 nodes][64 cols], 128-byte swizzle
+    static constexpr int V_TILE = 64 * 128;
+    static constexpr int P2_END = VT + 2 * V_TILE;
+    // phase 3: R^T hi/lo as the K-major tf32 B operand [128 cols][64 nodes]
+    static constexpr int RH = 0;
+    static constexpr int RL = 32768;
+    static constexpr int R_ATOM = 128 * 128;     // 32 nodes x 128 rows
     // small arrays
-    static constexpr int SMALL = ((A_END > B_END ? A_END : B_END) + 255) & ~255;
-    static constexpr int PAR = SMALL;               // int[64]   jump pointer
-    static constexpr int LEN = PAR + 256;           // int[64]   path length
-    static constexpr int L2 = LEN + 256;            // float[64] cumulative log2 gate
-    static constexpr int GAM = L2 + 256;            // float[64] gamma = 2^l2
-    static constexpr int BETA = GAM + 256;          // float[64]
-    static constexpr int MASK = BETA + 256;         // u64[64]   path(i) incl. i
-    static constexpr int BAR = MASK + 512;          // u64[2]
-    static constexpr int TMEMSLOT = BAR + 16;       // u32
-    static constexpr int FLAG = TMEMSLOT + 4;       // int
-    static constexpr int DMAX = FLAG + 4;           // int: tree depth
-    static constexpr int CNT = DMAX + 8;            // int[64]: nodes per depth level
-    static constexpr int START = CNT + 256;         // int[65]: first slot of each level in LVL
-    static constexpr int LVL = START + 272;         // int[64]: nodes sorted by depth
-    static constexpr int TOTAL = LVL + 256;
-    static_assert(ZT + BV * 256 <= SMALL, "Z^T placement");
-    static_assert(TP * (BV + 1) * 4 <= TP * RS * 4 || BV == 64, "gamma X_Q placement");
+    static constexpr int SMALL = 98304;
+    static constexpr int PAR = SMALL;            // int[64]   jump pointer
+    static constexpr int LEN = PAR + 256;        // int[64]   path length
+    static constexpr int L2 = LEN + 256;         // float[64] cumulative log2 gate
+    static constexpr int GAM = L2 + 256;         // float[64] gamma = 2^l2
+    static constexpr int BETA = GAM + 256;       // float[64]
+    static constexpr int MASK = BETA + 256;      // u64[64]   path(i) incl. i
+    static constexpr int BAR = MASK + 512;       // u64[3]
+    static constexpr int TMEMSLOT = BAR + 24;    // u32
+    static constexpr int FLAG = TMEMSLOT + 4;    // int
+    static constexpr int DMAX = FLAG + 4;        // int: tree depth
+    static constexpr int PLIST = DMAX + 4;       // u8[64][64]: path(i) from the root down
+    static constexpr int TOTAL = PLIST + TP * TP;
+    // Neumann: P^T hi/lo operand [64 rows][64] tf32 (after the small arrays)
+    static constexpr int PH = (TOTAL + 1023) & ~1023;
+    static constexpr int PL = PH + 16384;
+    static constexpr int P_ATOM = 64 * 128;
+    static constexpr int TOTAL_NEU = PL + 16384;
+    static_assert(P1_END <= SMALL && MT + TP * RS * 4 <= VT && P2_END <= SMALL && RL + 2 * R_ATOM <= VT,
+                  "layout");
 };
-
-// TMEM columns: X [0, BV), AC [BV, BV + 64); the Neumann variant adds
-// Y [BV + 64, 2 BV + 64) for the per-round products G Z.
-template <int BV, bool NEU>
-__host__ __device__ constexpr uint32_t tmem_cols() {
-    return (NEU && BV == 64) ? 256u : 128u;
-}
 
 struct Params {
     const __nv_bfloat16* v;
@@ -93,42 +105,38 @@ struct Params {
 __device__ inline float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ inline float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One element (column c, node i) of a K-major tf32 B operand [BV][64] in the
-// 128-byte swizzle layout: node i sits in atom i/32, 16-byte chunk (i%32)/4.
-template <int BV>
-__device__ inline void store_zt(uint8_t* base, int c, int i, float x) {
-    const int atom = i >> 5, chunk = (i & 31) >> 2;
-    *reinterpret_cast<uint32_t*>(base + atom * (BV * 128) + c * 128 + ((chunk ^ (c & 7)) << 4) + ((i & 3) << 2)) =
-        to_tf32(x);
+// tf32 hi/lo split for the three-product scheme: hi keeps the top 10
+// mantissa bits (exact in tf32), lo = x - hi is exact in fp32; the tensor core
+// reads lo to 10 bits, so hi + lo carries x to within 2^-20 |x|.
+__device__ inline void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = __float_as_uint(x) & 0xFFFFE000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
-// Raw 64-column AC row of this thread's TMEM lane into a padded smem row.
-__device__ inline void ac_row_to_smem(uint32_t lane_base, int acol, float* row) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld16(lane_base + acol + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tmem_ld16(lane_base + acol + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tmem_wait_ld();
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) row[32 * half + jj] = __uint_as_float(r[jj]);
-    }
+// Byte offset of element (row n, K index k) of a K-major tf32 operand in the
+// 128-byte swizzle layout with `rows` rows per 32-wide K atom.
+__device__ inline int kmajor_tf32_off(int n, int k, int rows) {
+    return (k >> 5) * (rows * 128) + n * 128 + ((((k & 31) >> 2) ^ (n & 7)) << 4) + ((k & 3) << 2);
 }
 
-// Bounded wait on an mbarrier phase by warp 0 only; the result is shared
-// through sFlag and agreed on at the barrier that follows.
-__device__ inline void warp0_wait(uint64_t* bar, uint32_t parity, int warp, int* sFlag) {
-    if (warp == 0) {
-        const bool ok = mbar_wait(bar, parity);
-        if (!ok && (threadIdx.x & 31) == 0) *sFlag = 1;
-    }
+// The k-th (0-based) set bit of a 64-bit mask.
+__device__ inline int nth_bit(uint64_t m, int k) {
+    const uint32_t lo = uint32_t(m), hi = uint32_t(m >> 32);
+    const int c = __popc(lo);
+    return (k < c) ? int(__fns(lo, 0, k + 1)) : 32 + int(__fns(hi, 0, k - c + 1));
 }
 
-template <int BV, bool NEU>
-__global__ void __launch_bounds__(128, 4)
-    verify_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, Params p) {
-    using L = Smem<BV>;
-    constexpr int NCC = BV / 32;  // value columns per lane
+// Bounded wait on an mbarrier phase by warp 0; a timeout is recorded in sFlag.
+__device__ inline void warp0_wait(uint64_t* bar, uint32_t parity, int* sFlag) {
+    const bool ok = mbar_wait(bar, parity);
+    if (!ok && (threadIdx.x & 31) == 0) *sFlag = 1;
+}
+
+template <bool NEU>
+__global__ void __launch_bounds__(NT, 2)
+    verify_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, Params p) {
+    using L = Smem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -142,46 +150,46 @@ __global__ void __launch_bounds__(128, 4)
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
     int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
     int* sDmax = reinterpret_cast<int*>(sm + L::DMAX);
-    int* sCnt = reinterpret_cast<int*>(sm + L::CNT);
-    int* sStart = reinterpret_cast<int*>(sm + L::START);
-    int* sLvl = reinterpret_cast<int*>(sm + L::LVL);
-    float* sG = reinterpret_cast<float*>(sm + L::GS);
-    float* sC = reinterpret_cast<float*>(sm + L::CS);
-    float* sR = reinterpret_cast<float*>(sm + L::RR);
-    float* sU = reinterpret_cast<float*>(sm + L::UR);
+    uint8_t* sPath = sm + L::PLIST;
+    float* sC = reinterpret_cast<float*>(sm + L::CT);
+    float* sG = reinterpret_cast<float*>(sm + L::GT);
+    float* sW = reinterpret_cast<float*>(sm + L::WT);
+    float* sM = reinterpret_cast<float*>(sm + L::MT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int vt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int quad = warp & 3, half = warp >> 2;      // TMEM lane quadrant, column half
+    const int row = quad * 32 + lane;                 // TMEM lane: 0..63 Q rows, 64..127 K rows
+    const int h = blockIdx.x, b = blockIdx.y;
     const int T = p.T, H = p.H;
-    const int v0 = vt * BV;
+    uint32_t mma_phase = 0;
+    bool v_issued = false;
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        mbar_init(&bars[0], 1);  // Q/K
+        mbar_init(&bars[1], 1);  // MMA completions
+        mbar_init(&bars[2], 1);  // V
         fence_mbar_init();
         *sFlag = 0;
         *sDmax = 0;
     }
     if (warp == 0) {
-        tmem_alloc(sTmem, tmem_cols<BV, NEU>());
+        tmem_alloc(sTmem, NEU ? kTmemColsNeu : kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
 
-    // S0 value tile: BV rows x 128 fp32, contiguous; 16-byte coalesced loads.
-    constexpr int NS = BV / 4;
-    float4 s0r[NS];
+    // S0 (128 rows x 128 fp32 = 64 KiB, contiguous): 16-byte coalesced loads
+    // issued first; the values are converted once the tables are done.
+    float4 s0r[16];
     {
-        const float4* src = reinterpret_cast<const float4*>(p.S0 + ((size_t(b) * H + h) * DV + v0) * DK);
+        const float4* src = reinterpret_cast<const float4*>(p.S0 + (size_t(b) * H + h) * DV * DK);
 #pragma unroll
-        for (int u = 0; u < NS; ++u) s0r[u] = __ldg(src + u * 128 + tid);
+        for (int u = 0; u < 16; ++u) s0r[u] = __ldg(src + u * NT + tid);
     }
     // Parents and gates; padded nodes get no path, beta = 0 and gamma = 1.
-    uint32_t vw[BV / 2];
     int bad = 0;
     if (tid < TP) {
         const int i = tid;
-        sCnt[i] = 0;
         int par = -1;
         float a = 1.f, be = 0.f;
         if (i < T) {
@@ -207,6 +215,7 @@ __global__ void __launch_bounds__(128, 4)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sTmem;
+    const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
 
     uint8_t* sQK = sm + L::QK;
     if (tid == 0) {
@@ -219,16 +228,18 @@ __global__ void __launch_bounds__(128, 4)
 
     // Tree prep (threads 0..63 own nodes; the whole CTA takes the barriers).
     jump_paths<1>(TP, sPtr, sLen, sL2, sMask);
-    int rank = 0;
     if (tid < TP) {
         const int i = tid;
         if (i >= T) sMask[i] = 0ull;  // padded nodes: empty path
         sGam[i] = exp2f(sL2[i]);
         if (i < T) {
             atomicMax(sDmax, sLen[i] - 1);
-            rank = atomicAdd(&sCnt[sLen[i] - 1], 1);
-            if (vt == 0) p.l[(size_t(b) * T + i) * H + h] = sL2[i] * 0.69314718055994531f;
-            if (vt == 0 && h == 0) {
+            // root path of i as a list of node ids, root first
+            int d = 0;
+            for (uint64_t bits = sMask[i]; bits; bits &= bits - 1)
+                sPath[i * TP + d++] = uint8_t(__ffsll(static_cast<long long>(bits)) - 1);
+            p.l[(size_t(b) * T + i) * H + h] = sL2[i] * 0.69314718055994531f;
+            if (h == 0) {
                 p.depth[size_t(b) * T + i] = sLen[i] - 1;
                 const uint64_t strict = sMask[i] & ~(1ull << i);
                 for (int w = 0; w < p.W; ++w)
@@ -237,38 +248,14 @@ __global__ void __launch_bounds__(128, 4)
         }
     }
     __syncthreads();
-    // Nodes grouped by depth level (order within a level is irrelevant: the
-    // nodes of one level never depend on each other).
-    if (warp == 0) {
-        // exclusive scan of the level counts by one warp (levels < 64)
-        const int dmax = *sDmax;
-        int c0 = (lane <= dmax) ? sCnt[lane] : 0;
-        int c1 = (lane + 32 <= dmax) ? sCnt[lane + 32] : 0;
-        int x0 = c0, x1 = c1;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y0 = __shfl_up_sync(0xffffffffu, x0, off);
-            const int y1 = __shfl_up_sync(0xffffffffu, x1, off);
-            if (lane >= off) {
-                x0 += y0;
-                x1 += y1;
-            }
-        }
-        const int tot0 = __shfl_sync(0xffffffffu, x0, 31);
-        const int tot1 = __shfl_sync(0xffffffffu, x1, 31);  // every lane takes part in the shuffle
-        sStart[lane] = x0 - c0;
-        sStart[lane + 32] = tot0 + x1 - c1;
-        if (lane == 0) sStart[64] = tot0 + tot1;
-    }
-    __syncthreads();
-    if (tid < T) sLvl[sStart[sLen[tid] - 1] + rank] = tid;
 
-    // S0 tile -> bf16 hi and lo planes, K-major with the 128-byte swizzle.
+    // S0 -> bf16 hi and lo planes (K-major, 128-byte swizzle), while the
+    // tree prep is done.
     {
         uint8_t* sS = sm + L::S;
 #pragma unroll
-        for (int u = 0; u < NS; ++u) {
-            const int f = u * 128 + tid;
+        for (int u = 0; u < 16; ++u) {
+            const int f = u * NT + tid;
             const int r = f >> 5, c4 = f & 31;
             const int atom = c4 >> 4, chunk = (c4 & 15) >> 1;
             const int off = atom * L::S_ATOM + r * 128 + ((chunk ^ (r & 7)) << 4) + ((c4 & 1) << 3);
@@ -283,29 +270,11 @@ __global__ void __launch_bounds__(128, 4)
                 make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
         }
     }
-    // V rows for the K-row threads (lane 64 + i holds node i): BV bf16;
-    // issued here so their latency overlaps the first MMAs.
-    {
-        const int i = tid - 64;
-        if (tid >= 64 && i < T) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.v + ((size_t(b) * T + i) * H + h) * DV + v0);
-#pragma unroll
-            for (int u = 0; u < BV / 8; ++u) {
-                uint4 x = __ldg(src + u);
-                vw[4 * u] = x.x;
-                vw[4 * u + 1] = x.y;
-                vw[4 * u + 2] = x.z;
-                vw[4 * u + 3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < BV / 2; ++u) vw[u] = 0;
-        }
-    }
     fence_proxy_async_smem();
     __syncthreads();
 
-    // First MMAs: X = [Q;K] (S0hi + S0lo)^T and AC = [Q;K] K^T.
+    // AC = [Q;K] K^T into the A-hi columns (rewritten later with [M; W]) and
+    // X = [Q;K] S0^T, one commit.
     if (warp == 0) {
         const bool ok = mbar_wait(&bars[0], 0);
         if (lane == 0) {
@@ -316,171 +285,165 @@ __global__ void __launch_bounds__(128, 4)
                 const uint32_t aQK = smem_u32(sQK);
                 const uint32_t aS = smem_u32(sm + L::S);
 #pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
+                    const uint64_t db = sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32);
+                    mma_bf16_ss(tmem + AH, da, db, idesc_bf16(128, 64), ks != 0);
+                }
+                // X = [Q;K] (S0hi + S0lo)^T, N = 128
+#pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
                         const uint64_t db =
                             sdesc_sw128(aS + part * L::S_PLANE + (ks >> 2) * L::S_ATOM + (ks & 3) * 32);
-                        mma_bf16_ss(tmem, da, db, idesc_bf16(128, BV), (part | ks) != 0);
+                        mma_bf16_ss(tmem + XC, da, db, idesc_bf16(128, 128), (part | ks) != 0);
                     }
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
-                    const uint64_t db = sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32);
-                    mma_bf16_ss(tmem + BV, da, db, idesc_bf16(128, 64), ks != 0);
-                }
                 mma_commit(&bars[1]);
             }
         }
         __syncwarp();
-        if (*sFlag == 0) warp0_wait(&bars[1], 0, warp, sFlag);
+        if (*sFlag == 0) warp0_wait(&bars[1], mma_phase, sFlag);
+    }
+    mma_phase ^= 1;
+    __syncthreads();
+    if (*sFlag) goto fail;
+    tc_fence_after();
+    // V (64 nodes x 128 columns bf16) by TMA into the space the products freed
+    if (tid == 0) {
+        v_issued = true;
+        mbar_expect_tx(&bars[2], 2 * L::V_TILE);
+        tma_load_4d(sm + L::VT, &tmV, &bars[2], 0, h, 0, b);
+        tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[2], 64, h, 0, b);
+    }
+
+    // C rows (Q lanes) and G rows (K lanes) into shared memory: raw products,
+    // then the decay (and beta) on the path entries, the only ones read
+    // later; each warp takes 32 of the 64 columns.  W starts as the identity,
+    // M as zero.
+    {
+        const bool qrow = row < 64;
+        const int i = qrow ? row : row - 64;
+        const int j0 = 32 * half;
+        float* trow = (qrow ? sC : sG) + i * RS;
+        uint32_t r[32];
+        tmem_ld16(lane_base + AH + j0, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tmem_ld16(lane_base + AH + j0 + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) trow[j0 + jj] = __uint_as_float(r[jj]);
+        // decay (and beta for G) on this row's path entries in this half
+        const float li = sL2[i];
+        const float scale = qrow ? 1.f : sBeta[i];
+        const uint64_t m = qrow ? sMask[i] : (sMask[i] & ~(1ull << i));
+        for (uint32_t bits = uint32_t(m >> j0); bits; bits &= bits - 1) {
+            const int j = j0 + __ffs(bits) - 1;
+            trow[j] *= scale * exp2f(li - sL2[j]);
+        }
+        if (NEU) {
+            for (int e = tid; e < TP * TP; e += NT) {
+                const int a = e >> 6, c = e & 63;
+                sW[a * RS + c] = (a == c) ? 1.f : 0.f;
+                sM[a * RS + c] = 0.f;
+            }
+        }
     }
     __syncthreads();
-    if (*sFlag) {
-        if (tid == 0) {
-            raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
-            mbar_wait(&bars[0], 0);  // let copies in flight land before leaving
-        }
-        goto teardown;
-    }
-    tc_fence_after();
-
-    {
-        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-        if (warp < 2) {
-            // Q rows: C row i (raw Q K^T, then the decay on the path entries,
-            // the only ones the output reads).
-            const int i = tid;
-            const float li = sL2[i];
-            float* crow = sC + i * RS;
-            ac_row_to_smem(lane_base, BV, crow);
-            for (uint64_t bits = sMask[i]; bits; bits &= bits - 1) {
-                const int j = __ffsll(static_cast<long long>(bits)) - 1;
-                crow[j] *= exp2f(li - sL2[j]);
-            }
-        } else {
-            const int i = tid - 64;
-            const float li = sL2[i], bi = sBeta[i], gi = sGam[i];
-            const uint64_t ms = sMask[i] & ~(1ull << i);
-            if constexpr (!NEU) {
-                // K rows: G row i on the strict ancestors, and R row i.
-                float* grow = sG + i * RS;
-                ac_row_to_smem(lane_base, BV, grow);
-                for (uint64_t bits = ms; bits; bits &= bits - 1) {
-                    const int j = __ffsll(static_cast<long long>(bits)) - 1;
-                    grow[j] *= bi * exp2f(li - sL2[j]);
-                }
-                float* rrow = sR + i * (BV + 1);
-#pragma unroll
-                for (int cb = 0; cb < BV / 16; ++cb) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_base + cb * 16, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int c = cb * 16 + jj;
-                        const float vv = (c & 1) ? bf16_hi(vw[c >> 1]) : bf16_lo(vw[c >> 1]);
-                        rrow[c] = bi * (vv - gi * __uint_as_float(r[jj]));
-                    }
-                }
-            }
-        }
-    }
 
     if constexpr (!NEU) {
-        __syncthreads();
-        // Level-synchronous forward substitution over the tree (canopy page,
-        // "The tree closed form", level-synchronous solve): the nodes of one
-        // depth level depend only on shallower nodes, so each level is one
-        // parallel step.  A warp takes a node, its lanes the value columns;
-        // u_i = R_i - sum_{j in A(i)} G_ij u_j runs over the ancestor bits.
-        const int dmax = *sDmax;
-        for (int lv = 0; lv <= dmax; ++lv) {
-            const int s1 = sStart[lv + 1];
-            for (int idx = sStart[lv] + warp; idx < s1; idx += 4) {
-                const int i = sLvl[idx];
-                const float* grow = sG + i * RS;
-                float a0[NCC], a1[NCC];
-#pragma unroll
-                for (int q = 0; q < NCC; ++q) {
-                    a0[q] = sR[i * (BV + 1) + lane + 32 * q];
-                    a1[q] = 0.f;
-                }
-                uint64_t bits = sMask[i] & ~(1ull << i);
-                while (bits) {
-                    const int j0 = __ffsll(static_cast<long long>(bits)) - 1;
-                    bits &= bits - 1;
-                    const float g0 = grow[j0];
-                    const float* u0 = sU + j0 * BV + lane;
-                    if (bits) {
-                        const int j1 = __ffsll(static_cast<long long>(bits)) - 1;
-                        bits &= bits - 1;
-                        const float g1 = grow[j1];
-                        const float* u1 = sU + j1 * BV + lane;
-#pragma unroll
-                        for (int q = 0; q < NCC; ++q) {
-                            a0[q] -= g0 * u0[32 * q];
-                            a1[q] -= g1 * u1[32 * q];
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < NCC; ++q) a0[q] -= g0 * u0[32 * q];
+        // W = (I + G)^-1 and M = C W, row by row.  From W (I + G) = I and
+        // M (I + G) = C, for node i and k on its root path,
+        //   W_ik = [i = k] - sum_{e in path(i) below k} W_ie G_ek,
+        //   M_ik =  C_ik   - sum_{e in path(i) below k} M_ie G_ek,
+        // so row i follows from walking i's root path from i upwards; rows
+        // are independent (no level barriers).  One thread per row: the Q
+        // lanes (threads 0..63) build the M rows, the K lanes (64..127) the W
+        // rows, each on its own row in shared memory, then write that row to
+        // its tensor-memory lane as the A operand (tf32 hi + lo, zero off the
+        // path).
+        if (warp < 4) {
+            const bool qrow = row < 64;
+            const int i = qrow ? row : row - 64;
+            float* orow = (qrow ? sM : sW) + i * RS;
+            if (i < T) {
+                const float* crow = sC + i * RS;
+                const uint8_t* pl = sPath + i * TP;
+                const int n = sLen[i];  // path length, i is at position n - 1
+                for (int d = n - 1; d >= 0; --d) {
+                    const int k = pl[d];
+                    float a0 = qrow ? crow[k] : ((d == n - 1) ? 1.f : 0.f), a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    int e = d + 1;
+                    for (; e + 3 < n; e += 4) {
+                        const int e0 = pl[e], e1 = pl[e + 1], e2 = pl[e + 2], e3 = pl[e + 3];
+                        a0 -= orow[e0] * sG[e0 * RS + k];
+                        a1 -= orow[e1] * sG[e1 * RS + k];
+                        a2 -= orow[e2] * sG[e2 * RS + k];
+                        a3 -= orow[e3] * sG[e3 * RS + k];
                     }
-                }
-                float* ug = p.U + ((size_t(b) * T + i) * H + h) * DV + v0 + lane;
-#pragma unroll
-                for (int q = 0; q < NCC; ++q) {
-                    const float u = a0[q] + a1[q];
-                    sU[i * BV + lane + 32 * q] = u;
-                    ug[32 * q] = u;
+                    for (; e < n; ++e) {
+                        const int e0 = pl[e];
+                        a0 -= orow[e0] * sG[e0 * RS + k];
+                    }
+                    orow[k] = (a0 + a1) + (a2 + a3);
                 }
             }
-            __syncthreads();
-        }
-    } else {
-        // Finite Neumann series (Bole's solve): U = sum_{m=0..d} (-G)^m R.
-        // Each round is one tcgen05 tf32 MMA, A = [.; G] read from TMEM (the
-        // K rows of the AC block, overwritten with G), B = Z^T from shared
-        // memory; rows 64..127 of the product are G Z_{m-1}, so
-        // Z_m = -G Z_{m-1}.  d rounds for a tree of depth d.
-        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-        uint8_t* sZt = sm + L::ZT;
-        float acc[BV];  // K rows: U row
-        const int i = tid - 64;
-        if (warp >= 2) {
-            const float li = sL2[i], bi = sBeta[i], gi = sGam[i];
-            const uint64_t ms = sMask[i] & ~(1ull << i);
+            // row -> tensor memory (whole warps; rows past T are zero)
+            const uint64_t pm = (i < T) ? sMask[i] : 0ull;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + BV + cb * 16, r);
-                tmem_wait_ld();
+                uint32_t rh[16], rl[16];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int j = cb * 16 + jj;
-                    const float gv = ((ms >> j) & 1ull) ? bi * __uint_as_float(r[jj]) * exp2f(li - sL2[j]) : 0.f;
-                    r[jj] = to_tf32(gv);
+                    const float x = ((pm >> j) & 1ull) ? orow[j] : 0.f;
+                    split_tf32(x, rh[jj], rl[jj]);
                 }
-                tmem_st16(lane_base + BV + cb * 16, r);
-            }
-#pragma unroll
-            for (int cb = 0; cb < BV / 16; ++cb) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + cb * 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int c = cb * 16 + jj;
-                    const float vv = (c & 1) ? bf16_hi(vw[c >> 1]) : bf16_lo(vw[c >> 1]);
-                    acc[c] = bi * (vv - gi * __uint_as_float(r[jj]));
-                    store_zt<BV>(sZt, c, i, acc[c]);
-                }
+                tmem_st16(lane_base + AH + cb * 16, rh);
+                tmem_st16(lane_base + AL + cb * 16, rl);
             }
             tmem_wait_st();
         }
+        __syncthreads();
+    } else {
+        // Finite Neumann series (Bole's solve) for W = sum_{m=0..d} (-G)^m on
+        // tcgen05: P_0 = I, P_m = -G P_{m-1}, d rounds; G is the A operand in
+        // tensor memory (K rows, tf32 hi + lo), P^T the B operand in shared
+        // memory (tf32 hi + lo); each round is hi*hi + hi*lo + lo*hi.
+        uint8_t* sPh = sm + L::PH;
+        uint8_t* sPl = sm + L::PL;
+        float wacc[32];  // K rows: this thread's 32 columns of its W row
+        const int i = row - 64;
+        const int jb = half * 32;
+        if (quad >= 2) {
+            // G row -> A hi/lo (K lanes, columns AH/AL); P_0 = I
+            if (half == 0) {
+                const uint64_t ms = sMask[i] & ~(1ull << i);
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t rh[16], rl[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = cb * 16 + jj;
+                        const float x = ((ms >> j) & 1ull) ? sG[i * RS + j] : 0.f;
+                        split_tf32(x, rh[jj], rl[jj]);
+                    }
+                    tmem_st16(lane_base + AH + cb * 16, rh);
+                    tmem_st16(lane_base + AL + cb * 16, rl);
+                }
+                tmem_wait_st();
+            }
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = jb + jj;
+                const float x = (j == i) ? 1.f : 0.f;
+                wacc[jj] = x;
+                // P^T[n = j][k = i] (K-major, 64 rows)
+                *reinterpret_cast<uint32_t*>(sPh + kmajor_tf32_off(j, i, 64)) = to_tf32(x);
+                *reinterpret_cast<uint32_t*>(sPl + kmajor_tf32_off(j, i, 64)) = 0u;
+            }
+        }
         const int rounds = *sDmax;
-        uint32_t parity = 1;
         for (int m = 1; m <= rounds; ++m) {
             fence_proxy_async_smem();
             tc_fence_before();
@@ -488,119 +451,227 @@ __global__ void __launch_bounds__(128, 4)
             if (warp == 0) {
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t aZ = smem_u32(sZt);
+                    const uint32_t aH = smem_u32(sPh), aL = smem_u32(sPl);
+                    // G P into the spare columns
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t db = sdesc_sw128(aZ + (ks >> 2) * (BV * 128) + (ks & 3) * 32);
-                        mma_tf32_ts(tmem + BV + 64, tmem + BV + ks * 8, db, idesc_tf32(128, BV), ks != 0);
-                    }
+                    for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t acol = (pass == 2 ? AL : AH) + ks * 8;
+                            const uint32_t bb = (pass == 1 ? aL : aH) + (ks >> 2) * L::P_ATOM + (ks & 3) * 32;
+                            mma_tf32_ts(tmem + YC, tmem + acol, sdesc_sw128(bb), idesc_tf32(128, 64),
+                                        (pass | ks) != 0);
+                        }
                     mma_commit(&bars[1]);
                 }
                 __syncwarp();
-                warp0_wait(&bars[1], parity, warp, sFlag);
+                warp0_wait(&bars[1], mma_phase, sFlag);
             }
-            parity ^= 1;
+            mma_phase ^= 1;
             __syncthreads();
-            if (*sFlag) {
-                if (tid == 0) raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
-                goto teardown;
-            }
+            if (*sFlag) goto fail;
             tc_fence_after();
-            if (warp >= 2) {
+            if (quad >= 2) {
+                uint32_t r[32];
+                tmem_ld16(lane_base + YC + jb, *reinterpret_cast<uint32_t(*)[16]>(r));
+                tmem_ld16(lane_base + YC + jb + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+                tmem_wait_ld();
                 const bool last = (m == rounds);
 #pragma unroll
-                for (int cb = 0; cb < BV / 16; ++cb) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_base + BV + 64 + cb * 16, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int c = cb * 16 + jj;
-                        const float z = -__uint_as_float(r[jj]);
-                        acc[c] += z;
-                        if (!last) store_zt<BV>(sZt, c, i, z);
+                for (int jj = 0; jj < 32; ++jj) {
+                    const float z = -__uint_as_float(r[jj]);
+                    wacc[jj] += z;
+                    if (!last) {
+                        uint32_t zh, zl;
+                        split_tf32(z, zh, zl);
+                        *reinterpret_cast<uint32_t*>(sPh + kmajor_tf32_off(jb + jj, i, 64)) = zh;
+                        *reinterpret_cast<uint32_t*>(sPl + kmajor_tf32_off(jb + jj, i, 64)) = zl;
                     }
                 }
             }
         }
-        __syncthreads();  // the last round's Z^T reads are done before sU overwrites
-        if (warp >= 2) {
+        if (quad >= 2) {
 #pragma unroll
-            for (int c = 0; c < BV; ++c) sU[i * BV + c] = acc[c];
-            if (i < T) {
-                float4* dst = reinterpret_cast<float4*>(p.U + ((size_t(b) * T + i) * H + h) * DV + v0);
+            for (int jj = 0; jj < 32; ++jj) sW[i * RS + jb + jj] = wacc[jj];
+        }
+        __syncthreads();
+        // M = C W: M_i. = sum_{k in path(i)} C_ik W_k. (zero off the paths,
+        // since W_k. is); one warp per row, lanes over columns.
+        for (int i2 = warp; i2 < TP; i2 += NT / 32) {
+            const uint64_t pi = sMask[i2];
+            const float* crow = sC + i2 * RS;
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < BV / 4; ++e)
-                    dst[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+            for (int wd = 0; wd < 2; ++wd) {
+                uint32_t bits = uint32_t(pi >> (32 * wd));
+                while (bits) {
+                    const int k = 32 * wd + __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const float ck = crow[k];
+                    a0 += ck * sW[k * RS + lane];
+                    a1 += ck * sW[k * RS + lane + 32];
+                }
             }
+            sM[i2 * RS + lane] = a0;
+            sM[i2 * RS + lane + 32] = a1;
         }
         __syncthreads();
     }
 
-    // gamma X_Q rows into shared memory (over G, no longer needed) so that
-    // the output can run with lanes over columns.
-    if (warp < 2) {
-        const int i = tid;
-        const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-        const float gi = sGam[i];
-        float* xrow = sG + i * (BV + 1);
-#pragma unroll
-        for (int cb = 0; cb < BV / 16; ++cb) {
-            uint32_t r[16];
-            tmem_ld16(lane_base + cb * 16, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) xrow[cb * 16 + jj] = gi * __uint_as_float(r[jj]);
-        }
-    }
-    __syncthreads();
 
-    // Output on CUDA cores in fp32, one warp per node, lanes over columns:
-    // o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
-    for (int i = warp; i < T; i += 4) {
-        const float* crow = sC + i * RS;
-        float a0[NCC], a1[NCC];
-#pragma unroll
-        for (int q = 0; q < NCC; ++q) {
-            a0[q] = sG[i * (BV + 1) + lane + 32 * q];
-            a1[q] = 0.f;
-        }
-        uint64_t bits = sMask[i];
-        while (bits) {
-            const int j0 = __ffsll(static_cast<long long>(bits)) - 1;
-            bits &= bits - 1;
-            const float c0 = crow[j0];
-            const float* u0 = sU + j0 * BV + lane;
-            if (bits) {
-                const int j1 = __ffsll(static_cast<long long>(bits)) - 1;
-                bits &= bits - 1;
-                const float c1 = crow[j1];
-                const float* u1 = sU + j1 * BV + lane;
-#pragma unroll
-                for (int q = 0; q < NCC; ++q) {
-                    a0[q] += c0 * u0[32 * q];
-                    a1[q] += c1 * u1[32 * q];
+    if constexpr (NEU) {
+        // [M; W] -> tensor memory as tf32 hi and lo; each warp takes 32 columns.
+        {
+            const bool qrow = row < 64;
+            const int i = qrow ? row : row - 64;
+            const float* trow = (qrow ? sM : sW) + i * RS;
+            const uint64_t pm = sMask[i];
+    #pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                const int j0 = 32 * half + 16 * cb;
+                uint32_t rh[16], rl[16];
+    #pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float x = ((pm >> (j0 + jj)) & 1ull) ? trow[j0 + jj] : 0.f;
+                    split_tf32(x, rh[jj], rl[jj]);
                 }
-            } else {
+                tmem_st16(lane_base + AH + j0, rh);
+                tmem_st16(lane_base + AL + j0, rl);
+            }
+            tmem_wait_st();
+        }
+        __syncthreads();
+    }
+
+    // V must have landed (all threads check the same phase; bounded wait)
+    if (!mbar_wait(&bars[2], 0)) *sFlag = 1;
+    __syncthreads();
+    if (*sFlag) goto fail;
+    // Q lanes: gamma X_Q in place.  K lanes: R = beta (V - gamma X_K) -> R^T
+    // hi/lo in shared memory, then zero X_K so the product below leaves U.
+    {
+        const bool qrow = row < 64;
+        const int i = qrow ? row : row - 64;
+        const float gi = sGam[i], bi = sBeta[i];
+        uint8_t* sRh = sm + L::RH;
+        uint8_t* sRl = sm + L::RL;
+        // element (column c, node i) of the K-major R^T operand: atom i/32,
+        // row c, 16-byte chunk ((i%32)/4) ^ (c%8), word i%4
+        const int ibase = (i >> 5) * L::R_ATOM + ((i & 3) << 2);
+        const int ichunk = (i & 31) >> 2;
+        uint32_t vw[32];
+        if (!qrow) {
+            const uint8_t* vrow = sm + L::VT + half * L::V_TILE + i * 128;
 #pragma unroll
-                for (int q = 0; q < NCC; ++q) a0[q] += c0 * u0[32 * q];
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 x = *reinterpret_cast<const uint4*>(vrow + ((ch ^ (i & 7)) << 4));
+                vw[4 * ch] = x.x;
+                vw[4 * ch + 1] = x.y;
+                vw[4 * ch + 2] = x.z;
+                vw[4 * ch + 3] = x.w;
             }
         }
-        const size_t ob = ((size_t(b) * T + i) * H + h) * DV + v0 + lane;
 #pragma unroll
-        for (int q = 0; q < NCC; ++q) {
-            const float x = a0[q] + a1[q];
-            if (p.o_bf16)
-                static_cast<__nv_bfloat16*>(p.o)[ob + 32 * q] = __float2bfloat16_rn(x);
-            else
-                static_cast<float*>(p.o)[ob + 32 * q] = x;
+        for (int cb = 0; cb < 4; ++cb) {
+            const int c0 = 64 * half + cb * 16;
+            uint32_t r[16];
+            tmem_ld16(lane_base + XC + c0, r);
+            tmem_wait_ld();
+            if (qrow) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) r[jj] = __float_as_uint(gi * __uint_as_float(r[jj]));
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int cw = cb * 16 + jj;  // column within this warp's 64
+                    const float vv = (cw & 1) ? bf16_hi(vw[cw >> 1]) : bf16_lo(vw[cw >> 1]);
+                    const float rr = bi * (vv - gi * __uint_as_float(r[jj]));
+                    uint32_t rh, rl;
+                    split_tf32(rr, rh, rl);
+                    const int c = c0 + jj;
+                    const int off = ibase + c * 128 + ((ichunk ^ (c & 7)) << 4);
+                    *reinterpret_cast<uint32_t*>(sRh + off) = rh;
+                    *reinterpret_cast<uint32_t*>(sRl + off) = rl;
+                    r[jj] = 0u;
+                }
+            }
+            tmem_st16(lane_base + XC + c0, r);
         }
+        tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // X += [M; W] R with three tf32 products (hi*hi + hi*lo + lo*hi).
+    if (warp == 0) {
+        if (lane == 0) {
+            tc_fence_after();
+            const uint32_t aRh = smem_u32(sm + L::RH), aRl = smem_u32(sm + L::RL);
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t acol = (pass == 2 ? AL : AH) + ks * 8;
+                    const uint32_t bb = (pass == 1 ? aRl : aRh) + (ks >> 2) * L::R_ATOM + (ks & 3) * 32;
+                    mma_tf32_ts(tmem + XC, tmem + acol, sdesc_sw128(bb), idesc_tf32(128, 128), 1);
+                }
+            mma_commit(&bars[1]);
+        }
+        __syncwarp();
+        warp0_wait(&bars[1], mma_phase, sFlag);
+    }
+    mma_phase ^= 1;
+    __syncthreads();
+    if (*sFlag) goto fail;
+    tc_fence_after();
+
+    // Rows 0..63 are o, rows 64..127 are U.
+    {
+        const bool qrow = row < 64;
+        const int i = qrow ? row : row - 64;
+        const bool live = i < T;
+        const size_t nb = ((size_t(b) * T + (live ? i : 0)) * H + h) * DV + 64 * half;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t r[16];
+            tmem_ld16(lane_base + XC + 64 * half + cb * 16, r);
+            tmem_wait_ld();
+            if (!live) continue;
+            if (qrow && p.o_bf16) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const __nv_bfloat162 pr =
+                        __floats2bfloat162_rn(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                    w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + nb + cb * 16);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+                float* base = qrow ? static_cast<float*>(p.o) : p.U;
+                float4* dst = reinterpret_cast<float4*>(base + nb + cb * 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                         __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            }
+        }
+    }
+    goto teardown;
+
+fail:
+    if (tid == 0) {
+        raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
+        mbar_wait(&bars[0], 0);  // let copies in flight land before leaving
+        if (v_issued) mbar_wait(&bars[2], 0);
     }
 
 teardown:
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, tmem_cols<BV, NEU>());
+    if (warp == 0) tmem_dealloc(tmem, NEU ? kTmemColsNeu : kTmemCols);
 }
 
 }  // namespace tc
@@ -626,7 +697,8 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [B][T][H][128] bf16 -> boxes of 64 (dk) x 64 (nodes) with the 128-byte swizzle.
+// [B][T][H][128] bf16 (q, k or v) -> boxes of 64 (last dim) x 64 (nodes) with
+// the 128-byte swizzle.
 static bool make_qk_map(CUtensorMap* m, const void* base, int B, int T, int H) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -639,26 +711,29 @@ static bool make_qk_map(CUtensorMap* m, const void* base, int B, int T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BV, bool NEU>
+template <bool NEU>
 static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
-    CUtensorMap mq, mk;
-    if (!make_qk_map(&mq, q, prm.B, prm.T, prm.H) || !make_qk_map(&mk, k, prm.B, prm.T, prm.H))
+    CUtensorMap mq, mk, mv;
+    if (!make_qk_map(&mq, q, prm.B, prm.T, prm.H) || !make_qk_map(&mk, k, prm.B, prm.T, prm.H) ||
+        !make_qk_map(&mv, prm.v, prm.B, prm.T, prm.H))
         return cudaErrorInvalidValue;
-    const int smem = tc::Smem<BV>::TOTAL + 1024;
+    const int smem = (NEU ? tc::Smem::TOTAL_NEU : tc::Smem::TOTAL) + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc::verify_kernel<BV, NEU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(tc::verify_kernel<NEU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid(tc::DV / BV, prm.H, prm.B);
-    tc::verify_kernel<BV, NEU><<<grid, 128, smem, st>>>(mq, mk, prm);
+    dim3 grid(prm.H, prm.B);
+    tc::verify_kernel<NEU><<<grid, tc::NT, smem, st>>>(mq, mk, mv, prm);
     return cudaGetLastError();
 }
 
 cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                              const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
                              const Ws& ws, int bv, int neumann, cudaStream_t st) {
+    (void)bv;
     tc::Params prm;
     prm.v = static_cast<const __nv_bfloat16*>(v);
     prm.g = g;
@@ -676,9 +751,8 @@ cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const 
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
-    if (neumann) return launch_tc<32, true>(q, k, prm, st);
-    if (bv == 64) return launch_tc<64, false>(q, k, prm, st);
-    return launch_tc<32, false>(q, k, prm, st);
+    if (neumann) return launch_tc<true>(q, k, prm, st);
+    return launch_tc<false>(q, k, prm, st);
 }
 
 }  // namespace canopy

@@ -70,6 +70,31 @@ def test_shapes_bf16(lib, fam, T):
     assert rel_err(o.cpu().numpy(), o_ref) <= TOL_BF16
 
 
+@pytest.mark.parametrize("fam", ["chain", "top2", "top4", "skewed", "random"])
+@pytest.mark.parametrize("T", [1, 2, 5, 16, 33, 64])
+def test_neumann_variant(lib, fam, T):
+    """The finite Neumann series solve (canopy page, "Design decisions") gives
+    outputs and, through commit, pseudo-values that match the oracle."""
+    inp = _inputs(T, fam)
+    o_ref, S_ref = oracle_outputs(inp, keep_states=True)
+    dev = to_device(inp, bf16=True)
+    on, ws_n, err = run_verify(lib, dev, solve="neumann")
+    assert err == 0
+    assert rel_err(on.cpu().numpy(), o_ref) <= TOL_BF16
+    B = dev["q"].shape[0]
+    acc = torch.full((B,), T - 1, dtype=torch.int32, device="cuda")
+    Sn = lib.commit(acc, dev["S0"], dev["k"], ws_n, T)
+    assert lib.read_device_error(ws_n) == 0
+    assert rel_err(Sn.cpu().numpy(), S_ref[:, T - 1]) <= TOL_BF16
+
+
+def test_neumann_unsupported_beyond_64(lib):
+    inp = _inputs(65, "random")
+    dev = to_device(inp, bf16=True)
+    with pytest.raises(lib.CanopyError):
+        run_verify(lib, dev, solve="neumann")
+
+
 @pytest.mark.parametrize("fam", ["chain", "top4", "random"])
 @pytest.mark.parametrize("T", [1, 3, 17, 64, 65, 256])
 def test_shapes_fp32(lib, fam, T):
