@@ -1,7 +1,5 @@
 // extern "C" entry points of libcanopy.so: argument checks, workspace
 // binding and kernel dispatch.  See include/canopy.h for the contract.
-#include <stdlib.h>
-
 #include "common.cuh"
 
 namespace canopy {
@@ -10,6 +8,9 @@ cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B
 cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                              const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
                              const Ws& ws, int bv, int neumann, cudaStream_t st);
+cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
+                                 const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
                                cudaStream_t st);
@@ -29,16 +30,6 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 bool sizes_ok(int B, int T, int H) { return B >= 1 && H >= 1 && T >= 1 && T <= kMaxT; }
 
 canopy_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CANOPY_OK : CANOPY_ERR_CUDA; }
-
-// Value-tile width of the tensor-core verify: 32 unless CANOPY_TC_BV=64.
-int tc_tile() {
-    static int bv = -1;
-    if (bv < 0) {
-        const char* s = getenv("CANOPY_TC_BV");
-        bv = (s && atoi(s) == 64) ? 64 : 32;
-    }
-    return bv;
-}
 
 }  // namespace
 
@@ -84,9 +75,9 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
     const bool tc = in_bf16 && dk == 128 && T <= 64;
     if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
-    if (tc)
-        return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, tc_tile(),
-                                            solve == CANOPY_SOLVE_NEUMANN, st));
+    if (tc && solve == CANOPY_SOLVE_NEUMANN)
+        return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, 0, 1, st));
+    if (tc) return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, st));
     cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, st));

@@ -155,6 +155,19 @@ __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+__device__ inline void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among `n` threads (a multiple of 32) of the CTA on named barrier `id`.
+__device__ inline void group_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Ask L2 to fetch [p, p + bytes) (16-byte aligned, bytes a multiple of 16).
+__device__ inline void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor cores, TMA) before a barrier.
 __device__ inline void fence_proxy_async_smem() {
@@ -226,6 +239,15 @@ __device__ inline void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, K = 16 (A: 8 columns of
+// bf16 pairs per lane, the lower K index in the low half).
+__device__ inline void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
 // Arrive on `bar` when every MMA issued so far by this thread has completed.
 __device__ inline void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -244,6 +266,24 @@ __device__ inline void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ inline void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+// 32 lanes x 32 bits, 8 consecutive columns per thread.
+__device__ inline void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+// 16 lanes x 256 bits, 4 repetitions along the columns (32 columns): for
+// repetition k, thread t holds r[4k] = (lane t/4, column 8k + 2(t%4)),
+// r[4k+1] = the next column, r[4k+2], r[4k+3] = the same columns of lane
+// t/4 + 8 (lanes relative to the 16-lane base of the address).
+__device__ inline void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
             taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])

@@ -698,8 +698,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 // [B][T][H][128] bf16 (q, k or v) -> boxes of 64 (last dim) x 64 (nodes) with
-// the 128-byte swizzle.
-static bool make_qk_map(CUtensorMap* m, const void* base, int B, int T, int H) {
+// the 128-byte swizzle; nodes past T read as zero.
+bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {128, cuuint64_t(H), cuuint64_t(T), cuuint64_t(B)};
@@ -714,8 +714,8 @@ static bool make_qk_map(CUtensorMap* m, const void* base, int B, int T, int H) {
 template <bool NEU>
 static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
-    if (!make_qk_map(&mq, q, prm.B, prm.T, prm.H) || !make_qk_map(&mk, k, prm.B, prm.T, prm.H) ||
-        !make_qk_map(&mv, prm.v, prm.B, prm.T, prm.H))
+    if (!make_bf16_row_map(&mq, q, prm.B, prm.T, prm.H) || !make_bf16_row_map(&mk, k, prm.B, prm.T, prm.H) ||
+        !make_bf16_row_map(&mv, prm.v, prm.B, prm.T, prm.H))
         return cudaErrorInvalidValue;
     const int smem = (NEU ? tc::Smem::TOTAL_NEU : tc::Smem::TOTAL) + 1024;
     static bool attr = false;
