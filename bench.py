@@ -14,9 +14,10 @@ layer verify.
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
 device synchronise on both sides, CUDA events on the launching stream, max
-over ranks.  Each set's verify call and commit call are captured once in a
-CUDA graph, and the timed loop replays them, so the host's per-call
-marshalling does not starve the GPU.  Inputs rotate over enough independent sets that the data one
+over ranks.  The timed steps are captured once as a CUDA graph of
+consecutive steps over the rotating sets and replayed, so the host's per-call
+marshalling does not starve the GPU; per-kernel durations come from graphs of
+the same launches of one kernel alone.  Inputs rotate over enough independent sets that the data one
 step touches is not in L2 (129 MB) when the step starts.  Clocks are sampled
 with nvidia-smi during the timed region.  Under torchrun each rank runs the
 same per-GPU workload (replicas: the units are independent, no collective in
@@ -187,21 +188,22 @@ def step(canopy, s, T, solve="fwdsub"):
     canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
 
 
-def capture_graphs(canopy, sets, T, solve):
-    """One CUDA graph per set for the verify call and one for the commit call
-    (the calls' kernels and arguments, captured on a side stream)."""
+def capture_graph(canopy, sets, T, solve, n, kind):
+    """One CUDA graph of n consecutive steps over the rotating input sets:
+    kind "step" = verify + commit, "verify" or "commit" = that call alone.
+    The host-side argument marshalling runs once, at capture."""
     import torch
-    out = []
-    for s in sets:
-        gv, gc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gv):
-            canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=solve,
-                          out=s["o"])
-        with torch.cuda.graph(gc):
-            canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
-        out.append((gv, gc))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            s = sets[i % len(sets)]
+            if kind in ("step", "verify"):
+                canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=solve,
+                              out=s["o"])
+            if kind in ("step", "commit"):
+                canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
     torch.cuda.synchronize()
-    return out
+    return g
 
 
 def set_bytes(s):
@@ -225,32 +227,42 @@ def run_canopy(args, world, rank, local):
         step(canopy, sets[i % len(sets)], T, args.solve)
     torch.cuda.synchronize()
     assert canopy.read_device_error(sets[0]["ws"]) == 0
-    graphs = capture_graphs(canopy, sets, T, args.solve)
-    for i in range(args.warmup):
-        for g in graphs[i % len(sets)]:
-            g.replay()
+    G = max(len(sets), (args.graph_steps // len(sets)) * len(sets))
+    g_step = capture_graph(canopy, sets, T, args.solve, G, "step")
+    g_ver = capture_graph(canopy, sets, T, args.solve, G, "verify")
+    g_com = capture_graph(canopy, sets, T, args.solve, G, "commit")
+    K = args.steps
+    reps, rem = divmod(K, G)
+    g_rem = capture_graph(canopy, sets, T, args.solve, rem, "step") if rem else None
+    for _ in range(max(1, -(-args.warmup // G))):
+        g_step.replay()
     torch.cuda.synchronize()
 
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    for i in range(K):
-        s = sets[i % len(sets)]
-        gv, gc = graphs[i % len(sets)]
-        ev[i][0].record()
-        gv.replay()
-        ev[i][1].record()
-        gc.replay()
-        ev[i][2].record()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g_step.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record()
     torch.cuda.synchronize()
     barrier(world)
+    total_ms = e0.elapsed_time(e1)
+    # per-kernel launch durations: the same launches, one kernel kind per graph
+    t_verify, t_commit = [], []
+    for g, out in ((g_ver, t_verify), (g_com, t_commit)):
+        for _ in range(args.kernel_reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            out.append(a.elapsed_time(b) / G)
     clk = clocks.stop()
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    t_verify = [e[0].elapsed_time(e[1]) for e in ev]
-    t_commit = [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = max_over_ranks(total_ms, world)
     errs = [canopy.read_device_error(s["ws"]) for s in sets]
     assert not any(errs), errs
@@ -280,6 +292,9 @@ def run_canopy(args, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "us_per_layer_verify": v_us, "us_per_commit": c_us,
         "verify_p10_p50_p90_us": [1e3 * float(np.percentile(t_verify, p)) for p in (10, 50, 90)],
+        "timing": f"one CUDA graph of {G} steps (verify + commit, sets rotating) replayed {reps} times "
+                  f"(+ a graph of the {rem} remaining steps) between two events; per-kernel durations from graphs of {G} launches of one kernel, "
+                  f"{args.kernel_reps} replays each (p10/p50/p90 over replays)",
         "roofline": {"bound": "hbm", "kernel": "verify (tensor-core fused)" if tc_path else "verify (fp32 SIMT)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
@@ -480,6 +495,8 @@ def main():
     ap.add_argument("--impl", choices=["canopy", "reference"], default="canopy")
     ap.add_argument("--solve", choices=["fwdsub", "neumann"], default="fwdsub")
     ap.add_argument("--sets", type=int, default=8)
+    ap.add_argument("--graph-steps", type=int, default=200, help="steps per captured graph")
+    ap.add_argument("--kernel-reps", type=int, default=5, help="replays of the one-kernel graphs")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -4,10 +4,10 @@
 // (last line) and "What the commit kernel stores", in the (dv, dk)
 // orientation:  S_new = gamma_a S0 + sum_{j in path(a)} exp(l_a - l_j) u_j k_j^T,
 // all in fp32, from the U, l and ancestor mask the verify call left in the
-// workspace.  Memory bound: every element of S0 is read once and S_new
-// written once, with 16-byte coalesced accesses issued before anything that
-// depends on the accepted node; the path's k rows and weighted u entries are
-// staged in shared memory 32 nodes at a time.
+// workspace.  Memory bound: every element of S0 is read once (one bulk copy
+// per tile) and S_new written once with 16-byte coalesced stores; the path's
+// k rows and weighted u entries are staged in shared memory 32 nodes at a
+// time.
 #include "common.cuh"
 
 namespace canopy {
@@ -18,47 +18,48 @@ constexpr int NT = 128;    // threads per CTA
 constexpr int ROWS = 32;   // value rows per CTA
 constexpr int CH = 32;     // path nodes staged per pass
 
-// 16 bytes of a k row -> fp32 in shared memory
-__device__ inline void stage_k16(float* dst, const float* src) {
-    *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
-}
-__device__ inline void stage_k16(float* dst, const __nv_bfloat16* src) {
-    const uint4 w = *reinterpret_cast<const uint4*>(src);
-    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        dst[2 * e] = __uint_as_float(x[e] << 16);
-        dst[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
-    }
+__device__ inline float4 k4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ inline float4 k4(const __nv_bfloat16* p) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xFFFF0000u));
 }
 
-// One CTA rebuilds ROWS value rows of one (stream, head) state.  The S0 tile
-// is requested first; meanwhile warp 0 turns the accepted node's ancestor
-// bitmask into a node list (one 32-bit word per lane, offsets by a warp
-// prefix sum); then the path's k rows and exp(l_a - l_j) u_j entries are
-// staged in shared memory and accumulated into the tile, which is stored in
-// place of (or beside) S0.
+// One CTA rebuilds ROWS value rows of one (stream, head) state.  Its S0 tile
+// is fetched by one bulk copy into shared memory at the start, so the short
+// chain of dependent loads that finds the path (accepted node -> ancestor
+// bitmask -> k rows, u entries and gates of the path) does not queue behind
+// it.  Warp 0 turns the bitmask into a node list (one 32-bit word per lane,
+// offsets by a warp prefix sum); the path's k rows and exp(l_a - l_j) u_j
+// entries are staged in shared memory and accumulated into the tile, which
+// is stored in place of (or beside) S0.
 template <typename InT, int DK, int DV>
-__global__ void __launch_bounds__(NT, 8) commit_kernel(const int32_t* __restrict__ accepted, const float* S0,
-                                                       float* S_new, const InT* __restrict__ k, int T, int H,
-                                                       Ws ws) {
-    constexpr int C4 = DK / 4;             // float4 per state row
-    constexpr int F4 = ROWS * C4 / NT;     // float4 per thread
+__global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted, const float* S0,
+                                                    float* S_new, const InT* __restrict__ k, int T, int H, Ws ws) {
+    constexpr int C4 = DK / 4;             // float4 per state row (threads per row)
+    constexpr int F4 = ROWS * C4 / NT;     // float4 per thread = rows per thread
     constexpr int KV = 16 / sizeof(InT);   // k elements per 16-byte load
-    static_assert(F4 >= 1 && (ROWS * C4) % NT == 0 && NT % C4 == 0, "tile shape");
+    constexpr uint32_t TILE = ROWS * DK * 4;
+    static_assert(F4 >= 2 && F4 % 2 == 0 && (ROWS * C4) % NT == 0 && NT % C4 == 0, "tile shape");
+    __shared__ __align__(128) float sS[ROWS * DK];
+    __shared__ __align__(16) InT sK[CH][DK];
+    __shared__ __align__(16) float sWU[CH][ROWS];
     __shared__ int sPath[kMaxT];
+    __shared__ __align__(8) uint64_t sBar;
     __shared__ int sN;
     __shared__ float sLa;
-    __shared__ __align__(16) float sK[CH][DK];
-    __shared__ float sWU[CH][ROWS];
     const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
     const int v0 = rt * ROWS;
-
+    // this thread: rows r0 .. r0 + F4 - 1 of the tile, float4 column c4
+    const int c4 = t % C4, r0 = (t / C4) * F4;
     const size_t sbase = ((size_t(b) * H + h) * DV + v0) * DK;
-    float4 acc[F4];
-#pragma unroll
-    for (int u = 0; u < F4; ++u) acc[u] = *reinterpret_cast<const float4*>(S0 + sbase + size_t(u * NT + t) * 4);
 
+    if (t == 0) {
+        mbar_init(&sBar, 1);
+        fence_mbar_init();
+        mbar_expect_tx(&sBar, TILE);
+        bulk_load(sS, S0 + sbase, TILE, &sBar);
+    }
     if (t < 32) {
         int a = accepted[b];
         if (a < -1 || a >= T) {
@@ -91,42 +92,53 @@ __global__ void __launch_bounds__(NT, 8) commit_kernel(const int32_t* __restrict
     const int n = sN;
     const float la = sLa;
     const float gamma_a = (n > 0) ? expf(la) : 1.f;
-#pragma unroll
-    for (int u = 0; u < F4; ++u) {
-        acc[u].x *= gamma_a;
-        acc[u].y *= gamma_a;
-        acc[u].z *= gamma_a;
-        acc[u].w *= gamma_a;
-    }
 
-    for (int c0 = 0; c0 < n; c0 += CH) {
-        const int cn = min(CH, n - c0);
+    float4 acc[F4];
+    bool have_tile = false;
+    for (int c0 = 0; c0 == 0 || c0 < n; c0 += CH) {
+        const int cn = max(0, min(CH, n - c0));
         if (c0) __syncthreads();
         for (int e = t; e < cn * (DK / KV); e += NT) {
             const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[c0 + r];
-            stage_k16(&sK[r][c], k + ((size_t(b) * T + j) * H + h) * DK + c);
+            *reinterpret_cast<uint4*>(&sK[r][c]) =
+                *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * H + h) * DK + c);
         }
         for (int e = t; e < cn * ROWS; e += NT) {
             const int r = e / ROWS, c = e % ROWS, j = sPath[c0 + r];
             const size_t nh = (size_t(b) * T + j) * H + h;
             sWU[r][c] = expf(la - ws.l[nh]) * ws.U[nh * DV + v0 + c];
         }
-        __syncthreads();
-        for (int r = 0; r < cn; ++r) {
+        if (!have_tile) {
+            if (!mbar_wait(&sBar, 0) && t == 0) raise_err(ws.err, CANOPY_DEVERR_TIMEOUT);
 #pragma unroll
             for (int u = 0; u < F4; ++u) {
-                const int f = u * NT + t, row = f / C4, c4 = f % C4;
-                const float wu = sWU[r][row];
-                const float4 kk = *reinterpret_cast<const float4*>(&sK[r][c4 * 4]);
-                acc[u].x += wu * kk.x;
-                acc[u].y += wu * kk.y;
-                acc[u].z += wu * kk.z;
-                acc[u].w += wu * kk.w;
+                const float4 s = *reinterpret_cast<const float4*>(&sS[((r0 + u) * C4 + c4) * 4]);
+                acc[u] = make_float4(gamma_a * s.x, gamma_a * s.y, gamma_a * s.z, gamma_a * s.w);
+            }
+            have_tile = true;
+        }
+        __syncthreads();
+        for (int r = 0; r < cn; ++r) {
+            const float4 kk = k4(&sK[r][c4 * 4]);
+            float wu[F4];
+#pragma unroll
+            for (int u2 = 0; u2 < F4; u2 += 2) {
+                const float2 w2 = *reinterpret_cast<const float2*>(&sWU[r][r0 + u2]);
+                wu[u2] = w2.x;
+                wu[u2 + 1] = w2.y;
+            }
+#pragma unroll
+            for (int u = 0; u < F4; ++u) {
+                acc[u].x += wu[u] * kk.x;
+                acc[u].y += wu[u] * kk.y;
+                acc[u].z += wu[u] * kk.z;
+                acc[u].w += wu[u] * kk.w;
             }
         }
     }
 #pragma unroll
-    for (int u = 0; u < F4; ++u) *reinterpret_cast<float4*>(S_new + sbase + size_t(u * NT + t) * 4) = acc[u];
+    for (int u = 0; u < F4; ++u)
+        *reinterpret_cast<float4*>(S_new + sbase + size_t((r0 + u) * C4 + c4) * 4) = acc[u];
 }
 
 }  // namespace cm

@@ -22,7 +22,7 @@
 //       lanes, nodes on the columns); R^T = beta (V - gamma X_K)^T as bf16
 //       hi + lo into tensor memory; the X_Q columns scaled by gamma.
 // Then Y^T = [gamma X_Q^T | 0] + R^T [M; W]^T by three bf16 products
-// (hi*hi + hi*lo + lo*hi, ~16 mantissa bits each side), and each warp stores
+// (hi*hi + hi*lo + lo*hi, ~15 mantissa bits each side), and each warp stores
 // 32 value columns of o (warps 0-3) or U (warps 4-7) for every node.
 // Decay ratios are only ever 2^(l2_i - l2_j) with j on i's root path, so they
 // lie in (0, 1] and never overflow ("Hard constraints", log-space gates).
@@ -59,9 +59,15 @@ struct Smem {
     static constexpr int BAR = MASK + 512;       // u64[8]
     static constexpr int TMEMSLOT = BAR + 64;    // u32
     static constexpr int FLAG = TMEMSLOT + 4;    // int
-    static constexpr int PLIST = FLAG + 12;      // u8[64][64] path(i) from the root down
+    static constexpr int BG = BAR + 128;         // float2[64] (beta, beta gamma)
+    static constexpr int PLIST = BG + 512;       // u8[64][64] path(i) from the root down
     static constexpr int TOTAL = PLIST + TP * TP;
-    static_assert(XV % 16 == 0 && GP % 16 == 0, "align");
+    // after the output product: o and U tiles [64 nodes][128 columns] for the TMA stores
+    static constexpr int OT = 0;
+    static constexpr int UT = 32768;
+    static_assert(UT + TP * DV * 4 <= PAR, "output tiles overlap the small arrays");
+    static_assert(XV % 16 == 0 && GP % 16 == 0 && BAR % 256 == 0 && BG % 16 == 0 && GAM % 16 == 0, "align");
+    static_assert(FLAG + 4 <= BG, "small arrays overlap");
 };
 
 enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, NBAR };
@@ -80,15 +86,19 @@ struct Params {
     int B, T, H, W, o_bf16;
 };
 
-__device__ inline uint32_t pack_bf16(float lo_half, float hi_half) {
-    const __nv_bfloat162 p = __floats2bfloat162_rn(lo_half, hi_half);
-    return *reinterpret_cast<const uint32_t*>(&p);
-}
-
-// x -> bf16 hi (round to nearest) and bf16 lo = bf16(x - hi).
-__device__ inline void split_bf16(float x, float& hi, float& lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = x - hi;
+// Two-part bf16 split with integer operations only (the conversion unit is
+// a quarter-rate pipe, and these splits run for every S0, R and [M; W]
+// element): hi = x rounded half-up to 8 significant bits, lo = x - hi
+// (exact in fp32), and the lo kept as its top 16 bits (truncated), so
+// |x - (hi + lo16)| < 2^-15 |x|.
+__device__ inline uint32_t hi_bits(float x) { return (__float_as_uint(x) + 0x8000u) & 0xFFFF0000u; }
+// bf16 pair from the top halves of two fp32 words: a -> low half, b -> high half.
+__device__ inline uint32_t pack_top(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
+// Split x0, x1 into packed bf16 hi and lo pairs.
+__device__ inline void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const uint32_t h0 = hi_bits(x0), h1 = hi_bits(x1);
+    hi = pack_top(h0, h1);
+    lo = pack_top(__float_as_uint(x0 - __uint_as_float(h0)), __float_as_uint(x1 - __uint_as_float(h1)));
 }
 
 __device__ inline void wait_or_flag(uint64_t* bar, int* sFlag) {
@@ -97,7 +107,8 @@ __device__ inline void wait_or_flag(uint64_t* bar, int* sFlag) {
 
 __global__ void __launch_bounds__(NT, 2)
     verify_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, Params p) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const __grid_constant__ CUtensorMap tmU, Params p) {
     using L = Smem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -111,6 +122,7 @@ __global__ void __launch_bounds__(NT, 2)
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
     int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
     uint8_t* sPath = sm + L::PLIST;
+    float2* sBG = reinterpret_cast<float2*>(sm + L::BG);
     float* sX = reinterpret_cast<float*>(sm + L::XV);
     float* sGp = reinterpret_cast<float*>(sm + L::GP);
 
@@ -191,7 +203,9 @@ __global__ void __launch_bounds__(NT, 2)
         if (tid < TP) {
             const int i = tid;
             sL2[i] = myl2;  // every walk has read the per-node gates by now
-            sGam[i] = exp2f(myl2);
+            const float gm = exp2f(myl2);
+            sGam[i] = gm;
+            sBG[i] = make_float2(sBeta[i], sBeta[i] * gm);  // zero for padded nodes
             if (i < T) {
                 int d = 0;
                 for (uint64_t bits = sMask[i]; bits; bits &= bits - 1)
@@ -256,19 +270,55 @@ __global__ void __launch_bounds__(NT, 2)
         group_sync(1, 128);
 
         // ---- W and M rows: right-looking substitution along path(i) ----------
-        // x_d -= x_e Gp[pl[e]][d] for e = n-1 .. 1 and d < e; Gp rows are
-        // zero beyond their length, so whole float4 groups are safe.
-        for (int e = n - 1; e >= 1; --e) {
-            const float xe = xr[e];
-            const float* gr = sGp + pl[e] * XS;
-            for (int d = 0; d < e; d += 4) {
-                float4 x4 = *reinterpret_cast<const float4*>(xr + d);
-                const float4 g4 = *reinterpret_cast<const float4*>(gr + d);
-                x4.x -= xe * g4.x;
-                x4.y -= xe * g4.y;
-                x4.z -= xe * g4.z;
-                x4.w -= xe * g4.w;
-                *reinterpret_cast<float4*>(xr + d) = x4;
+        // x_d -= x_e Gp[pl[e]][d] for e = n-1 .. 1 and d < e, four pivots per
+        // pass: the group of positions 4G..4G+3 is resolved in registers
+        // (its pivots are final once every higher position has been applied),
+        // then all four are applied to the groups below in one sweep.  Gp
+        // rows are zero from their own position for four entries, so whole
+        // groups are safe; pivots past the path count as zero.
+        if (n > 1) {
+            int G = (n - 1) >> 2;
+            float4 xg = *reinterpret_cast<const float4*>(xr + 4 * G);
+            for (;;) {
+                const int base = 4 * G;
+                int a[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a[q] = pl[min(base + q, n - 1)];
+                float xv[4] = {xg.x, xg.y, xg.z, xg.w};
+#pragma unroll
+                for (int q = 3; q >= 1; --q) {
+                    const float4 gq = *reinterpret_cast<const float4*>(sGp + a[q] * XS + base);
+                    const float pv = (base + q < n) ? xv[q] : 0.f;
+                    if (q > 0) xv[0] -= pv * gq.x;
+                    if (q > 1) xv[1] -= pv * gq.y;
+                    if (q > 2) xv[2] -= pv * gq.z;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (base + q >= n) xv[q] = 0.f;
+                *reinterpret_cast<float4*>(xr + base) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+                if (G == 0) break;
+                const float* g0 = sGp + a[0] * XS;
+                const float* g1 = sGp + a[1] * XS;
+                const float* g2 = sGp + a[2] * XS;
+                const float* g3 = sGp + a[3] * XS;
+#pragma unroll 2
+                for (int g = G - 1; g >= 0; --g) {
+                    float4 x4 = *reinterpret_cast<const float4*>(xr + 4 * g);
+                    const float4 h0 = *reinterpret_cast<const float4*>(g0 + 4 * g);
+                    const float4 h1 = *reinterpret_cast<const float4*>(g1 + 4 * g);
+                    const float4 h2 = *reinterpret_cast<const float4*>(g2 + 4 * g);
+                    const float4 h3 = *reinterpret_cast<const float4*>(g3 + 4 * g);
+                    x4.x -= xv[0] * h0.x + xv[1] * h1.x + xv[2] * h2.x + xv[3] * h3.x;
+                    x4.y -= xv[0] * h0.y + xv[1] * h1.y + xv[2] * h2.y + xv[3] * h3.y;
+                    x4.z -= xv[0] * h0.z + xv[1] * h1.z + xv[2] * h2.z + xv[3] * h3.z;
+                    x4.w -= xv[0] * h0.w + xv[1] * h1.w + xv[2] * h2.w + xv[3] * h3.w;
+                    if (g == G - 1)
+                        xg = x4;  // the next pass's group stays in registers
+                    else
+                        *reinterpret_cast<float4*>(xr + 4 * g) = x4;
+                }
+                --G;
             }
         }
 
@@ -284,11 +334,11 @@ __global__ void __launch_bounds__(NT, 2)
             }
             for (int d = 0; d < n; ++d) {
                 const int j = pl[d];
-                float hi, lo;
-                split_bf16(xr[d], hi, lo);
+                const float x = xr[d];
+                const uint32_t hb = hi_bits(x);
                 const int off = ((((j >> 3) ^ (r & 7))) << 4) + ((j & 7) << 1);
-                *reinterpret_cast<__nv_bfloat16*>(bh + off) = __float2bfloat16_rn(hi);
-                *reinterpret_cast<__nv_bfloat16*>(bl + off) = __float2bfloat16_rn(lo);
+                *reinterpret_cast<uint16_t*>(bh + off) = uint16_t(hb >> 16);
+                *reinterpret_cast<uint16_t*>(bl + off) = uint16_t(__float_as_uint(x - __uint_as_float(hb)) >> 16);
             }
         }
         fence_proxy_async_smem();
@@ -337,7 +387,7 @@ __global__ void __launch_bounds__(NT, 2)
                 const float4* r0p = reinterpret_cast<const float4*>(S0 + size_t(row0) * DK) + csub;
                 const float4* r1p = reinterpret_cast<const float4*>(S0 + size_t(row0 + 8) * DK) + csub;
                 const uint32_t taddr = tmem + (uint32_t(quad * 32 + hf * 16) << 16);
-#pragma unroll 2
+#pragma unroll 1
                 for (int grp = 0; grp < 2; ++grp) {      // 32 columns = 64 dk values per group
                     float4 f0[4], f1[4];
 #pragma unroll
@@ -348,23 +398,10 @@ __global__ void __launch_bounds__(NT, 2)
                     uint32_t wh[16], wl[16];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        float h0, l0, h1, l1, h2, l2, h3, l3;
-                        split_bf16(f0[k].x, h0, l0);
-                        split_bf16(f0[k].y, h1, l1);
-                        split_bf16(f0[k].z, h2, l2);
-                        split_bf16(f0[k].w, h3, l3);
-                        wh[4 * k] = pack_bf16(h0, h1);
-                        wh[4 * k + 1] = pack_bf16(h2, h3);
-                        wl[4 * k] = pack_bf16(l0, l1);
-                        wl[4 * k + 1] = pack_bf16(l2, l3);
-                        split_bf16(f1[k].x, h0, l0);
-                        split_bf16(f1[k].y, h1, l1);
-                        split_bf16(f1[k].z, h2, l2);
-                        split_bf16(f1[k].w, h3, l3);
-                        wh[4 * k + 2] = pack_bf16(h0, h1);
-                        wh[4 * k + 3] = pack_bf16(h2, h3);
-                        wl[4 * k + 2] = pack_bf16(l0, l1);
-                        wl[4 * k + 3] = pack_bf16(l2, l3);
+                        split2(f0[k].x, f0[k].y, wh[4 * k], wl[4 * k]);
+                        split2(f0[k].z, f0[k].w, wh[4 * k + 1], wl[4 * k + 1]);
+                        split2(f1[k].x, f1[k].y, wh[4 * k + 2], wl[4 * k + 2]);
+                        split2(f1[k].z, f1[k].w, wh[4 * k + 3], wl[4 * k + 3]);
                     }
                     tmem_st_16x256b_x4(taddr + TA + grp * 32, wh);
                     tmem_st_16x256b_x4(taddr + TA + 64 + grp * 32, wl);
@@ -400,39 +437,45 @@ __global__ void __launch_bounds__(NT, 2)
         {
             const uint8_t* vt = sm + L::VT + (c >> 6) * L::V_TILE;
             const int cb = ((c & 63) >> 3), cw = (c & 7) << 1;
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                uint32_t xk[16];
-                tmem_ld16(lane_base + TD + 64 + blk * 16, xk);
+#pragma unroll 1
+            for (int hb = 0; hb < 2; ++hb) {          // 32 nodes per pass
+                uint32_t xk[32];
+                tmem_ld16(lane_base + TD + 64 + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xk));
+                tmem_ld16(lane_base + TD + 64 + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xk + 16));
                 tmem_wait_ld();
-                uint32_t wh[8], wl[8];
+                uint32_t wh[16], wl[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 16; ++e) {
                     float rv[2];
 #pragma unroll
-                    for (int s = 0; s < 2; ++s) {
-                        const int i = blk * 16 + 2 * e + s;
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const int i = hb * 32 + 2 * e + s2;
                         const float vv = __bfloat162float(
                             *reinterpret_cast<const __nv_bfloat16*>(vt + i * 128 + ((cb ^ (i & 7)) << 4) + cw));
-                        rv[s] = (i < T) ? sBeta[i] * (vv - sGam[i] * __uint_as_float(xk[2 * e + s])) : 0.f;
+                        const float2 bg = sBG[i];
+                        rv[s2] = bg.x * vv - bg.y * __uint_as_float(xk[2 * e + s2]);
                     }
-                    float h0, l0, h1, l1;
-                    split_bf16(rv[0], h0, l0);
-                    split_bf16(rv[1], h1, l1);
-                    wh[e] = pack_bf16(h0, h1);
-                    wl[e] = pack_bf16(l0, l1);
+                    split2(rv[0], rv[1], wh[e], wl[e]);
                 }
-                tmem_st8(lane_base + TA + blk * 8, wh);
-                tmem_st8(lane_base + TA + 32 + blk * 8, wl);
+                tmem_st16(lane_base + TA + hb * 16, wh);
+                tmem_st16(lane_base + TA + 32 + hb * 16, wl);
             }
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                uint32_t xq[16];
-                tmem_ld16(lane_base + TD + blk * 16, xq);
+#pragma unroll 1
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t xq[32];
+                tmem_ld16(lane_base + TD + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
+                tmem_ld16(lane_base + TD + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) xq[e] = __float_as_uint(sGam[blk * 16 + e] * __uint_as_float(xq[e]));
-                tmem_st16(lane_base + TD + blk * 16, xq);
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 gm = *reinterpret_cast<const float4*>(sGam + hb * 32 + 4 * e4);
+                    xq[4 * e4] = __float_as_uint(gm.x * __uint_as_float(xq[4 * e4]));
+                    xq[4 * e4 + 1] = __float_as_uint(gm.y * __uint_as_float(xq[4 * e4 + 1]));
+                    xq[4 * e4 + 2] = __float_as_uint(gm.z * __uint_as_float(xq[4 * e4 + 2]));
+                    xq[4 * e4 + 3] = __float_as_uint(gm.w * __uint_as_float(xq[4 * e4 + 3]));
+                }
+                tmem_st16(lane_base + TD + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
+                tmem_st16(lane_base + TD + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
             }
             tmem_wait_st();
         }
@@ -464,34 +507,38 @@ __global__ void __launch_bounds__(NT, 2)
     wait_or_flag(&bars[BAR_Y], sFlag);
     tc_fence_after();
 
-    // ---- store: warps 0-3 o, warps 4-7 U; lane = value column --------------------
+    // ---- store: warps 0-3 o, warps 4-7 U (lane = value column) into shared
+    // tiles [node][column], then one TMA store each (rows past T clipped) ---
     {
         const int c = quad * 32 + lane;
         const uint32_t col0 = TD + (solve ? 0 : 64);
-#pragma unroll
+        float* tile = reinterpret_cast<float*>(sm + (solve ? L::OT : L::UT));
+        __nv_bfloat16* tile16 = reinterpret_cast<__nv_bfloat16*>(sm + L::OT);
+        const bool o16 = solve && p.o_bf16;
+#pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
             uint32_t y[16];
             tmem_ld16(lane_base + col0 + blk * 16, y);
             tmem_wait_ld();
+            if (o16) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int i = blk * 16 + e;
-                if (i < T) {
-                    const size_t off = ((size_t(b) * T + i) * H + h) * DV + c;
-                    const float yv = __uint_as_float(y[e]);
-                    if (!solve)
-                        p.U[off] = yv;
-                    else if (p.o_bf16)
-                        static_cast<__nv_bfloat16*>(p.o)[off] = __float2bfloat16_rn(yv);
-                    else
-                        static_cast<float*>(p.o)[off] = yv;
-                }
+                for (int e = 0; e < 16; ++e) tile16[(blk * 16 + e) * DV + c] = __float2bfloat16_rn(__uint_as_float(y[e]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) tile[(blk * 16 + e) * DV + c] = __uint_as_float(y[e]);
             }
         }
+        fence_proxy_async_smem();
     }
-
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+        tma_store_4d(&tmO, sm + L::OT, 0, h, 0, b);
+        tma_store_4d(&tmU, sm + L::UT, 0, h, 0, b);
+        bulk_commit_group();
+    }
+
+    if (tid == 0) bulk_wait_read_all();
     if (tid == 128 && *sFlag) {
         // a wait gave up: let the copies in flight land before leaving
         raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
@@ -507,13 +554,15 @@ __global__ void __launch_bounds__(NT, 2)
 // Host side.
 
 bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H);
+bool make_out_map(CUtensorMap* m, void* base, int B, int T, int H, int bf16);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
                                  const Ws& ws, cudaStream_t st) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo, mu;
     if (!make_bf16_row_map(&mq, q, B, T, H) || !make_bf16_row_map(&mk, k, B, T, H) ||
-        !make_bf16_row_map(&mv, v, B, T, H))
+        !make_bf16_row_map(&mv, v, B, T, H) || !make_out_map(&mo, o, B, T, H, o_bf16) ||
+        !make_out_map(&mu, ws.U, B, T, H, 0))
         return cudaErrorInvalidValue;
     tcf::Params prm;
     prm.g = g;
@@ -538,7 +587,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tcf::verify_fwd_kernel<<<dim3(H, B), tcf::NT, smem, st>>>(mq, mk, mv, prm);
+    tcf::verify_fwd_kernel<<<dim3(H, B), tcf::NT, smem, st>>>(mq, mk, mv, mo, mu, prm);
     return cudaGetLastError();
 }
 
