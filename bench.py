@@ -44,6 +44,10 @@ WORKLOAD = dict(name="batched verify B=16 T=64 H=16 dk=dv=128 random trees depth
                 case=2, B=16, T=64, H=16, d=128)
 METRIC = "µs per GDN layer tree-verify and verified nodes/s (B=16,T=64); % HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (read + write) of one verify launch of this workload, from the
+# ncu capture summarised in profiles/verify_fwd_kernel_B16_T64_H16_d128.md;
+# set to None whenever the kernel changes until it is captured again.
+VERIFY_DRAM_TRAFFIC = 29_549_056 + 3_328
 
 
 def verify_bytes(B, T, H, d, in_bytes=2, o_bytes=4):
@@ -297,7 +301,7 @@ def run_canopy(args, world, rank, local):
                   f"{args.kernel_reps} replays each (p10/p50/p90 over replays)",
         "roofline": {"bound": "hbm", "kernel": "verify (tensor-core fused)" if tc_path else "verify (fp32 SIMT)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
+                     "traffic": VERIFY_DRAM_TRAFFIC if tc_path else None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
         "roofline_commit": {"bound": "hbm", "achieved": cb / (c_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
                             "frac": cb / (c_us * 1e-6) / 1e9 / peak, "algorithmic_bytes": cb},
         "gpu_launches": launches_per_step * K,

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     __shared__ __align__(16) InT sK[CH][DK];
     __shared__ __align__(16) float sWU[CH][ROWS];
     __shared__ int sPath[kMaxT];
+    __shared__ uint32_t sMaskB[128];   // the stream's ancestor masks when T * W <= 128
+    __shared__ float sLB[64];          // the head's log gates when T <= 64
     __shared__ __align__(8) uint64_t sBar;
     __shared__ int sN;
     __shared__ float sLa;
@@ -54,13 +56,22 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     const int c4 = t % C4, r0 = (t / C4) * F4;
     const size_t sbase = ((size_t(b) * H + h) * DV + v0) * DK;
 
+    pdl_wait();
+    pdl_trigger();
     if (t == 0) {
         mbar_init(&sBar, 1);
         fence_mbar_init();
         mbar_expect_tx(&sBar, TILE);
         bulk_load(sS, S0 + sbase, TILE, &sBar);
     }
+    // T <= 64: the stream's masks and the head's gates are read together with
+    // the accepted node, so the path costs one dependent round trip less
+    const bool spec = T <= 64;
     if (t < 32) {
+        if (spec) {
+            for (int w = t; w < T * ws.W; w += 32) sMaskB[w] = ws.mask[size_t(b) * T * ws.W + w];
+            for (int j = t; j < T; j += 32) sLB[j] = ws.l[(size_t(b) * T + j) * H + h];
+        }
         int a = accepted[b];
         if (a < -1 || a >= T) {
             if (t == 0 && h == 0 && rt == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
@@ -68,8 +79,10 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
         }
         int n = 0;
         float la = 0.f;
+        __syncwarp();
         if (a >= 0) {
-            const uint32_t word = (t < ws.W) ? ws.mask[(size_t(b) * T + a) * ws.W + t] : 0u;
+            uint32_t word = 0u;
+            if (t < ws.W) word = spec ? sMaskB[a * ws.W + t] : ws.mask[(size_t(b) * T + a) * ws.W + t];
             const int c = __popc(word);
             int off = c;
 #pragma unroll
@@ -80,7 +93,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
             n = __shfl_sync(0xffffffffu, off, 31) + 1;
             off -= c;
             for (uint32_t bits = word; bits; bits &= bits - 1) sPath[off++] = 32 * t + __ffs(bits) - 1;
-            la = ws.l[(size_t(b) * T + a) * H + h];
+            la = spec ? sLB[a] : ws.l[(size_t(b) * T + a) * H + h];
             if (t == 0) sPath[n - 1] = a;
         }
         if (t == 0) {
@@ -106,7 +119,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
         for (int e = t; e < cn * ROWS; e += NT) {
             const int r = e / ROWS, c = e % ROWS, j = sPath[c0 + r];
             const size_t nh = (size_t(b) * T + j) * H + h;
-            sWU[r][c] = expf(la - ws.l[nh]) * ws.U[nh * DV + v0 + c];
+            sWU[r][c] = expf(la - (spec ? sLB[j] : ws.l[nh])) * ws.U[nh * DV + v0 + c];
         }
         if (!have_tile) {
             if (!mbar_wait(&sBar, 0) && t == 0) raise_err(ws.err, CANOPY_DEVERR_TIMEOUT);
@@ -147,8 +160,8 @@ template <typename InT, int D>
 static cudaError_t launch_commit_typed(const int32_t* accepted, const float* S0, float* S_new, const void* k,
                                        int T, int B, int H, const Ws& ws, cudaStream_t st) {
     dim3 grid(D / cm::ROWS, H, B);
-    cm::commit_kernel<InT, D, D><<<grid, cm::NT, 0, st>>>(accepted, S0, S_new, static_cast<const InT*>(k), T, H, ws);
-    return cudaGetLastError();
+    return launch_pdl(cm::commit_kernel<InT, D, D>, grid, dim3(cm::NT), 0, st, accepted, S0, S_new,
+                      static_cast<const InT*>(k), T, H, ws);
 }
 
 cudaError_t launch_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k, int in_bf16,

@@ -122,6 +122,32 @@ __device__ inline uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch -----------------------------------------
+// A kernel launched with launch_pdl() may start while the previous kernel of
+// the stream is still running; pdl_wait() blocks until that kernel has
+// completed and its memory is visible (a no-op otherwise), and pdl_trigger()
+// lets the next such kernel begin its own launch.  Kernels here call both
+// before their first global access, so only launch latency and the previous
+// kernel's tail overlap.
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- mbarrier --------------------------------------------------------------
 
 __device__ inline void mbar_init(uint64_t* bar, uint32_t count) {

@@ -58,7 +58,8 @@ struct Smem {
     static constexpr int MASK = BETA + 256;      // u64[64] path(i), i included
     static constexpr int BAR = MASK + 512;       // u64[8]
     static constexpr int TMEMSLOT = BAR + 64;    // u32
-    static constexpr int FLAG = TMEMSLOT + 4;    // int
+    static constexpr int FLAG = TMEMSLOT + 4;    // int: a wait gave up
+
     static constexpr int BG = BAR + 128;         // float2[64] (beta, beta gamma)
     static constexpr int PLIST = BG + 512;       // u8[64][64] path(i) from the root down
     static constexpr int TOTAL = PLIST + TP * TP;
@@ -105,6 +106,35 @@ __device__ inline void wait_or_flag(uint64_t* bar, int* sFlag) {
     if (!mbar_wait(bar, 0)) *sFlag = 1;
 }
 
+// One pass of R^T = beta (V - gamma X_K)^T over 32 nodes (hb = 0: nodes
+// 0..31, hb = 1: 32..63) for value column c (this thread's TMEM lane): X_K
+// from the accumulator columns, V from the shared tile, the result as bf16
+// hi + lo into the A-operand columns.
+__device__ __forceinline__ void r_pass(int hb, const uint8_t* sm, const float2* sBG, uint32_t lane_base, int c) {
+    const uint8_t* vt = sm + Smem::VT + (c >> 6) * Smem::V_TILE;
+    const int cb = ((c & 63) >> 3), cw = (c & 7) << 1;
+    uint32_t xk[32];
+    tmem_ld16(lane_base + TD + 64 + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xk));
+    tmem_ld16(lane_base + TD + 64 + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xk + 16));
+    tmem_wait_ld();
+    uint32_t wh[16], wl[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        float rv[2];
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+            const int i = hb * 32 + 2 * e + s2;
+            const float vv = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16*>(vt + i * 128 + ((cb ^ (i & 7)) << 4) + cw));
+            const float2 bg = sBG[i];
+            rv[s2] = bg.x * vv - bg.y * __uint_as_float(xk[2 * e + s2]);
+        }
+        split2(rv[0], rv[1], wh[e], wl[e]);
+    }
+    tmem_st16(lane_base + TA + hb * 16, wh);
+    tmem_st16(lane_base + TA + 32 + hb * 16, wl);
+}
+
 __global__ void __launch_bounds__(NT, 2)
     verify_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -121,6 +151,7 @@ __global__ void __launch_bounds__(NT, 2)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
     int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
+
     uint8_t* sPath = sm + L::PLIST;
     float2* sBG = reinterpret_cast<float2*>(sm + L::BG);
     float* sX = reinterpret_cast<float*>(sm + L::XV);
@@ -133,6 +164,8 @@ __global__ void __launch_bounds__(NT, 2)
     const int T = p.T, H = p.H;
     const float* S0 = p.S0 + (size_t(b) * H + h) * DV * DK;
 
+    pdl_wait();
+    pdl_trigger();
     uint8_t* sQK = sm + L::QK;
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
@@ -352,6 +385,7 @@ __global__ void __launch_bounds__(NT, 2)
                     p.mask[(size_t(b) * T + tid) * p.W + w] = uint32_t(strict >> (32 * w));
             }
         }
+
     } else {
         // ---- state warps: S0 rows -> bf16 hi/lo A operand in tensor memory ----
         // AC = [Q;K] K^T (M = 128, N = 64) as soon as Q and K have landed;
@@ -435,31 +469,7 @@ __global__ void __launch_bounds__(NT, 2)
         wait_or_flag(&bars[BAR_PREP], sFlag);
         tc_fence_after();
         {
-            const uint8_t* vt = sm + L::VT + (c >> 6) * L::V_TILE;
-            const int cb = ((c & 63) >> 3), cw = (c & 7) << 1;
-#pragma unroll 1
-            for (int hb = 0; hb < 2; ++hb) {          // 32 nodes per pass
-                uint32_t xk[32];
-                tmem_ld16(lane_base + TD + 64 + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xk));
-                tmem_ld16(lane_base + TD + 64 + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xk + 16));
-                tmem_wait_ld();
-                uint32_t wh[16], wl[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float rv[2];
-#pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int i = hb * 32 + 2 * e + s2;
-                        const float vv = __bfloat162float(
-                            *reinterpret_cast<const __nv_bfloat16*>(vt + i * 128 + ((cb ^ (i & 7)) << 4) + cw));
-                        const float2 bg = sBG[i];
-                        rv[s2] = bg.x * vv - bg.y * __uint_as_float(xk[2 * e + s2]);
-                    }
-                    split2(rv[0], rv[1], wh[e], wl[e]);
-                }
-                tmem_st16(lane_base + TA + hb * 16, wh);
-                tmem_st16(lane_base + TA + 32 + hb * 16, wl);
-            }
+            r_pass(0, sm, sBG, lane_base, c);
 #pragma unroll 1
             for (int hb = 0; hb < 2; ++hb) {
                 uint32_t xq[32];
@@ -477,6 +487,7 @@ __global__ void __launch_bounds__(NT, 2)
                 tmem_st16(lane_base + TD + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
                 tmem_st16(lane_base + TD + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
             }
+            r_pass(1, sm, sBG, lane_base, c);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -587,8 +598,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tcf::verify_fwd_kernel<<<dim3(H, B), tcf::NT, smem, st>>>(mq, mk, mv, mo, mu, prm);
-    return cudaGetLastError();
+    return launch_pdl(tcf::verify_fwd_kernel, dim3(H, B), dim3(tcf::NT), smem, st, mq, mk, mv, mo, mu, prm);
 }
 
 }  // namespace canopy
