@@ -727,6 +727,20 @@ bool make_out_map(CUtensorMap* m, void* base, int B, int T, int H, int bf16) {
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// S0 [B][H][128][128] fp32 -> boxes of 32 columns x 128 rows with the
+// 128-byte swizzle (one (stream, head) state is four boxes).
+bool make_state_map(CUtensorMap* m, const float* base, int B, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {128, 128, cuuint64_t(H), cuuint64_t(B)};
+    const cuuint64_t strides[3] = {128 * 4, 128 * 128 * 4, cuuint64_t(H) * 128 * 128 * 4};
+    const cuuint32_t box[4] = {32, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool NEU>
 static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
     CUtensorMap mq, mk, mv;

@@ -32,7 +32,6 @@ namespace canopy {
 
 namespace tcf {
 
-constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr int TP = 64;    // nodes per block
 constexpr int NT = 256;   // threads per CTA
@@ -56,8 +55,8 @@ struct Smem {
     static constexpr int GAM = L2 + 256;         // float[64] gamma
     static constexpr int BETA = GAM + 256;       // float[64]
     static constexpr int MASK = BETA + 256;      // u64[64] path(i), i included
-    static constexpr int BAR = MASK + 512;       // u64[8]
-    static constexpr int TMEMSLOT = BAR + 64;    // u32
+    static constexpr int BAR = MASK + 512;       // u64[12]
+    static constexpr int TMEMSLOT = BAR + 96;    // u32
     static constexpr int FLAG = TMEMSLOT + 4;    // int: a wait gave up
 
     static constexpr int BG = BAR + 128;         // float2[64] (beta, beta gamma)
@@ -66,17 +65,22 @@ struct Smem {
     // after the output product: o and U tiles [64 nodes][128 columns] for the TMA stores
     static constexpr int OT = 0;
     static constexpr int UT = 32768;
+    // at the start: the S0 tile (fp32, 4 boxes of [128 rows][32 columns],
+    // 128-byte swizzle) over V, the work vectors and Gp, all unused until it
+    // has been converted into tensor memory
+    static constexpr int S0S = 32768;
+    static constexpr int S0_BOX = 128 * 128;
+    static_assert(S0S + 4 * S0_BOX <= PAR && S0S % 1024 == 0, "S0 staging");
     static_assert(UT + TP * DV * 4 <= PAR, "output tiles overlap the small arrays");
     static_assert(XV % 16 == 0 && GP % 16 == 0 && BAR % 256 == 0 && BG % 16 == 0 && GAM % 16 == 0, "align");
     static_assert(FLAG + 4 <= BG, "small arrays overlap");
 };
 
-enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, NBAR };
+enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, BAR_S0, BAR_SFREE, NBAR };
 
 struct Params {
     const float* g;
     const float* beta;
-    const float* S0;
     const int32_t* parent;
     void* o;
     float* U;
@@ -138,7 +142,8 @@ __device__ __forceinline__ void r_pass(int hb, const uint8_t* sm, const float2* 
 __global__ void __launch_bounds__(NT, 2)
     verify_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                      const __grid_constant__ CUtensorMap tmU, Params p) {
+                      const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmS,
+                      Params p) {
     using L = Smem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -162,50 +167,57 @@ __global__ void __launch_bounds__(NT, 2)
     const bool solve = warp < 4;
     const int h = blockIdx.x, b = blockIdx.y;
     const int T = p.T, H = p.H;
-    const float* S0 = p.S0 + (size_t(b) * H + h) * DV * DK;
 
     pdl_wait();
     pdl_trigger();
+    // Parents and gates first (threads 0..63), so that these small loads
+    // enter the memory system ahead of the tile copies below.
+    int par = -1;
+    float ga = 1.f, gb = 0.f;
+    if (tid < TP && tid < T) {
+        par = p.parent[size_t(b) * T + tid];
+        ga = p.g[(size_t(b) * T + tid) * H + h];
+        gb = p.beta[(size_t(b) * T + tid) * H + h];
+    }
     uint8_t* sQK = sm + L::QK;
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *sFlag = 0;
-        // Q and K first: the solve path waits on them
+        // Q and K next: the solve path waits on them
         mbar_expect_tx(&bars[BAR_QK], 4 * 64 * 64 * 2);
         tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, h, 0, b);
         tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, h, 0, b);
         tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, h, 0, b);
         tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, h, 0, b);
+        // then the S0 tile, by the copy engine, into the staging area
+        mbar_expect_tx(&bars[BAR_S0], 4 * L::S0_BOX);
+        for (int i = 0; i < 4; ++i) tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0], 32 * i, 0, h, b);
     }
     if (warp == 0) {
         tmem_alloc(sTmem, kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
-    // Parents and gates (threads 0..63); padded nodes: no path, beta 0, gamma 1.
+    // Validate; padded nodes: no path, beta 0, gamma 1.
     if (tid < TP) {
         const int i = tid;
-        int par = -1, bad = 0;
-        float a = 1.f, be = 0.f;
+        int bad = 0;
         if (i < T) {
-            par = p.parent[size_t(b) * T + i];
-            a = p.g[(size_t(b) * T + i) * H + h];
-            be = p.beta[(size_t(b) * T + i) * H + h];
             if (!((i == 0) ? (par == -1) : (par >= 0 && par < i))) {
                 bad |= CANOPY_DEVERR_TREE;
                 par = (i == 0) ? -1 : 0;
             }
-            if (!gate_ok(a, be)) {
+            if (!gate_ok(ga, gb)) {
                 bad |= CANOPY_DEVERR_GATE;
-                a = 1.f;
-                be = 0.f;
+                ga = 1.f;
+                gb = 0.f;
             }
         }
         if (bad) raise_err(p.err, bad);
         sPar[i] = par;
-        sL2[i] = log2f(a);
-        sBeta[i] = be;
+        sL2[i] = log2f(ga);
+        sBeta[i] = gb;
     }
     __syncthreads();
     tc_fence_after();
@@ -254,6 +266,7 @@ __global__ void __launch_bounds__(NT, 2)
         const int i = r & (TP - 1);
         float* xr = sX + r * XS;               // this row's work vector
         wait_or_flag(&bars[BAR_AC], sFlag);
+        wait_or_flag(&bars[BAR_SFREE], sFlag);  // the S0 staging area is ours now
         tc_fence_after();
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
@@ -405,46 +418,36 @@ __global__ void __launch_bounds__(NT, 2)
                 *sFlag = 1;
             }
             mma_commit(&bars[BAR_AC]);
-            mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
-            tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
-            tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
         }
         __syncwarp();
-        // S0 row (32 quad + 16 half + lane/4 [+ 8]) -> tensor-memory lane of the
-        // same index; each group of four threads reads 64 contiguous bytes of
-        // a row (16 dk values = 8 columns of bf16 pairs).
+        // S0 row c (landed in shared memory by the copy engine) -> bf16 hi/lo
+        // pairs in tensor-memory lane c; the 128-byte swizzle makes these
+        // row-per-thread reads conflict-free.
+        wait_or_flag(&bars[BAR_S0], sFlag);
         {
-            const int rsub = lane >> 2, csub = lane & 3;
 #pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                const int row0 = quad * 32 + hf * 16 + rsub;
-                const float4* r0p = reinterpret_cast<const float4*>(S0 + size_t(row0) * DK) + csub;
-                const float4* r1p = reinterpret_cast<const float4*>(S0 + size_t(row0 + 8) * DK) + csub;
-                const uint32_t taddr = tmem + (uint32_t(quad * 32 + hf * 16) << 16);
-#pragma unroll 1
-                for (int grp = 0; grp < 2; ++grp) {      // 32 columns = 64 dk values per group
-                    float4 f0[4], f1[4];
+            for (int i = 0; i < 4; ++i) {
+                const uint8_t* rowp = sm + L::S0S + i * L::S0_BOX + c * 128;
+                uint32_t wh[16], wl[16];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        f0[k] = r0p[(grp * 4 + k) * 4];
-                        f1[k] = r1p[(grp * 4 + k) * 4];
-                    }
-                    uint32_t wh[16], wl[16];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        split2(f0[k].x, f0[k].y, wh[4 * k], wl[4 * k]);
-                        split2(f0[k].z, f0[k].w, wh[4 * k + 1], wl[4 * k + 1]);
-                        split2(f1[k].x, f1[k].y, wh[4 * k + 2], wl[4 * k + 2]);
-                        split2(f1[k].z, f1[k].w, wh[4 * k + 3], wl[4 * k + 3]);
-                    }
-                    tmem_st_16x256b_x4(taddr + TA + grp * 32, wh);
-                    tmem_st_16x256b_x4(taddr + TA + 64 + grp * 32, wl);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 f = *reinterpret_cast<const float4*>(rowp + ((j ^ (c & 7)) << 4));
+                    split2(f.x, f.y, wh[2 * j], wl[2 * j]);
+                    split2(f.z, f.w, wh[2 * j + 1], wl[2 * j + 1]);
                 }
+                tmem_st16(lane_base + TA + i * 16, wh);
+                tmem_st16(lane_base + TA + 64 + i * 16, wl);
             }
         }
         tmem_wait_st();
         tc_fence_before();
         group_sync(2, 128);
+        if (tid == 128) {
+            mbar_arrive(&bars[BAR_SFREE]);  // the staging area is free: V, then the solve tables
+            mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
+            tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
+            tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
+        }
         if (tid == 128) {
             // X^T = S0 [Q;K]^T (M = 128 value rows, N = 128 nodes) once the
             // AC columns have been read out
@@ -554,6 +557,7 @@ __global__ void __launch_bounds__(NT, 2)
         // a wait gave up: let the copies in flight land before leaving
         raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
         mbar_wait(&bars[BAR_QK], 0);
+        mbar_wait(&bars[BAR_S0], 0);
         mbar_wait(&bars[BAR_V], 0);
     }
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -566,19 +570,19 @@ __global__ void __launch_bounds__(NT, 2)
 
 bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H);
 bool make_out_map(CUtensorMap* m, void* base, int B, int T, int H, int bf16);
+bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
                                  const Ws& ws, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mo, mu;
+    CUtensorMap mq, mk, mv, mo, mu, ms;
     if (!make_bf16_row_map(&mq, q, B, T, H) || !make_bf16_row_map(&mk, k, B, T, H) ||
         !make_bf16_row_map(&mv, v, B, T, H) || !make_out_map(&mo, o, B, T, H, o_bf16) ||
-        !make_out_map(&mu, ws.U, B, T, H, 0))
+        !make_out_map(&mu, ws.U, B, T, H, 0) || !make_state_map(&ms, S0, B, H))
         return cudaErrorInvalidValue;
     tcf::Params prm;
     prm.g = g;
     prm.beta = beta;
-    prm.S0 = S0;
     prm.parent = parent;
     prm.o = o;
     prm.U = ws.U;
@@ -598,7 +602,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_pdl(tcf::verify_fwd_kernel, dim3(H, B), dim3(tcf::NT), smem, st, mq, mk, mv, mo, mu, prm);
+    return launch_pdl(tcf::verify_fwd_kernel, dim3(H, B), dim3(tcf::NT), smem, st, mq, mk, mv, mo, mu, ms, prm);
 }
 
 }  // namespace canopy
