@@ -20,6 +20,9 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     __shared__ uint64_t sM[kMaxT * 4];
     __shared__ int sSize[kMaxT];
     __shared__ int sPos[kMaxT];
+    __shared__ double sLg[kMaxT * 16];  // log gates, then cumulative, for 16 heads (fp64: l_i - l_j
+                                        // must stay accurate over deep paths)
+    __shared__ int sJp[kMaxT];         // jump pointers
     const int b = blockIdx.x, i = threadIdx.x;
     int bad = 0;
     if (i < T) {
@@ -47,25 +50,49 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
         }
     }
 
-    // cumulative log gates, summed root first along each path, every head
+    // cumulative log gates l_n = log g_n + l_parent(n) for every head, by
+    // pointer jumping over 16 heads at a time (ceil(log2 T) rounds)
     int badg = 0;
-    for (int e = i; e < T * H; e += blockDim.x) {
-        const int n = e / H, hh = e % H;
-        float s = 0.f;
-        for (int w = 0; w < 4; ++w) {
-            uint64_t bits = sM[n * 4 + w];
-            while (bits) {
-                const int j = 64 * w + __ffsll(static_cast<long long>(bits)) - 1;
-                bits &= bits - 1;
-                float a = g[(size_t(b) * T + j) * H + hh];
-                if (!(a > 0.f) || !isfinite(a)) {
-                    badg = CANOPY_DEVERR_GATE;
-                    a = 1.f;
-                }
-                s += logf(a);
+    for (int h0 = 0; h0 < H; h0 += 16) {
+        const int hn = min(16, H - h0);
+        __syncthreads();
+        for (int e = i; e < T * hn; e += blockDim.x) {
+            const int n = e / hn, hh = e % hn;
+            float a = g[(size_t(b) * T + n) * H + h0 + hh];
+            if (!(a > 0.f) || !isfinite(a)) {
+                badg = CANOPY_DEVERR_GATE;
+                a = 1.f;
             }
+            sLg[n * 16 + hh] = log(double(a));
         }
-        ws.l[(size_t(b) * T + n) * H + hh] = s;
+        if (i < T) sJp[i] = sPar[i];
+        __syncthreads();
+        for (int span = 1; span < T; span *= 2) {
+            double nv[16];
+            int np = -1;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int e = i + u * 256;
+                nv[u] = 0.0;
+                if (e < T * hn) {
+                    const int n = e / hn, hh = e % hn, pn = sJp[n];
+                    nv[u] = sLg[n * 16 + hh] + ((pn >= 0) ? sLg[pn * 16 + hh] : 0.0);
+                }
+            }
+            if (i < T) np = (sJp[i] >= 0) ? sJp[sJp[i]] : -1;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int e = i + u * 256;
+                if (e < T * hn) sLg[(e / hn) * 16 + e % hn] = nv[u];
+            }
+            if (i < T) sJp[i] = np;
+            __syncthreads();
+        }
+        for (int e = i; e < T * hn; e += blockDim.x) {
+            const int n = e / hn, hh = e % hn;
+            ws.l[(size_t(b) * T + n) * H + h0 + hh] = float(sLg[n * 16 + hh]);
+        }
     }
     if (badg) raise_err(ws.err, badg);
 

@@ -8,7 +8,7 @@
 //          gamma_i X_K,i) into scratch; and for every j on path(i):
 //          G_ij = beta_i exp(l_i - l_j) k_i.k_j (j != i), C_ij = exp(l_i - l_j)
 //          q_i.k_j into scratch [B][H][T][T] (other entries are never read);
-//   solve: per (b, h), one thread per value column, nodes in index order:
+//   solve: per (b, h), level by level (nodes of equal depth together):
 //          u_i = R_i - sum_{j in A(i)} G_ij u_j (forward substitution over the
 //          ancestor bitmask), o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
 // All arithmetic is fp32.
@@ -20,16 +20,32 @@ namespace simt {
 
 constexpr int ROWS = 16;
 
+// Eight consecutive elements (16 or 32 bytes, aligned) as fp32.
+__device__ inline void load8(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(v[e] << 16);
+        x[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+    }
+}
+__device__ inline void load8(const float* p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p), c = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+}
+
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, const InT* __restrict__ k,
                                                    const InT* __restrict__ v, const float* __restrict__ beta,
                                                    const float* __restrict__ S0, int T, int H, Ws ws) {
     constexpr int GROUPS = 256 / DV;          // row groups for the S0 products
     constexpr int RPG = ROWS / GROUPS;        // rows per group
-    constexpr int EL = DK / 32;               // dk elements per lane
     __shared__ float sq[ROWS][DK];
     __shared__ float sk[ROWS][DK];
     __shared__ float sS0[DV][33];
+    __shared__ int sPathList[8][kMaxT];
     const int i0 = blockIdx.x * ROWS, h = blockIdx.y, b = blockIdx.z;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const size_t rowstride = size_t(H) * DK;
@@ -81,76 +97,233 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
         }
     }
 
-    // G and C along each root path: one warp per row, lanes split dk.
+    // G and C along each root path: one warp per row; the row's path is
+    // turned into a list, and each lane takes whole entries (a full dk-long
+    // dot product per lane, so the entries of a deep path run in parallel).
+    __syncthreads();
+    int* plist = sPathList[warp];
     for (int r = warp; r < ROWS; r += 8) {
         const int i = i0 + r;
         if (i >= T) break;
         const size_t ni = (size_t(b) * T + i) * H + h;
         const float li = ws.l[ni], bi = beta[ni];
-        float ki[EL], qi[EL];
-#pragma unroll
-        for (int e = 0; e < EL; ++e) {
-            ki[e] = sk[r][lane * EL + e];
-            qi[e] = sq[r][lane * EL + e];
-        }
         const uint32_t* mrow = ws.mask + (size_t(b) * T + i) * ws.W;
+        uint32_t word = (lane < ws.W) ? mrow[lane] : 0u;
+        if (lane == (i >> 5)) word |= 1u << (i & 31);  // path(i) = A(i) + {i}
+        const int cntw = __popc(word);
+        int off = cntw;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, off, sh);
+            if (lane >= sh) off += y;
+        }
+        const int n = __shfl_sync(0xffffffffu, off, 31);
+        off -= cntw;
+        for (uint32_t bits = word; bits; bits &= bits - 1) plist[off++] = 32 * lane + __ffs(bits) - 1;
+        __syncwarp();
         float* Grow = ws.gs + ((size_t(b) * H + h) * T + i) * T;
         float* Crow = ws.cs + ((size_t(b) * H + h) * T + i) * T;
-        for (int w = 0; w <= (i >> 5); ++w) {
-            uint32_t bits = (w < ws.W) ? mrow[w] : 0u;
-            if (w == (i >> 5)) bits |= 1u << (i & 31);  // path(i) = A(i) + {i}
-            while (bits) {
-                const int j = 32 * w + __ffs(bits) - 1;
-                bits &= bits - 1;
-                const InT* kj = k + (size_t(b) * T + j) * rowstride + size_t(h) * DK + lane * EL;
-                float kk = 0.f, qk = 0.f;
+        for (int p = lane; p < n; p += 32) {
+            const int j = plist[p];
+            const InT* kj = k + (size_t(b) * T + j) * rowstride + size_t(h) * DK;
+            float kk0 = 0.f, kk1 = 0.f, qk0 = 0.f, qk1 = 0.f;
+#pragma unroll 2
+            for (int d = 0; d < DK; d += 8) {
+                float x[8];
+                load8(kj + d, x);
 #pragma unroll
-                for (int e = 0; e < EL; ++e) {
-                    const float x = to_f(kj[e]);
-                    kk += ki[e] * x;
-                    qk += qi[e] * x;
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    kk += __shfl_xor_sync(0xffffffffu, kk, off);
-                    qk += __shfl_xor_sync(0xffffffffu, qk, off);
-                }
-                if (lane == 0) {
-                    const float gam = expf(li - ws.l[(size_t(b) * T + j) * H + h]);
-                    Grow[j] = (j == i) ? 0.f : bi * gam * kk;
-                    Crow[j] = gam * qk;
+                for (int e = 0; e < 8; e += 2) {
+                    kk0 += sk[r][d + e] * x[e];
+                    kk1 += sk[r][d + e + 1] * x[e + 1];
+                    qk0 += sq[r][d + e] * x[e];
+                    qk1 += sq[r][d + e + 1] * x[e + 1];
                 }
             }
+            const float gam = expf(li - ws.l[(size_t(b) * T + j) * H + h]);
+            Grow[j] = (j == i) ? 0.f : bi * gam * (kk0 + kk1);
+            Crow[j] = gam * (qk0 + qk1);
         }
+        __syncwarp();
     }
 }
 
+constexpr int SOLVE_NT = 512;  // threads of the solve kernel
+constexpr int CHN = 16;        // nodes of one level staged at a time
+constexpr int PSTRIDE = 256;   // staged path entries per node (kMaxT)
+
+// Shared-memory bytes of solve_level_kernel for T nodes and DV value columns.
+__host__ __device__ constexpr size_t solve_smem(int T, int DV) {
+    return size_t(T) * DV * 4 + size_t(3 * kMaxT + 1) * 4 + size_t(CHN) * 8 + size_t(CHN) * PSTRIDE * 12;
+}
+
+// Forward substitution level by level: all nodes of one depth depend only on
+// shallower nodes, so they are solved together.  Per node i (in a level):
+//   u_i = R_i - sum_{j in A(i)} G_ij u_j,
+//   o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
+// One CTA per (stream, head): SOLVE_NT / DV groups of DV threads (one per
+// value column); U of every solved node stays in shared memory.  Per chunk
+// of a level, one warp per node turns its ancestor bitmask into a list and
+// stages (j, G_ij, C_ij); then each group takes nodes of the chunk.
 template <typename OutT, int DV>
-__global__ void __launch_bounds__(128) solve_kernel(OutT* __restrict__ o, int T, int H, Ws ws) {
-    extern __shared__ float sU[];  // [T][DV]
-    const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-    if (c >= DV) return;
-    for (int i = 0; i < T; ++i) {
-        const size_t n = (size_t(b) * T + i) * H + h;
-        float acc = ws.rr[n * DV + c];
-        float out = ws.xq[n * DV + c];
-        const uint32_t* mrow = ws.mask + (size_t(b) * T + i) * ws.W;
-        const float* Grow = ws.gs + ((size_t(b) * H + h) * T + i) * T;
-        const float* Crow = ws.cs + ((size_t(b) * H + h) * T + i) * T;
-        for (int w = 0; w < ws.W; ++w) {
-            uint32_t bits = mrow[w];
-            while (bits) {
-                const int j = 32 * w + __ffs(bits) - 1;
-                bits &= bits - 1;
-                const float uj = sU[j * DV + c];
-                acc -= Grow[j] * uj;
-                out += Crow[j] * uj;
-            }
+__global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict__ o, int T, int H, Ws ws) {
+    constexpr int NG = SOLVE_NT / DV;
+    extern __shared__ float smem[];
+    float* sU = smem;                                       // [T][DV]
+    int* sOrder = reinterpret_cast<int*>(sU + size_t(T) * DV);  // [kMaxT] nodes by depth
+    int* sOff = sOrder + kMaxT;                             // [kMaxT + 1] level offsets
+    int* sCnt = sOff + kMaxT + 1;                           // [kMaxT] nodes per level, then fill counters
+    int* sNode = sCnt + kMaxT;                              // [CHN]
+    int* sLen = sNode + CHN;                                // [CHN] ancestors staged per node
+    int* sJ = sLen + CHN;                                   // [CHN][PSTRIDE]
+    float* sG = reinterpret_cast<float*>(sJ + CHN * PSTRIDE);   // [CHN][PSTRIDE]
+    float* sC = sG + CHN * PSTRIDE;                         // [CHN][PSTRIDE]; entry PSTRIDE-1 unused
+    __shared__ float sCii[CHN];
+    __shared__ int sMaxD;
+    __shared__ float2 sPart[SOLVE_NT];  // per-thread partial sums when groups share a node
+    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+    const int lane = t & 31, warp = t >> 5;
+    const size_t bh = size_t(b) * H + h;
+
+    for (int d = t; d < kMaxT; d += SOLVE_NT) sCnt[d] = 0;
+    if (t == 0) sMaxD = 0;
+    __syncthreads();
+    int myd = 0;
+    if (t < T) {
+        myd = ws.depth[size_t(b) * T + t];
+        myd = min(max(myd, 0), kMaxT - 1);
+        atomicAdd(&sCnt[myd], 1);
+        atomicMax(&sMaxD, myd);
+    }
+    __syncthreads();
+    const int maxd = sMaxD;
+    if (t == 0) {
+        int acc = 0;
+        for (int d = 0; d <= maxd; ++d) {
+            sOff[d] = acc;
+            acc += sCnt[d];
+            sCnt[d] = 0;
         }
-        sU[i * DV + c] = acc;
-        ws.U[n * DV + c] = acc;
-        out += Crow[i] * acc;
-        store_out(o + n * DV + c, out);
+        sOff[maxd + 1] = acc;
+    }
+    __syncthreads();
+    if (t < T) sOrder[sOff[myd] + atomicAdd(&sCnt[myd], 1)] = t;
+    __syncthreads();
+
+    const int c = t % DV, grp = t / DV;
+    const float* gsb = ws.gs + bh * T * T;
+    const float* csb = ws.cs + bh * T * T;
+    for (int lv = 0; lv <= maxd; ++lv) {
+        for (int c0 = sOff[lv]; c0 < sOff[lv + 1]; c0 += CHN) {
+            const int cn = min(CHN, sOff[lv + 1] - c0);
+            // stage the chunk's ancestor lists and coefficients (one warp per node)
+            if (warp < cn) {
+                const int e = warp, i = sOrder[c0 + e];
+                const uint32_t word = (lane < ws.W) ? ws.mask[(size_t(b) * T + i) * ws.W + lane] : 0u;
+                const int cntw = __popc(word);
+                int off = cntw;
+#pragma unroll
+                for (int sh = 1; sh < 32; sh <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, off, sh);
+                    if (lane >= sh) off += y;
+                }
+                const int n = __shfl_sync(0xffffffffu, off, 31);
+                off -= cntw;
+                int* jrow = sJ + e * PSTRIDE;
+                for (uint32_t bits = word; bits; bits &= bits - 1) jrow[off++] = 32 * lane + __ffs(bits) - 1;
+                __syncwarp();
+                const float* grow = gsb + size_t(i) * T;
+                const float* crow = csb + size_t(i) * T;
+                // all of a lane's loads in flight at once (paths up to 256 long)
+                for (int p0 = lane; p0 < n; p0 += 32 * 8) {
+                    int jj[8];
+                    float gv[8], cv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) jj[u] = (p0 + 32 * u < n) ? jrow[p0 + 32 * u] : i;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        gv[u] = grow[jj[u]];
+                        cv[u] = crow[jj[u]];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (p0 + 32 * u < n) {
+                            sG[e * PSTRIDE + p0 + 32 * u] = gv[u];
+                            sC[e * PSTRIDE + p0 + 32 * u] = cv[u];
+                        }
+                }
+                if (lane == 0) {
+                    sNode[e] = i;
+                    sLen[e] = n;
+                    sCii[e] = crow[i];
+                }
+            }
+            __syncthreads();
+            // groups per node: several groups share a node when the chunk has
+            // fewer nodes than groups (deep trees: few nodes per level, long
+            // paths); their partial sums meet in shared memory
+            int gpn = 1;
+            while (gpn * 2 * cn <= NG) gpn *= 2;
+            if (gpn > 1) {
+                const int e = grp / gpn, sub = grp % gpn;
+                float acc = 0.f, out = 0.f;
+                if (e < cn) {
+                    const int n = sLen[e];
+                    const int* jrow = sJ + e * PSTRIDE;
+                    const float* gr = sG + e * PSTRIDE;
+                    const float* cr = sC + e * PSTRIDE;
+                    for (int p = sub; p < n; p += gpn) {
+                        const float u0 = sU[jrow[p] * DV + c];
+                        acc -= gr[p] * u0;
+                        out += cr[p] * u0;
+                    }
+                }
+                sPart[t] = make_float2(acc, out);
+                __syncthreads();
+                if (e < cn && sub == 0) {
+                    for (int q = 1; q < gpn; ++q) {
+                        const float2 pq = sPart[t + q * DV];
+                        acc += pq.x;
+                        out += pq.y;
+                    }
+                    const int i = sNode[e];
+                    const size_t ni = (size_t(b) * T + i) * H + h;
+                    acc += ws.rr[ni * DV + c];
+                    out += ws.xq[ni * DV + c] + sCii[e] * acc;
+                    sU[i * DV + c] = acc;
+                    ws.U[ni * DV + c] = acc;
+                    store_out(o + ni * DV + c, out);
+                }
+            } else {
+                for (int e = grp; e < cn; e += NG) {
+                    const int i = sNode[e], n = sLen[e];
+                    const size_t ni = (size_t(b) * T + i) * H + h;
+                    const int* jrow = sJ + e * PSTRIDE;
+                    const float* gr = sG + e * PSTRIDE;
+                    const float* cr = sC + e * PSTRIDE;
+                    float acc = ws.rr[ni * DV + c], out = ws.xq[ni * DV + c];
+                    float acc2 = 0.f, out2 = 0.f;
+                    int p = 0;
+                    for (; p + 1 < n; p += 2) {
+                        const float u0 = sU[jrow[p] * DV + c], u1 = sU[jrow[p + 1] * DV + c];
+                        acc -= gr[p] * u0;
+                        out += cr[p] * u0;
+                        acc2 -= gr[p + 1] * u1;
+                        out2 += cr[p + 1] * u1;
+                    }
+                    if (p < n) {
+                        const float u0 = sU[jrow[p] * DV + c];
+                        acc -= gr[p] * u0;
+                        out += cr[p] * u0;
+                    }
+                    acc += acc2;
+                    out += out2 + sCii[e] * acc;
+                    sU[i * DV + c] = acc;
+                    ws.U[ni * DV + c] = acc;
+                    store_out(o + ni * DV + c, out);
+                }
+            }
+            __syncthreads();
+        }
     }
 }
 
@@ -165,26 +338,28 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
                                                       static_cast<const InT*>(v), beta, S0, T, H, ws);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int smem = T * DV * 4;
+    const size_t smem = simt::solve_smem(T, DV);
+    const size_t smem_max = simt::solve_smem(kMaxT, DV);
     dim3 g2(H, B);
     if (o_bf16) {
         static bool attr = false;
         if (!attr) {
-            e = cudaFuncSetAttribute(simt::solve_kernel<__nv_bfloat16, DV>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxT * DV * 4);
+            e = cudaFuncSetAttribute(simt::solve_level_kernel<__nv_bfloat16, DV>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max));
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        simt::solve_kernel<__nv_bfloat16, DV><<<g2, DV, smem, st>>>(static_cast<__nv_bfloat16*>(o), T, H, ws);
+        simt::solve_level_kernel<__nv_bfloat16, DV><<<g2, simt::SOLVE_NT, smem, st>>>(
+            static_cast<__nv_bfloat16*>(o), T, H, ws);
     } else {
         static bool attr = false;
         if (!attr) {
-            e = cudaFuncSetAttribute(simt::solve_kernel<float, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kMaxT * DV * 4);
+            e = cudaFuncSetAttribute(simt::solve_level_kernel<float, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(smem_max));
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        simt::solve_kernel<float, DV><<<g2, DV, smem, st>>>(static_cast<float*>(o), T, H, ws);
+        simt::solve_level_kernel<float, DV><<<g2, simt::SOLVE_NT, smem, st>>>(static_cast<float*>(o), T, H, ws);
     }
     return cudaGetLastError();
 }
