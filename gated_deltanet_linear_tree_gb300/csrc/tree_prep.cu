@@ -4,7 +4,7 @@
 // canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed form"
 // (A(i), path(i), depth, l_i = log alpha_i + l_parent(i)) and "Design
 // decisions" (DFS pre-order keeps subtrees contiguous; a T x T bitmask).
-// One CTA of 256 threads per stream; T <= 256.
+// One CTA of 256 threads per (stream, group of 16 heads); T <= 256.
 #include "common.cuh"
 
 namespace canopy {
@@ -20,10 +20,12 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     __shared__ uint64_t sM[kMaxT * 4];
     __shared__ int sSize[kMaxT];
     __shared__ int sPos[kMaxT];
-    __shared__ double sLg[kMaxT * 16];  // log gates, then cumulative, for 16 heads (fp64: l_i - l_j
-                                        // must stay accurate over deep paths)
+    __shared__ double sLg[kMaxT * 16];  // log gates, then cumulative sums, for 16 heads (summed in
+                                        // fp64: l_i - l_j must stay accurate over deep paths)
     __shared__ int sJp[kMaxT];         // jump pointers
     const int b = blockIdx.x, i = threadIdx.x;
+    const int hc = blockIdx.y;            // this CTA's 16 heads
+    const bool lead = hc == 0;            // writes the per-stream outputs
     int bad = 0;
     if (i < T) {
         int par = parent[size_t(b) * T + i];
@@ -36,12 +38,12 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
         sPar[i] = par;
         sS[i] = 0.f;
     }
-    if (bad) raise_err(ws.err, bad);
+    if (bad && lead) raise_err(ws.err, bad);
     __syncthreads();
     jump_paths<4>(T, sPtr, sLen, sS, sM);
 
     // depth and strict-ancestor mask
-    if (i < T) {
+    if (lead && i < T) {
         ws.depth[size_t(b) * T + i] = sLen[i] - 1;
         for (int w = 0; w < ws.W; ++w) {
             uint64_t word = sM[i * 4 + (w >> 1)];
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     // cumulative log gates l_n = log g_n + l_parent(n) for every head, by
     // pointer jumping over 16 heads at a time (ceil(log2 T) rounds)
     int badg = 0;
-    for (int h0 = 0; h0 < H; h0 += 16) {
+    for (int h0 = 16 * hc; h0 < min(H, 16 * hc + 16); h0 += 16) {
         const int hn = min(16, H - h0);
         __syncthreads();
         for (int e = i; e < T * hn; e += blockDim.x) {
@@ -63,7 +65,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
                 badg = CANOPY_DEVERR_GATE;
                 a = 1.f;
             }
-            sLg[n * 16 + hh] = log(double(a));
+            sLg[n * 16 + hh] = double(logf(a));  // fp32 log, fp64 sums
         }
         if (i < T) sJp[i] = sPar[i];
         __syncthreads();
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     // DFS pre-order (children in index order): subtree sizes bottom-up, then
     // each child takes the next free slot after its parent.
     __syncthreads();
+    if (!lead) return;
     if (i == 0) {
         for (int n = 0; n < T; ++n) sSize[n] = 1;
         for (int n = T - 1; n >= 1; --n) sSize[sPar[n]] += sSize[n];
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
 
 cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
                              cudaStream_t st) {
-    prep::tree_prep_kernel<<<B, 256, 0, st>>>(parent, g, T, H, ws);
+    prep::tree_prep_kernel<<<dim3(B, (H + 15) / 16), 256, 0, st>>>(parent, g, T, H, ws);
     return cudaGetLastError();
 }
 
