@@ -44,9 +44,9 @@ WORKLOAD = dict(name="batched verify B=16 T=64 H=16 dk=dv=128 random trees depth
                 case=2, B=16, T=64, H=16, d=128)
 METRIC = "µs per GDN layer tree-verify and verified nodes/s (B=16,T=64); % HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes (read + write) of one verify launch of this workload, from the
-# ncu capture summarised in profiles/verify_fwd_kernel_B16_T64_H16_d128.md;
-# set to None whenever the kernel changes until it is captured again.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one verify
+# launch of the default workload, from an ncu capture of the current kernel;
+# set to None whenever the kernel changes, until it is captured again.
 VERIFY_DRAM_TRAFFIC = 29_550_592
 
 
