@@ -21,6 +21,7 @@ OK, ERR_ARG, ERR_TREE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
 SOLVE = {"fwdsub": 0, "neumann": 1}
 DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+VERIFY_INPUTS_READY = 0x1
 
 # name -> (restype, argtypes); mirrors include/canopy.h
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -28,7 +29,7 @@ SIGNATURES = {
     "canopy_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_workspace_init": (_I, [_P, _S, _P]),
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
-    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, ctypes.c_uint, _P]),
     "canopy_commit": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
@@ -114,8 +115,11 @@ def tree_prep(parent, g, ws):
     _check(load().canopy_tree_prep(_ptr(parent), _ptr(g), T, B, H, _ptr(ws), _stream()), "canopy_tree_prep")
 
 
-def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None):
-    """o [B, T, H, dv] for every node of every stream's tree."""
+def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None,
+           inputs_ready: bool = False):
+    """o [B, T, H, dv] for every node of every stream's tree.  inputs_ready:
+    q, k, v, g, beta and parent are not written by the kernel launched just
+    before this call on the current stream (CANOPY_VERIFY_INPUTS_READY)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     _need(q, "q")
@@ -131,7 +135,7 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
     _need(out, "o", None, (B, T, H, dv))
     st = load().canopy_tree_verify(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
                                    _ptr(parent), T, B, H, dk, dv, SOLVE[solve], _ptr(out), _dt(out),
-                                   _ptr(ws), _stream())
+                                   _ptr(ws), VERIFY_INPUTS_READY if inputs_ready else 0, _stream())
     _check(st, "canopy_tree_verify")
     return out
 

@@ -10,7 +10,7 @@ cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const 
                              const Ws& ws, int bv, int neumann, cudaStream_t st);
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                 const Ws& ws, cudaStream_t st);
+                                 const Ws& ws, int inputs_ready, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
                                cudaStream_t st);
@@ -61,12 +61,12 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                  const float* g, const float* beta, const float* S0, const int32_t* parent, int T,
                                  int B, int H, int dk, int dv, canopy_solve solve, void* o, canopy_dtype o_dtype,
-                                 void* workspace, void* stream) {
+                                 void* workspace, unsigned flags, void* stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
         !aligned16(parent) || !aligned16(o) || !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
-        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN))
+        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN) || (flags & ~CANOPY_VERIFY_INPUTS_READY))
         return CANOPY_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
@@ -77,7 +77,9 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
     if (tc && solve == CANOPY_SOLVE_NEUMANN)
         return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, 0, 1, st));
-    if (tc) return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, st));
+    if (tc)
+        return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws,
+                                                (flags & CANOPY_VERIFY_INPUTS_READY) != 0, st));
     cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, st));

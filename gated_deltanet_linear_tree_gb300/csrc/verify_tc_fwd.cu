@@ -89,6 +89,7 @@ struct Params {
     uint32_t* mask;
     int32_t* err;
     int B, T, H, W, o_bf16;
+    int inputs_ready;  // the inputs other than S0 may be read before the preceding kernel completes
 };
 
 // Two-part bf16 split with integer operations only (the conversion unit is
@@ -168,7 +169,12 @@ __global__ void __launch_bounds__(NT, 2)
     const int h = blockIdx.x, b = blockIdx.y;
     const int T = p.T, H = p.H;
 
-    pdl_wait();
+    // Programmatic dependent launch: the next kernel may begin launching at
+    // once.  With inputs_ready, until the preceding kernel has completed
+    // (pdl_wait, by the thread that requests S0) only q, k, v, g, beta and
+    // parent are read and nothing global is written; S0, the workspace and o
+    // come after.  Otherwise everything waits.
+    if (!p.inputs_ready) pdl_wait();
     pdl_trigger();
     // Parents and gates first (threads 0..63), so that these small loads
     // enter the memory system ahead of the tile copies below.
@@ -190,19 +196,17 @@ __global__ void __launch_bounds__(NT, 2)
         tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, h, 0, b);
         tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, h, 0, b);
         tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, h, 0, b);
-        // then the S0 tile, by the copy engine, into the staging area
-        mbar_expect_tx(&bars[BAR_S0], 4 * L::S0_BOX);
-        for (int i = 0; i < 4; ++i) tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0], 32 * i, 0, h, b);
     }
     if (warp == 0) {
         tmem_alloc(sTmem, kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
-    // Validate; padded nodes: no path, beta 0, gamma 1.
+    // Validate; padded nodes: no path, beta 0, gamma 1.  Error bits are kept
+    // and raised with the tree outputs, after the preceding kernel is done.
+    int bad = 0;
     if (tid < TP) {
         const int i = tid;
-        int bad = 0;
         if (i < T) {
             if (!((i == 0) ? (par == -1) : (par >= 0 && par < i))) {
                 bad |= CANOPY_DEVERR_TREE;
@@ -214,7 +218,6 @@ __global__ void __launch_bounds__(NT, 2)
                 gb = 0.f;
             }
         }
-        if (bad) raise_err(p.err, bad);
         sPar[i] = par;
         sL2[i] = log2f(ga);
         sBeta[i] = gb;
@@ -388,7 +391,9 @@ __global__ void __launch_bounds__(NT, 2)
             }
         }
         fence_proxy_async_smem();
-        // tree outputs for the commit: l (natural log), depth, strict-ancestor mask
+        // tree outputs for the commit: l (natural log), depth, strict-ancestor
+        // mask (X has completed, so the preceding kernel has too)
+        if (bad) raise_err(p.err, bad);
         if (tid < TP && tid < T) {
             p.l[(size_t(b) * T + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
             if (h == 0) {
@@ -418,6 +423,12 @@ __global__ void __launch_bounds__(NT, 2)
                 *sFlag = 1;
             }
             mma_commit(&bars[BAR_AC]);
+            // S0 (and everything written from here on) only once the
+            // preceding kernel of the stream has completed
+            pdl_wait();
+            mbar_expect_tx(&bars[BAR_S0], 4 * L::S0_BOX);
+            for (int i = 0; i < 4; ++i)
+                tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0], 32 * i, 0, h, b);
         }
         __syncwarp();
         // S0 row c (landed in shared memory by the copy engine) -> bf16 hi/lo
@@ -574,7 +585,7 @@ bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                 const Ws& ws, cudaStream_t st) {
+                                 const Ws& ws, int inputs_ready, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mo, mu, ms;
     if (!make_bf16_row_map(&mq, q, B, T, H) || !make_bf16_row_map(&mk, k, B, T, H) ||
         !make_bf16_row_map(&mv, v, B, T, H) || !make_out_map(&mo, o, B, T, H, o_bf16) ||
@@ -595,6 +606,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
+    prm.inputs_ready = inputs_ready;
     const int smem = tcf::Smem::TOTAL + 1024;
     static bool attr = false;
     if (!attr) {

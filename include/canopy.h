@@ -63,6 +63,10 @@ typedef enum {
     CANOPY_SOLVE_NEUMANN = 1   /* finite Neumann series, d rounds (Bole's solve) */
 } canopy_solve;
 
+/* Flags of canopy_tree_verify. */
+#define CANOPY_VERIFY_INPUTS_READY 0x1u  /* q, k, v, g, beta, parent are not written by the
+                                            kernel launched just before this call */
+
 /* Bits of the device error word. */
 #define CANOPY_DEVERR_TREE     0x1  /* parent[b][0] != -1 or parent[b][i] not in [0,i) */
 #define CANOPY_DEVERR_GATE     0x2  /* g <= 0, g or beta not finite                     */
@@ -96,12 +100,21 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
  *   O = diag(gamma) Q S0^T + C U
  * Writes o (device, o_dtype) and, into the workspace, U, l, depth, mask.
  * in_dtype CANOPY_BF16 selects the tensor-core path (tcgen05, bf16 operands,
- * fp32 accumulation); CANOPY_F32 selects the fp32 path.  S0 is read only. */
+ * fp32 accumulation); CANOPY_F32 selects the fp32 path.  S0 is read only.
+ * flags: 0 or CANOPY_VERIFY_INPUTS_READY.  The tensor-core forward-
+ * substitution kernel is launched with programmatic dependent launch and may
+ * begin while the kernel launched just before it on `stream` finishes.  With
+ * flags = 0 it touches no global memory until that kernel has completed.
+ * With CANOPY_VERIFY_INPUTS_READY the caller asserts that q, k, v, g, beta
+ * and parent are not written by that kernel: the call then reads them (and
+ * runs tree prep and the triangular solve) while it finishes; S0, the
+ * workspace and o are still touched only after it has completed.  Other
+ * bits return CANOPY_ERR_ARG. */
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                  const float* g, const float* beta, const float* S0,
                                  const int32_t* parent, int T, int B, int H, int dk, int dv,
                                  canopy_solve solve, void* o, canopy_dtype o_dtype,
-                                 void* workspace, void* stream);
+                                 void* workspace, unsigned flags, void* stream);
 
 /* Commit (canopy page, "The tree closed form", last line, and "What the
  * commit kernel stores"): for every stream b with accepted node a = accepted[b],

@@ -53,9 +53,9 @@ def test_status_strings_and_version(lib):
     assert lib.canopy_version() >= 1
 
 
-def _verify(lib, ptrs, T=64, B=1, H=1, d=128, in_dt=1, solve=0, o_dt=0):
+def _verify(lib, ptrs, T=64, B=1, H=1, d=128, in_dt=1, solve=0, o_dt=0, flags=0):
     q, k, v, g, be, S0, par, o, ws = ptrs
-    return lib.canopy_tree_verify(q, k, v, in_dt, g, be, S0, par, T, B, H, d, d, solve, o, o_dt, ws, None)
+    return lib.canopy_tree_verify(q, k, v, in_dt, g, be, S0, par, T, B, H, d, d, solve, o, o_dt, ws, flags, None)
 
 
 def test_host_argument_errors(lib):
@@ -72,6 +72,7 @@ def test_host_argument_errors(lib):
     assert _verify(lib, good, d=64) == 3                            # unsupported head size
     assert _verify(lib, good, in_dt=7) == 1                         # bad enum
     assert _verify(lib, good, solve=5) == 1
+    assert _verify(lib, good, flags=2) == 1                         # unknown flag
     assert lib.canopy_commit(None, good[1], good[2], good[3], 1, 64, 1, 1, 128, 128, good[4], None) == 1
     assert lib.canopy_commit(good[0], good[1], good[2], good[3], 1, 300, 1, 1, 128, 128, good[4], None) == 3
     assert lib.canopy_tree_prep(good[0], good[1], 0, 1, 1, good[2], None) == 3
