@@ -207,7 +207,9 @@ def capture_graph(canopy, sets, T, solve, n, kind):
                 canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=solve,
                               out=s["o"], inputs_ready=True)
             if kind in ("step", "commit"):
-                canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
+                # the kernel before each commit (its verify, or a commit of
+                # another set) writes neither S0 nor the accepted nodes
+                canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"], state_ready=True)
     torch.cuda.synchronize()
     return g
 

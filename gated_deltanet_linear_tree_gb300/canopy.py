@@ -22,6 +22,7 @@ F32, BF16 = 0, 1
 SOLVE = {"fwdsub": 0, "neumann": 1}
 DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 VERIFY_INPUTS_READY = 0x1
+COMMIT_STATE_READY = 0x1
 
 # name -> (restype, argtypes); mirrors include/canopy.h
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -30,7 +31,7 @@ SIGNATURES = {
     "canopy_workspace_init": (_I, [_P, _S, _P]),
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, ctypes.c_uint, _P]),
-    "canopy_commit": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "canopy_commit": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "canopy_serial_replay_static": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
@@ -140,8 +141,10 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
     return out
 
 
-def commit(accepted, S0, k, ws, T: int, out=None):
-    """S_new [B, H, dv, dk] for the accepted node of every stream."""
+def commit(accepted, S0, k, ws, T: int, out=None, state_ready: bool = False):
+    """S_new [B, H, dv, dk] for the accepted node of every stream.  state_ready:
+    S0 and accepted are not written by the kernel launched just before this
+    call on the current stream (CANOPY_COMMIT_STATE_READY)."""
     B, H, dv, dk = S0.shape
     _need(accepted, "accepted", torch.int32, (B,))
     _need(S0, "S0", torch.float32)
@@ -150,7 +153,7 @@ def commit(accepted, S0, k, ws, T: int, out=None):
         out = torch.empty_like(S0)
     _need(out, "S_new", torch.float32, S0.shape)
     st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _dt(k), T, B, H, dk, dv,
-                              _ptr(ws), _stream())
+                              _ptr(ws), COMMIT_STATE_READY if state_ready else 0, _stream())
     _check(st, "canopy_commit")
     return out
 

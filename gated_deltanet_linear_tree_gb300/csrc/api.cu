@@ -15,7 +15,7 @@ cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int 
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
                                cudaStream_t st);
 cudaError_t launch_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k, int in_bf16,
-                          int T, int B, int H, int d, const Ws& ws, cudaStream_t st);
+                          int T, int B, int H, int d, const Ws& ws, int state_ready, cudaStream_t st);
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
                           const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int d,
                           void* o, int o_bf16, float* snap, int32_t* err, cudaStream_t st);
@@ -87,15 +87,16 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,
                             canopy_dtype in_dtype, int T, int B, int H, int dk, int dv, const void* workspace,
-                            void* stream) {
+                            unsigned flags, void* stream) {
     if (!aligned16(accepted) || !aligned16(S0) || !aligned16(S_new) || !aligned16(k) || !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if (in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) return CANOPY_ERR_ARG;
+    if (flags & ~CANOPY_COMMIT_STATE_READY) return CANOPY_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
     Ws ws = ws_bind(const_cast<void*>(workspace), B, T, H, dv);
     return cuda_status(launch_commit(accepted, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, H, dk, ws,
-                                     static_cast<cudaStream_t>(stream)));
+                                     (flags & CANOPY_COMMIT_STATE_READY) != 0, static_cast<cudaStream_t>(stream)));
 }
 
 canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, canopy_dtype in_dtype,

@@ -35,7 +35,8 @@ __device__ inline float4 k4(const __nv_bfloat16* p) {
 // is stored in place of (or beside) S0.
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted, const float* S0,
-                                                    float* S_new, const InT* __restrict__ k, int T, int H, Ws ws) {
+                                                    float* S_new, const InT* __restrict__ k, int T, int H, Ws ws,
+                                                    int state_ready) {
     constexpr int C4 = DK / 4;             // float4 per state row (threads per row)
     constexpr int F4 = ROWS * C4 / NT;     // float4 per thread = rows per thread
     constexpr int KV = 16 / sizeof(InT);   // k elements per 16-byte load
@@ -56,7 +57,10 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     const int c4 = t % C4, r0 = (t / C4) * F4;
     const size_t sbase = ((size_t(b) * H + h) * DV + v0) * DK;
 
-    pdl_wait();
+    // Programmatic dependent launch: with state_ready, the S0 tile and the
+    // accepted node are read while the preceding kernel finishes; the
+    // workspace and S_new only after it has completed.
+    if (!state_ready) pdl_wait();
     pdl_trigger();
     if (t == 0) {
         mbar_init(&sBar, 1);
@@ -64,6 +68,8 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
         mbar_expect_tx(&sBar, TILE);
         bulk_load(sS, S0 + sbase, TILE, &sBar);
     }
+    const int a_in = (t < 32) ? accepted[b] : -1;
+    if (state_ready) pdl_wait();
     // T <= 64: the stream's masks and the head's gates are read together with
     // the accepted node, so the path costs one dependent round trip less
     const bool spec = T <= 64;
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
             for (int w = t; w < T * ws.W; w += 32) sMaskB[w] = ws.mask[size_t(b) * T * ws.W + w];
             for (int j = t; j < T; j += 32) sLB[j] = ws.l[(size_t(b) * T + j) * H + h];
         }
-        int a = accepted[b];
+        int a = a_in;
         if (a < -1 || a >= T) {
             if (t == 0 && h == 0 && rt == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
             a = -1;
@@ -158,20 +164,20 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
 
 template <typename InT, int D>
 static cudaError_t launch_commit_typed(const int32_t* accepted, const float* S0, float* S_new, const void* k,
-                                       int T, int B, int H, const Ws& ws, cudaStream_t st) {
+                                       int T, int B, int H, const Ws& ws, int state_ready, cudaStream_t st) {
     dim3 grid(D / cm::ROWS, H, B);
     return launch_pdl(cm::commit_kernel<InT, D, D>, grid, dim3(cm::NT), 0, st, accepted, S0, S_new,
-                      static_cast<const InT*>(k), T, H, ws);
+                      static_cast<const InT*>(k), T, H, ws, state_ready);
 }
 
 cudaError_t launch_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k, int in_bf16,
-                          int T, int B, int H, int d, const Ws& ws, cudaStream_t st) {
+                          int T, int B, int H, int d, const Ws& ws, int state_ready, cudaStream_t st) {
     if (d == 128) {
-        if (in_bf16) return launch_commit_typed<__nv_bfloat16, 128>(accepted, S0, S_new, k, T, B, H, ws, st);
-        return launch_commit_typed<float, 128>(accepted, S0, S_new, k, T, B, H, ws, st);
+        if (in_bf16) return launch_commit_typed<__nv_bfloat16, 128>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
+        return launch_commit_typed<float, 128>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
     }
-    if (in_bf16) return launch_commit_typed<__nv_bfloat16, 32>(accepted, S0, S_new, k, T, B, H, ws, st);
-    return launch_commit_typed<float, 32>(accepted, S0, S_new, k, T, B, H, ws, st);
+    if (in_bf16) return launch_commit_typed<__nv_bfloat16, 32>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
+    return launch_commit_typed<float, 32>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
 }
 
 }  // namespace canopy

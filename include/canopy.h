@@ -67,6 +67,10 @@ typedef enum {
 #define CANOPY_VERIFY_INPUTS_READY 0x1u  /* q, k, v, g, beta, parent are not written by the
                                             kernel launched just before this call */
 
+/* Flags of canopy_commit. */
+#define CANOPY_COMMIT_STATE_READY 0x1u   /* S0 and accepted are not written by the kernel
+                                            launched just before this call */
+
 /* Bits of the device error word. */
 #define CANOPY_DEVERR_TREE     0x1  /* parent[b][0] != -1 or parent[b][i] not in [0,i) */
 #define CANOPY_DEVERR_GATE     0x2  /* g <= 0, g or beta not finite                     */
@@ -122,11 +126,19 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
  * using U, l and the ancestor mask that the preceding verify call left in
  * the workspace (same parent, g and T).  a = -1 means nothing accepted:
  * S_new = S0.  S_new may alias S0 (the update is elementwise in S0).
+ * flags: 0 or CANOPY_COMMIT_STATE_READY.  The kernel is launched with
+ * programmatic dependent launch; with flags = 0 it touches no global memory
+ * until the kernel launched just before it on `stream` has completed.  With
+ * CANOPY_COMMIT_STATE_READY the caller asserts that S0 and accepted are not
+ * written by that kernel (a verify call only reads S0): the commit then
+ * requests its S0 tiles and reads accepted while that kernel finishes; the
+ * workspace and S_new are touched only after it has completed.  Other bits
+ * return CANOPY_ERR_ARG.
  *   accepted device int32 [B]; S0, S_new device fp32 [B][H][dv][dk];
  *   k device [B][T][H][dk] in in_dtype (the verify call's k). */
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new,
                             const void* k, canopy_dtype in_dtype, int T, int B, int H,
-                            int dk, int dv, const void* workspace, void* stream);
+                            int dk, int dv, const void* workspace, unsigned flags, void* stream);
 
 /* Bytes of the per-node snapshot buffer of the serial replay:
  * fp32 [B][T][H][dv][dk]. */

@@ -156,3 +156,35 @@ def test_round_trip_fp32_20_rounds(lib):
     wo, ws_ = _round_trip(lib, 4, 64, 4, 20, False, lambda r: range(4))
     print("fp32 20 rounds: worst o err", wo, "worst state err", ws_)
     assert wo <= TOL_F32 and ws_ <= TOL_F32
+
+
+def test_overlapped_verify_commit_steps(lib):
+    """verify(inputs_ready) then commit(state_ready), back to back over
+    rotating input sets (each kernel may start while the one before it
+    finishes), give the same bits as the waiting calls."""
+    sets = []
+    for s in range(3):
+        inp = synth.config_inputs(2, rnd=s)
+        dev = to_device(inp, bf16=True)
+        B, T, H, d = dev["q"].shape
+        dev["ws"] = lib.workspace(B, T, H, d)
+        dev["acc"] = torch.full((B,), T - 1 - s, dtype=torch.int32, device="cuda")
+        sets.append(dev)
+
+    def run(overlap):
+        outs = []
+        for rep in range(2):
+            for dev in sets:
+                o = lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"],
+                               dev["ws"], inputs_ready=overlap)
+                Sn = lib.commit(dev["acc"], dev["S0"], dev["k"], dev["ws"], dev["q"].shape[1], state_ready=overlap)
+                outs.append((o, Sn))
+        torch.cuda.synchronize()
+        return outs
+
+    ref = run(False)
+    got = run(True)
+    for (o0, s0), (o1, s1) in zip(ref, got):
+        assert torch.equal(o0, o1) and torch.equal(s0, s1)
+    for dev in sets:
+        assert lib.read_device_error(dev["ws"]) == 0
