@@ -35,7 +35,8 @@ namespace tcf {
 constexpr int DV = 128;
 constexpr int TP = 64;    // nodes per block
 constexpr int NT = 256;   // threads per CTA
-constexpr int XS = 68;    // row stride (floats) of the per-row work vectors and of Gp
+constexpr int XS = 68;        // row stride (floats) of the work vectors and Gp: paths of up to 64 nodes
+constexpr int XS_SHORT = 36;  // the same for paths of up to 33 nodes (depth <= 32)
 constexpr uint32_t kTmemCols = 256;
 // tensor-memory columns
 constexpr uint32_t TA = 0;      // S0 as A: hi [0,64), lo [64,128); later R^T: hi [0,32), lo [32,64)
@@ -49,6 +50,10 @@ struct Smem {
     static constexpr int V_TILE = 64 * 128;
     static constexpr int XV = VT + 2 * V_TILE;   // per-row work vectors fp32 [128][XS]
     static constexpr int GP = XV + 128 * XS * 4; // Gp fp32 [64][XS]: G rows by path position
+    // trees of depth <= 32: work vectors and Gp with the short stride, clear
+    // of the S0 staging area (so the solve runs while S0 is on its way)
+    static constexpr int XV_SHORT = 65536;
+    static constexpr int GP_SHORT = XV_SHORT + 128 * XS_SHORT * 4;
     static constexpr int PAR = GP + TP * XS * 4; // int[64] parent
     static constexpr int LEN = PAR + 256;        // int[64] path length
     static constexpr int L2 = LEN + 256;         // float[64] log2 gate, then cumulative
@@ -58,6 +63,7 @@ struct Smem {
     static constexpr int BAR = MASK + 512;       // u64[12]
     static constexpr int TMEMSLOT = BAR + 96;    // u32
     static constexpr int FLAG = TMEMSLOT + 4;    // int: a wait gave up
+    static constexpr int NMAX = FLAG + 4;        // int: longest root path (nodes)
 
     static constexpr int BG = BAR + 128;         // float2[64] (beta, beta gamma)
     static constexpr int PLIST = BG + 512;       // u8[64][64] path(i) from the root down
@@ -65,18 +71,19 @@ struct Smem {
     // after the output product: o and U tiles [64 nodes][128 columns] for the TMA stores
     static constexpr int OT = 0;
     static constexpr int UT = 32768;
-    // at the start: the S0 tile (fp32, 4 boxes of [128 rows][32 columns],
-    // 128-byte swizzle) over V, the work vectors and Gp, all unused until it
-    // has been converted into tensor memory
+    // the S0 tile (fp32, 4 boxes of [128 rows][32 columns], 128-byte
+    // swizzle) passes through a two-box staging area, two boxes at a time;
+    // V and the long-stride tables reuse it once it has been converted
     static constexpr int S0S = 32768;
     static constexpr int S0_BOX = 128 * 128;
-    static_assert(S0S + 4 * S0_BOX <= PAR && S0S % 1024 == 0, "S0 staging");
+    static_assert(S0S + 2 * S0_BOX <= XV_SHORT && S0S % 1024 == 0, "S0 staging");
     static_assert(UT + TP * DV * 4 <= PAR, "output tiles overlap the small arrays");
     static_assert(XV % 16 == 0 && GP % 16 == 0 && BAR % 256 == 0 && BG % 16 == 0 && GAM % 16 == 0, "align");
-    static_assert(FLAG + 4 <= BG, "small arrays overlap");
+    static_assert(NMAX + 4 <= BG, "small arrays overlap");
+    static_assert(GP_SHORT + TP * XS_SHORT * 4 <= PAR, "short tables overlap the small arrays");
 };
 
-enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, BAR_S0, BAR_SFREE, NBAR };
+enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, BAR_S0, BAR_S0B, BAR_SFREE, NBAR };
 
 struct Params {
     const float* g;
@@ -157,11 +164,10 @@ __global__ void __launch_bounds__(NT, 2)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + L::TMEMSLOT);
     int* sFlag = reinterpret_cast<int*>(sm + L::FLAG);
+    int* sNmax = reinterpret_cast<int*>(sm + L::NMAX);
 
     uint8_t* sPath = sm + L::PLIST;
     float2* sBG = reinterpret_cast<float2*>(sm + L::BG);
-    float* sX = reinterpret_cast<float*>(sm + L::XV);
-    float* sGp = reinterpret_cast<float*>(sm + L::GP);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
@@ -190,6 +196,7 @@ __global__ void __launch_bounds__(NT, 2)
         for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *sFlag = 0;
+        *sNmax = 0;
         // Q and K next: the solve path waits on them
         mbar_expect_tx(&bars[BAR_QK], 4 * 64 * 64 * 2);
         tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, h, 0, b);
@@ -246,6 +253,7 @@ __global__ void __launch_bounds__(NT, 2)
             }
             sMask[i] = m;
             sLen[i] = n;
+            atomicMax(sNmax, n);
         }
         group_sync(1, 128);
         if (tid < TP) {
@@ -264,13 +272,23 @@ __global__ void __launch_bounds__(NT, 2)
         if (tid == 0) mbar_arrive(&bars[BAR_PREP]);  // gamma is ready for the state warps
 
         // ---- C and G rows from AC (lane r: Q row r, or K row r - 64) ----------
+        // Trees of depth <= 32 keep their tables (short stride) clear of the
+        // S0 staging area; deeper trees use the long stride over it and wait
+        // until S0 has been converted.
+        const bool shortp = *sNmax <= XS_SHORT - 3;
+        const int xs = shortp ? XS_SHORT : XS;
+        float* sX = reinterpret_cast<float*>(sm + (shortp ? L::XV_SHORT : L::XV));
+        float* sGp = reinterpret_cast<float*>(sm + (shortp ? L::GP_SHORT : L::GP));
         const int r = tid;                     // 0..127: TMEM lane of this thread
         const bool qrow = r < TP;
         const int i = r & (TP - 1);
-        float* xr = sX + r * XS;               // this row's work vector
+        float* xr = sX + r * xs;               // this row's work vector
         wait_or_flag(&bars[BAR_AC], sFlag);
-        wait_or_flag(&bars[BAR_SFREE], sFlag);  // the S0 staging area is ours now
         tc_fence_after();
+        // The raw row goes to this thread's private array (local memory,
+        // cached in L1): it is gathered by node index below, and shared
+        // memory has no room for it next to the S0 staging.
+        float raw[TP];
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
             uint32_t a[32];
@@ -278,32 +296,28 @@ __global__ void __launch_bounds__(NT, 2)
             tmem_ld16(lane_base + TD + hc * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
             tmem_wait_ld();
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4)
-                *reinterpret_cast<float4*>(xr + hc * 32 + 4 * j4) =
-                    make_float4(__uint_as_float(a[4 * j4]), __uint_as_float(a[4 * j4 + 1]),
-                                __uint_as_float(a[4 * j4 + 2]), __uint_as_float(a[4 * j4 + 3]));
+            for (int jj = 0; jj < 32; ++jj) raw[hc * 32 + jj] = __uint_as_float(a[jj]);
         }
         tc_fence_before();
         group_sync(1, 128);
         if (tid == 0) mbar_arrive(&bars[BAR_ACC]);  // the AC columns may be overwritten
+        if (!shortp) wait_or_flag(&bars[BAR_SFREE], sFlag);
 
         const int n = (i < T) ? sLen[i] : 0;
         const uint8_t* pl = sPath + i * TP;
         const float li = sL2[i];
         // C row (Q lanes) or G row (K lanes, strict ancestors, scaled by beta)
-        // by path position, four positions per batch (loads before stores;
-        // the C row is compacted in place: position d <= node id j, and a
-        // batch writes only positions below every later read).
+        // by path position, four positions per batch.
         {
             const int cnt = qrow ? n : n - 1;
-            float* dst = qrow ? xr : sGp + i * XS;
+            float* dst = qrow ? xr : sGp + i * xs;
             const float sc = qrow ? 1.f : sBeta[i];
             for (int d0 = 0; d0 < cnt; d0 += 4) {
                 float v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int j = pl[min(d0 + u, cnt - 1)];
-                    v[u] = sc * exp2f(li - sL2[j]) * xr[j];
+                    v[u] = sc * exp2f(li - sL2[j]) * raw[j];
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -336,7 +350,7 @@ __global__ void __launch_bounds__(NT, 2)
                 float xv[4] = {xg.x, xg.y, xg.z, xg.w};
 #pragma unroll
                 for (int q = 3; q >= 1; --q) {
-                    const float4 gq = *reinterpret_cast<const float4*>(sGp + a[q] * XS + base);
+                    const float4 gq = *reinterpret_cast<const float4*>(sGp + a[q] * xs + base);
                     const float pv = (base + q < n) ? xv[q] : 0.f;
                     if (q > 0) xv[0] -= pv * gq.x;
                     if (q > 1) xv[1] -= pv * gq.y;
@@ -347,10 +361,10 @@ __global__ void __launch_bounds__(NT, 2)
                     if (base + q >= n) xv[q] = 0.f;
                 *reinterpret_cast<float4*>(xr + base) = make_float4(xv[0], xv[1], xv[2], xv[3]);
                 if (G == 0) break;
-                const float* g0 = sGp + a[0] * XS;
-                const float* g1 = sGp + a[1] * XS;
-                const float* g2 = sGp + a[2] * XS;
-                const float* g3 = sGp + a[3] * XS;
+                const float* g0 = sGp + a[0] * xs;
+                const float* g1 = sGp + a[1] * xs;
+                const float* g2 = sGp + a[2] * xs;
+                const float* g3 = sGp + a[3] * xs;
 #pragma unroll 2
                 for (int g = G - 1; g >= 0; --g) {
                     float4 x4 = *reinterpret_cast<const float4*>(xr + 4 * g);
@@ -426,19 +440,23 @@ __global__ void __launch_bounds__(NT, 2)
             // S0 (and everything written from here on) only once the
             // preceding kernel of the stream has completed
             pdl_wait();
-            mbar_expect_tx(&bars[BAR_S0], 4 * L::S0_BOX);
-            for (int i = 0; i < 4; ++i)
+            mbar_expect_tx(&bars[BAR_S0], 2 * L::S0_BOX);
+            for (int i = 0; i < 2; ++i)
                 tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0], 32 * i, 0, h, b);
         }
         __syncwarp();
         // S0 row c (landed in shared memory by the copy engine) -> bf16 hi/lo
         // pairs in tensor-memory lane c; the 128-byte swizzle makes these
-        // row-per-thread reads conflict-free.
-        wait_or_flag(&bars[BAR_S0], sFlag);
-        {
+        // row-per-thread reads conflict-free.  Two boxes at a time: the
+        // second half is copied into the staging area once the first half
+        // has been read.
 #pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-                const uint8_t* rowp = sm + L::S0S + i * L::S0_BOX + c * 128;
+        for (int hv = 0; hv < 2; ++hv) {
+            wait_or_flag(&bars[hv ? BAR_S0B : BAR_S0], sFlag);
+#pragma unroll 1
+            for (int ib = 0; ib < 2; ++ib) {
+                const int i = 2 * hv + ib;
+                const uint8_t* rowp = sm + L::S0S + ib * L::S0_BOX + c * 128;
                 uint32_t wh[16], wl[16];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -448,6 +466,14 @@ __global__ void __launch_bounds__(NT, 2)
                 }
                 tmem_st16(lane_base + TA + i * 16, wh);
                 tmem_st16(lane_base + TA + 64 + i * 16, wl);
+            }
+            if (hv == 0) {
+                group_sync(2, 128);  // every thread has read the first half
+                if (tid == 128) {
+                    mbar_expect_tx(&bars[BAR_S0B], 2 * L::S0_BOX);
+                    for (int ib = 0; ib < 2; ++ib)
+                        tma_load_4d(sm + L::S0S + ib * L::S0_BOX, &tmS, &bars[BAR_S0B], 32 * (2 + ib), 0, h, b);
+                }
             }
         }
         tmem_wait_st();
@@ -569,6 +595,7 @@ __global__ void __launch_bounds__(NT, 2)
         raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
         mbar_wait(&bars[BAR_QK], 0);
         mbar_wait(&bars[BAR_S0], 0);
+        mbar_wait(&bars[BAR_S0B], 0);
         mbar_wait(&bars[BAR_V], 0);
     }
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
