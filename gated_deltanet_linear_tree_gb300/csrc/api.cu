@@ -5,9 +5,9 @@
 namespace canopy {
 cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
                              cudaStream_t st);
-cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                             const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                             const Ws& ws, int bv, int neumann, cudaStream_t st);
+cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
+                                  const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
                                  const Ws& ws, int inputs_ready, cudaStream_t st);
@@ -76,7 +76,7 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     const bool tc = in_bf16 && dk == 128 && T <= 64;
     if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
     if (tc && solve == CANOPY_SOLVE_NEUMANN)
-        return cuda_status(launch_verify_tc(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, 0, 1, st));
+        return cuda_status(launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, st));
     if (tc)
         return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws,
                                                 (flags & CANOPY_VERIFY_INPUTS_READY) != 0, st));

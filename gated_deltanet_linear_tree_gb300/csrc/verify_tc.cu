@@ -1,33 +1,35 @@
-// Closed-form tree verify on tcgen05 tensor cores (bf16 q/k/v, fp32 S0,
-// fp32 accumulation in tensor memory), one 64-node block (T <= 64).
+// Closed-form tree verify with the finite Neumann series solve, on tcgen05
+// tensor cores (bf16 q/k/v, fp32 S0, fp32 accumulation in tensor memory), one
+// 64-node block (T <= 64).  The forward-substitution kernel is the default
+// path; this variant is the solve of the canopy page's "Design decisions"
+// (Bole's solve), kept selectable and checked against the same oracle.
 //
 // Method: canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed
 // form" (Bole's Theorem 1):
 //     (I + G) U = R,  R = diag(beta) (V - diag(gamma) K S0^T),
 //     O = diag(gamma) Q S0^T + C U.
-// Here the solve is carried by the inverse W = (I + G)^-1, which has the
-// ancestor sparsity of G, and by M = C W:
-//     U = W R,   O = diag(gamma) Q S0^T + M R.
+// G is strictly lower triangular on the ancestor pattern, so (-G)^m = 0 once
+// m exceeds the tree depth d and W = (I + G)^-1 = sum_{m=0..d} (-G)^m exactly.
+// With M = C W:  U = W R,  O = diag(gamma) Q S0^T + M R.
 // One CTA (256 threads) owns one (stream b, head h) and all 128 value columns:
 //   1. tree prep: parent -> path bitmask, depth, l_i = sum log2 alpha, by
 //      pointer jumping;
-//   2. AC = [Q;K] K^T on tcgen05 (M = 128: Q rows then K rows, N = 64);
-//      C_ij = 2^(l2_i - l2_j) q_i.k_j and G_ij = beta_i 2^(l2_i - l2_j) k_i.k_j
-//      on the root-path entries into shared memory;
-//   3. W = (I + G)^-1 and M = C W by substitution along each node's root
-//      path (rows are independent: W (I + G) = I, M (I + G) = C), in fp32;
-//      the finite Neumann series variant builds W on tcgen05 instead;
-//   4. [M; W] is written to tensor memory as tf32 hi + lo parts (the A
-//      operand of step 6);
-//   5. X = [Q;K] S0^T on tcgen05 (N = 128), issued with step 2; S0 is split
-//      into bf16 hi + lo in shared memory so the product keeps ~16 mantissa
-//      bits of fp32;
-//   6. R = beta (V - gamma X_K) goes to shared memory as tf32 hi + lo; the
+//   2. AC = [Q;K] K^T and X = [Q;K] S0^T on tcgen05 in one commit (M = 128:
+//      Q rows then K rows); S0 is split into bf16 hi + lo in shared memory so
+//      X keeps ~16 mantissa bits of fp32; C_ij = 2^(l2_i - l2_j) q_i.k_j and
+//      G_ij = beta_i 2^(l2_i - l2_j) k_i.k_j on the root-path entries go to
+//      shared memory;
+//   3. W by d rounds P_m = -G P_(m-1) on tcgen05 (G as the tf32 hi + lo A
+//      operand in tensor memory, P^T as the B operand in shared memory, three
+//      products per round), then M = C W on the CUDA cores;
+//   4. [M; W] is written to tensor memory as tf32 hi + lo parts;
+//   5. R = beta (V - gamma X_K) goes to shared memory as tf32 hi + lo; the
 //      X_Q rows are scaled by gamma and the X_K rows zeroed in place; then
 //      X += [M; W] R by three tf32 MMAs (hi*hi + hi*lo + lo*hi), which keeps
 //      fp32 accuracy: rows 0..63 become o, rows 64..127 become U.
 // Decay ratios are only ever 2^(l2_i - l2_j) with j on i's root path, so they
 // lie in (0, 1] and never overflow ("Hard constraints", log-space gates).
+// This file also holds the tensor-map encoders both tensor-core kernels use.
 #include "common.cuh"
 
 namespace canopy {
@@ -132,9 +134,8 @@ __device__ inline void warp0_wait(uint64_t* bar, uint32_t parity, int* sFlag) {
     if (!ok && (threadIdx.x & 31) == 0) *sFlag = 1;
 }
 
-template <bool NEU>
 __global__ void __launch_bounds__(NT, 2)
-    verify_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    verify_neumann_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, Params p) {
     using L = Smem;
     extern __shared__ uint8_t smem_raw[];
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(NT, 2)
         *sDmax = 0;
     }
     if (warp == 0) {
-        tmem_alloc(sTmem, NEU ? kTmemColsNeu : kTmemCols);
+        tmem_alloc(sTmem, kTmemColsNeu);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(NT, 2)
             const int j = j0 + __ffs(bits) - 1;
             trow[j] *= scale * exp2f(li - sL2[j]);
         }
-        if (NEU) {
+        {
             for (int e = tid; e < TP * TP; e += NT) {
                 const int a = e >> 6, c = e & 63;
                 sW[a * RS + c] = (a == c) ? 1.f : 0.f;
@@ -351,61 +352,7 @@ __global__ void __launch_bounds__(NT, 2)
     }
     __syncthreads();
 
-    if constexpr (!NEU) {
-        // W = (I + G)^-1 and M = C W, row by row.  From W (I + G) = I and
-        // M (I + G) = C, for node i and k on its root path,
-        //   W_ik = [i = k] - sum_{e in path(i) below k} W_ie G_ek,
-        //   M_ik =  C_ik   - sum_{e in path(i) below k} M_ie G_ek,
-        // so row i follows from walking i's root path from i upwards; rows
-        // are independent (no level barriers).  One thread per row: the Q
-        // lanes (threads 0..63) build the M rows, the K lanes (64..127) the W
-        // rows, each on its own row in shared memory, then write that row to
-        // its tensor-memory lane as the A operand (tf32 hi + lo, zero off the
-        // path).
-        if (warp < 4) {
-            const bool qrow = row < 64;
-            const int i = qrow ? row : row - 64;
-            float* orow = (qrow ? sM : sW) + i * RS;
-            if (i < T) {
-                const float* crow = sC + i * RS;
-                const uint8_t* pl = sPath + i * TP;
-                const int n = sLen[i];  // path length, i is at position n - 1
-                for (int d = n - 1; d >= 0; --d) {
-                    const int k = pl[d];
-                    float a0 = qrow ? crow[k] : ((d == n - 1) ? 1.f : 0.f), a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                    int e = d + 1;
-                    for (; e + 3 < n; e += 4) {
-                        const int e0 = pl[e], e1 = pl[e + 1], e2 = pl[e + 2], e3 = pl[e + 3];
-                        a0 -= orow[e0] * sG[e0 * RS + k];
-                        a1 -= orow[e1] * sG[e1 * RS + k];
-                        a2 -= orow[e2] * sG[e2 * RS + k];
-                        a3 -= orow[e3] * sG[e3 * RS + k];
-                    }
-                    for (; e < n; ++e) {
-                        const int e0 = pl[e];
-                        a0 -= orow[e0] * sG[e0 * RS + k];
-                    }
-                    orow[k] = (a0 + a1) + (a2 + a3);
-                }
-            }
-            // row -> tensor memory (whole warps; rows past T are zero)
-            const uint64_t pm = (i < T) ? sMask[i] : 0ull;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t rh[16], rl[16];
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = cb * 16 + jj;
-                    const float x = ((pm >> j) & 1ull) ? orow[j] : 0.f;
-                    split_tf32(x, rh[jj], rl[jj]);
-                }
-                tmem_st16(lane_base + AH + cb * 16, rh);
-                tmem_st16(lane_base + AL + cb * 16, rl);
-            }
-            tmem_wait_st();
-        }
-        __syncthreads();
-    } else {
+    {
         // Finite Neumann series (Bole's solve) for W = sum_{m=0..d} (-G)^m on
         // tcgen05: P_0 = I, P_m = -G P_{m-1}, d rounds; G is the A operand in
         // tensor memory (K rows, tf32 hi + lo), P^T the B operand in shared
@@ -519,7 +466,7 @@ __global__ void __launch_bounds__(NT, 2)
     }
 
 
-    if constexpr (NEU) {
+    {
         // [M; W] -> tensor memory as tf32 hi and lo; each warp takes 32 columns.
         {
             const bool qrow = row < 64;
@@ -671,7 +618,7 @@ fail:
 teardown:
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, NEU ? kTmemColsNeu : kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kTmemColsNeu);
 }
 
 }  // namespace tc
@@ -741,29 +688,27 @@ bool make_state_map(CUtensorMap* m, const float* base, int B, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool NEU>
-static cudaError_t launch_tc(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
+static cudaError_t launch_neumann(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
     if (!make_bf16_row_map(&mq, q, prm.B, prm.T, prm.H) || !make_bf16_row_map(&mk, k, prm.B, prm.T, prm.H) ||
         !make_bf16_row_map(&mv, prm.v, prm.B, prm.T, prm.H))
         return cudaErrorInvalidValue;
-    const int smem = (NEU ? tc::Smem::TOTAL_NEU : tc::Smem::TOTAL) + 1024;
+    const int smem = tc::Smem::TOTAL_NEU + 1024;
     static bool attr = false;
     if (!attr) {
         cudaError_t e =
-            cudaFuncSetAttribute(tc::verify_kernel<NEU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            cudaFuncSetAttribute(tc::verify_neumann_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     dim3 grid(prm.H, prm.B);
-    tc::verify_kernel<NEU><<<grid, tc::NT, smem, st>>>(mq, mk, mv, prm);
+    tc::verify_neumann_kernel<<<grid, tc::NT, smem, st>>>(mq, mk, mv, prm);
     return cudaGetLastError();
 }
 
-cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                             const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                             const Ws& ws, int bv, int neumann, cudaStream_t st) {
-    (void)bv;
+cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
+                                  const Ws& ws, cudaStream_t st) {
     tc::Params prm;
     prm.v = static_cast<const __nv_bfloat16*>(v);
     prm.g = g;
@@ -781,8 +726,7 @@ cudaError_t launch_verify_tc(const void* q, const void* k, const void* v, const 
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
-    if (neumann) return launch_tc<true>(q, k, prm, st);
-    return launch_tc<false>(q, k, prm, st);
+    return launch_neumann(q, k, prm, st);
 }
 
 }  // namespace canopy

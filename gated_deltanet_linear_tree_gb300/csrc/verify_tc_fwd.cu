@@ -68,22 +68,25 @@ struct Smem {
     static constexpr int BG = BAR + 128;         // float2[64] (beta, beta gamma)
     static constexpr int PLIST = BG + 512;       // u8[64][64] path(i) from the root down
     static constexpr int TOTAL = PLIST + TP * TP;
-    // after the output product: o and U tiles [64 nodes][128 columns] for the TMA stores
-    static constexpr int OT = 0;
+    // after the output product: o and U tiles [64 nodes][128 columns] for the
+    // TMA stores, clear of the [M; W] operand (the U product still reads it
+    // while the o tile is written)
     static constexpr int UT = 32768;
+    static constexpr int OT = 65536;
     // the S0 tile (fp32, 4 boxes of [128 rows][32 columns], 128-byte
     // swizzle) passes through a two-box staging area, two boxes at a time;
     // V and the long-stride tables reuse it once it has been converted
     static constexpr int S0S = 32768;
     static constexpr int S0_BOX = 128 * 128;
     static_assert(S0S + 2 * S0_BOX <= XV_SHORT && S0S % 1024 == 0, "S0 staging");
-    static_assert(UT + TP * DV * 4 <= PAR, "output tiles overlap the small arrays");
+    static_assert(UT + TP * DV * 4 <= OT && OT + TP * DV * 4 <= PAR, "output tiles overlap");
     static_assert(XV % 16 == 0 && GP % 16 == 0 && BAR % 256 == 0 && BG % 16 == 0 && GAM % 16 == 0, "align");
     static_assert(NMAX + 4 <= BG, "small arrays overlap");
     static_assert(GP_SHORT + TP * XS_SHORT * 4 <= PAR, "short tables overlap the small arrays");
 };
 
-enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, BAR_S0, BAR_S0B, BAR_SFREE, NBAR };
+enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, BAR_YU, BAR_S0, BAR_S0B, BAR_SFREE, NBAR };
+static_assert(NBAR <= 12, "barrier slots");
 
 struct Params {
     const float* g;
@@ -390,10 +393,12 @@ __global__ void __launch_bounds__(NT, 2)
         {
             uint8_t* bh = sm + L::BH + r * 128;
             uint8_t* bl = sm + L::BL + r * 128;
+            // zero the row chunk by chunk in swizzled order, so that the eight
+            // rows of a quarter-warp write eight different bank groups
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                *reinterpret_cast<uint4*>(bh + (c << 4)) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(bl + (c << 4)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(bh + ((c ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(bl + ((c ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
             }
             for (int d = 0; d < n; ++d) {
                 const int j = pl[d];
@@ -467,39 +472,39 @@ __global__ void __launch_bounds__(NT, 2)
                 tmem_st16(lane_base + TA + i * 16, wh);
                 tmem_st16(lane_base + TA + 64 + i * 16, wl);
             }
-            if (hv == 0) {
-                group_sync(2, 128);  // every thread has read the first half
-                if (tid == 128) {
+            tmem_wait_st();
+            tc_fence_before();
+            group_sync(2, 128);  // every thread has read (and stored) this half
+            if (tid == 128) {
+                if (hv == 0) {
                     mbar_expect_tx(&bars[BAR_S0B], 2 * L::S0_BOX);
                     for (int ib = 0; ib < 2; ++ib)
                         tma_load_4d(sm + L::S0S + ib * L::S0_BOX, &tmS, &bars[BAR_S0B], 32 * (2 + ib), 0, h, b);
+                    // the AC columns must have been read out before X
+                    // overwrites them
+                    if (!mbar_wait(&bars[BAR_ACC], 0)) *sFlag = 1;
+                } else {
+                    mbar_arrive(&bars[BAR_SFREE]);  // the staging area is free: V, then the solve tables
+                    mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
+                    tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
+                    tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
                 }
+                // X^T = S0 [Q;K]^T (M = 128 value rows, N = 128 nodes), the
+                // 64 keys of this half (hi and lo parts) while the next
+                // half is on its way
+                tc_fence_after();
+                const uint32_t aQK = smem_u32(sQK);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int ks = 4 * hv + k4;
+                        const uint64_t db = sdesc_sw128(aQK + hv * 16384 + k4 * 32);
+                        mma_bf16_ts(tmem + TD, tmem + TA + part * 64 + ks * 8, db, idesc_bf16(128, 128),
+                                    (hv | part | k4) != 0);
+                    }
+                if (hv == 1) mma_commit(&bars[BAR_X]);
             }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        group_sync(2, 128);
-        if (tid == 128) {
-            mbar_arrive(&bars[BAR_SFREE]);  // the staging area is free: V, then the solve tables
-            mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
-            tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
-            tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
-        }
-        if (tid == 128) {
-            // X^T = S0 [Q;K]^T (M = 128 value rows, N = 128 nodes) once the
-            // AC columns have been read out
-            if (!mbar_wait(&bars[BAR_ACC], 0)) *sFlag = 1;
-            tc_fence_after();
-            const uint32_t aQK = smem_u32(sQK);
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t db = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
-                    mma_bf16_ts(tmem + TD, tmem + TA + part * 64 + ks * 8, db, idesc_bf16(128, 128),
-                                (part | ks) != 0);
-                }
-            mma_commit(&bars[BAR_X]);
         }
         __syncwarp();
 
@@ -535,6 +540,8 @@ __global__ void __launch_bounds__(NT, 2)
     __syncthreads();
 
     // ---- Y^T = [gamma X_Q^T | 0] + R^T [M; W]^T (bf16 x3) -------------------------
+    // o columns first, with their own commit: the o tile is written and
+    // stored while the U product runs.
     if (tid == 128) {
         tc_fence_after();
         const uint32_t bH = smem_u32(sm + L::BH), bL = smem_u32(sm + L::BL);
@@ -551,15 +558,16 @@ __global__ void __launch_bounds__(NT, 2)
                     mma_bf16_ts(d, tmem + acol + ks * 8, sdesc_sw128(bb + ks * 32), idesc_bf16(128, 64),
                                 (part == 0) || pass != 0 || ks != 0);
             }
+            mma_commit(&bars[part ? BAR_YU : BAR_Y]);
         }
-        mma_commit(&bars[BAR_Y]);
     }
     __syncwarp();
-    wait_or_flag(&bars[BAR_Y], sFlag);
+    wait_or_flag(&bars[solve ? BAR_Y : BAR_YU], sFlag);
     tc_fence_after();
 
     // ---- store: warps 0-3 o, warps 4-7 U (lane = value column) into shared
-    // tiles [node][column], then one TMA store each (rows past T clipped) ---
+    // tiles [node][column], then one TMA store per warp group (rows past T
+    // clipped) ---
     {
         const int c = quad * 32 + lane;
         const uint32_t col0 = TD + (solve ? 0 : 64);
@@ -581,15 +589,15 @@ __global__ void __launch_bounds__(NT, 2)
         }
         fence_proxy_async_smem();
     }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        tma_store_4d(&tmO, sm + L::OT, 0, h, 0, b);
-        tma_store_4d(&tmU, sm + L::UT, 0, h, 0, b);
+    if (solve)
+        group_sync(1, 128);
+    else
+        group_sync(2, 128);
+    if (tid == 0 || tid == 128) {
+        tma_store_4d(solve ? &tmO : &tmU, sm + (solve ? L::OT : L::UT), 0, h, 0, b);
         bulk_commit_group();
+        bulk_wait_read_all();
     }
-
-    if (tid == 0) bulk_wait_read_all();
     if (tid == 128 && *sFlag) {
         // a wait gave up: let the copies in flight land before leaving
         raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
@@ -598,6 +606,8 @@ __global__ void __launch_bounds__(NT, 2)
         mbar_wait(&bars[BAR_S0B], 0);
         mbar_wait(&bars[BAR_V], 0);
     }
+    tc_fence_before();
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
