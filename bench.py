@@ -203,9 +203,10 @@ def capture_graph(canopy, sets, T, solve, n, kind):
             s = sets[i % len(sets)]
             if kind in ("step", "verify"):
                 # the kernel before each verify in the graph (a commit or a
-                # verify of another input set) never writes its inputs
+                # verify of another input set) never writes its inputs, S0
+                # included (commits write S_new)
                 canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=solve,
-                              out=s["o"], inputs_ready=True)
+                              out=s["o"], inputs_ready=True, state_ready=True)
             if kind in ("step", "commit"):
                 # the kernel before each commit (its verify, or a commit of
                 # another set) writes neither S0 nor the accepted nodes

@@ -22,6 +22,7 @@ F32, BF16 = 0, 1
 SOLVE = {"fwdsub": 0, "neumann": 1}
 DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 VERIFY_INPUTS_READY = 0x1
+VERIFY_STATE_READY = 0x2
 COMMIT_STATE_READY = 0x1
 
 # name -> (restype, argtypes); mirrors include/canopy.h
@@ -117,10 +118,11 @@ def tree_prep(parent, g, ws):
 
 
 def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None,
-           inputs_ready: bool = False):
+           inputs_ready: bool = False, state_ready: bool = False):
     """o [B, T, H, dv] for every node of every stream's tree.  inputs_ready:
     q, k, v, g, beta and parent are not written by the kernel launched just
-    before this call on the current stream (CANOPY_VERIFY_INPUTS_READY)."""
+    before this call on the current stream (CANOPY_VERIFY_INPUTS_READY);
+    state_ready (with inputs_ready): nor is S0 (CANOPY_VERIFY_STATE_READY)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     _need(q, "q")
@@ -136,7 +138,8 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
     _need(out, "o", None, (B, T, H, dv))
     st = load().canopy_tree_verify(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
                                    _ptr(parent), T, B, H, dk, dv, SOLVE[solve], _ptr(out), _dt(out),
-                                   _ptr(ws), VERIFY_INPUTS_READY if inputs_ready else 0, _stream())
+                                   _ptr(ws), (VERIFY_INPUTS_READY if inputs_ready else 0)
+                                   | (VERIFY_STATE_READY if state_ready else 0), _stream())
     _check(st, "canopy_tree_verify")
     return out
 

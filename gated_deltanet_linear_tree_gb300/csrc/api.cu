@@ -10,7 +10,7 @@ cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, c
                                   const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                 const Ws& ws, int inputs_ready, cudaStream_t st);
+                                 const Ws& ws, int inputs_ready, int state_ready, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
                                cudaStream_t st);
@@ -66,7 +66,7 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         !aligned16(parent) || !aligned16(o) || !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
-        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN) || (flags & ~CANOPY_VERIFY_INPUTS_READY))
+        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN) || (flags & ~(CANOPY_VERIFY_INPUTS_READY | CANOPY_VERIFY_STATE_READY)))
         return CANOPY_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
@@ -79,7 +79,8 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         return cuda_status(launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, st));
     if (tc)
         return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws,
-                                                (flags & CANOPY_VERIFY_INPUTS_READY) != 0, st));
+                                                (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
+                                                (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
     cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, st));

@@ -41,8 +41,8 @@ constexpr int DV = 128;
 constexpr int TP = 64;       // nodes per block
 constexpr int RS = 65;       // padded row stride (floats) of the T x T tables
 constexpr int NT = 256;      // threads per CTA
-constexpr uint32_t kTmemCols = 256;  // X [0,128), A hi [128,192), A lo [192,256)
-constexpr uint32_t kTmemColsNeu = 512;  // + Neumann products G P at [256,320)
+// X [0,128), A hi [128,192), A lo [192,256), the products G P at [256,320)
+constexpr uint32_t kTmemColsNeu = 512;
 constexpr int YC = 256;
 constexpr int XC = 0, AH = 128, AL = 192;
 

@@ -74,7 +74,7 @@ struct Smem {
     static constexpr int UT = 32768;
     static constexpr int OT = 65536;
     // the S0 tile (fp32, 4 boxes of [128 rows][32 columns], 128-byte
-    // swizzle) passes through a two-box staging area, two boxes at a time;
+    // swizzle) passes through a two-box staging area, one slot per box;
     // V and the long-stride tables reuse it once it has been converted
     static constexpr int S0S = 32768;
     static constexpr int S0_BOX = 128 * 128;
@@ -86,6 +86,7 @@ struct Smem {
 };
 
 enum { BAR_QK = 0, BAR_V, BAR_PREP, BAR_AC, BAR_ACC, BAR_X, BAR_Y, BAR_YU, BAR_S0, BAR_S0B, BAR_SFREE, NBAR };
+static_assert(BAR_S0B == BAR_S0 + 1, "S0 slot barriers");
 static_assert(NBAR <= 12, "barrier slots");
 
 struct Params {
@@ -100,6 +101,7 @@ struct Params {
     int32_t* err;
     int B, T, H, W, o_bf16;
     int inputs_ready;  // the inputs other than S0 may be read before the preceding kernel completes
+    int state_ready;   // with inputs_ready: S0 too
 };
 
 // Two-part bf16 split with integer operations only (the conversion unit is
@@ -182,7 +184,9 @@ __global__ void __launch_bounds__(NT, 2)
     // once.  With inputs_ready, until the preceding kernel has completed
     // (pdl_wait, by the thread that requests S0) only q, k, v, g, beta and
     // parent are read and nothing global is written; S0, the workspace and o
-    // come after.  Otherwise everything waits.
+    // come after.  With state_ready as well, S0 is read early too, and only
+    // the writes wait (each writing thread waits itself).  Otherwise
+    // everything waits.
     if (!p.inputs_ready) pdl_wait();
     pdl_trigger();
     // Parents and gates first (threads 0..63), so that these small loads
@@ -310,21 +314,25 @@ __global__ void __launch_bounds__(NT, 2)
         const uint8_t* pl = sPath + i * TP;
         const float li = sL2[i];
         // C row (Q lanes) or G row (K lanes, strict ancestors, scaled by beta)
-        // by path position, four positions per batch.
+        // by path position, eight positions per batch (the raw row is in
+        // local memory, and its loads should overlap).
         {
             const int cnt = qrow ? n : n - 1;
             float* dst = qrow ? xr : sGp + i * xs;
             const float sc = qrow ? 1.f : sBeta[i];
-            for (int d0 = 0; d0 < cnt; d0 += 4) {
-                float v[4];
+            for (int d0 = 0; d0 < cnt; d0 += 8) {
+                int jj[8];
+                float rv[8], lv[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int j = pl[min(d0 + u, cnt - 1)];
-                    v[u] = sc * exp2f(li - sL2[j]) * raw[j];
+                for (int u = 0; u < 8; ++u) jj[u] = pl[min(d0 + u, cnt - 1)];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    rv[u] = raw[jj[u]];
+                    lv[u] = sL2[jj[u]];
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (d0 + u < cnt) dst[d0 + u] = v[u];
+                for (int u = 0; u < 8; ++u)
+                    if (d0 + u < cnt) dst[d0 + u] = sc * exp2f(li - lv[u]) * rv[u];
             }
             if (!qrow && n > 0) {
                 // Gp row zero-padded by 4; the work vector becomes e_(n-1)
@@ -411,7 +419,8 @@ __global__ void __launch_bounds__(NT, 2)
         }
         fence_proxy_async_smem();
         // tree outputs for the commit: l (natural log), depth, strict-ancestor
-        // mask (X has completed, so the preceding kernel has too)
+        // mask, once the preceding kernel has completed
+        if (tid < TP) pdl_wait();
         if (bad) raise_err(p.err, bad);
         if (tid < TP && tid < T) {
             p.l[(size_t(b) * T + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
@@ -442,68 +451,71 @@ __global__ void __launch_bounds__(NT, 2)
                 *sFlag = 1;
             }
             mma_commit(&bars[BAR_AC]);
-            // S0 (and everything written from here on) only once the
-            // preceding kernel of the stream has completed
-            pdl_wait();
-            mbar_expect_tx(&bars[BAR_S0], 2 * L::S0_BOX);
-            for (int i = 0; i < 2; ++i)
-                tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0], 32 * i, 0, h, b);
+            // S0 only once the preceding kernel of the stream has completed,
+            // unless the caller says it does not write S0
+            if (!p.state_ready) pdl_wait();
+            for (int i = 0; i < 2; ++i) {
+                mbar_expect_tx(&bars[BAR_S0 + i], L::S0_BOX);
+                tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0 + i], 32 * i, 0, h, b);
+            }
         }
         __syncwarp();
         // S0 row c (landed in shared memory by the copy engine) -> bf16 hi/lo
         // pairs in tensor-memory lane c; the 128-byte swizzle makes these
-        // row-per-thread reads conflict-free.  Two boxes at a time: the
-        // second half is copied into the staging area once the first half
-        // has been read.
+        // row-per-thread reads conflict-free.  The four boxes (32 keys each)
+        // pass through two slots: box i uses slot i & 1 (barrier BAR_S0 +
+        // (i & 1), phase i >> 1), and a slot is requested again as soon as
+        // its box has been read.
 #pragma unroll 1
-        for (int hv = 0; hv < 2; ++hv) {
-            wait_or_flag(&bars[hv ? BAR_S0B : BAR_S0], sFlag);
-#pragma unroll 1
-            for (int ib = 0; ib < 2; ++ib) {
-                const int i = 2 * hv + ib;
-                const uint8_t* rowp = sm + L::S0S + ib * L::S0_BOX + c * 128;
-                uint32_t wh[16], wl[16];
+        for (int i = 0; i < 4; ++i) {
+            const int slot = i & 1;
+            if (!mbar_wait(&bars[BAR_S0 + slot], uint32_t(i >> 1))) *sFlag = 1;
+            const uint8_t* rowp = sm + L::S0S + slot * L::S0_BOX + c * 128;
+            uint32_t wh[16], wl[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 f = *reinterpret_cast<const float4*>(rowp + ((j ^ (c & 7)) << 4));
-                    split2(f.x, f.y, wh[2 * j], wl[2 * j]);
-                    split2(f.z, f.w, wh[2 * j + 1], wl[2 * j + 1]);
-                }
-                tmem_st16(lane_base + TA + i * 16, wh);
-                tmem_st16(lane_base + TA + 64 + i * 16, wl);
+            for (int j = 0; j < 8; ++j) {
+                const float4 f = *reinterpret_cast<const float4*>(rowp + ((j ^ (c & 7)) << 4));
+                split2(f.x, f.y, wh[2 * j], wl[2 * j]);
+                split2(f.z, f.w, wh[2 * j + 1], wl[2 * j + 1]);
             }
+            tmem_st16(lane_base + TA + i * 16, wh);
+            tmem_st16(lane_base + TA + 64 + i * 16, wl);
             tmem_wait_st();
             tc_fence_before();
-            group_sync(2, 128);  // every thread has read (and stored) this half
+            group_sync(2, 128);  // every thread has read (and stored) box i
             if (tid == 128) {
-                if (hv == 0) {
-                    mbar_expect_tx(&bars[BAR_S0B], 2 * L::S0_BOX);
-                    for (int ib = 0; ib < 2; ++ib)
-                        tma_load_4d(sm + L::S0S + ib * L::S0_BOX, &tmS, &bars[BAR_S0B], 32 * (2 + ib), 0, h, b);
-                    // the AC columns must have been read out before X
-                    // overwrites them
-                    if (!mbar_wait(&bars[BAR_ACC], 0)) *sFlag = 1;
-                } else {
+                if (i < 2) {
+                    mbar_expect_tx(&bars[BAR_S0 + slot], L::S0_BOX);
+                    tma_load_4d(sm + L::S0S + slot * L::S0_BOX, &tmS, &bars[BAR_S0 + slot], 32 * (i + 2), 0, h,
+                                b);
+                }
+                if (i == 3) {
                     mbar_arrive(&bars[BAR_SFREE]);  // the staging area is free: V, then the solve tables
                     mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
                     tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
                     tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
                 }
-                // X^T = S0 [Q;K]^T (M = 128 value rows, N = 128 nodes), the
-                // 64 keys of this half (hi and lo parts) while the next
-                // half is on its way
-                tc_fence_after();
-                const uint32_t aQK = smem_u32(sQK);
+                if (i & 1) {
+                    // X^T = S0 [Q;K]^T (M = 128 value rows, N = 128 nodes)
+                    // over the 64 keys of boxes i - 1 and i (hi and lo
+                    // parts); the first half goes while boxes 2 and 3 are
+                    // on their way.  The AC columns must have been read out
+                    // before X overwrites them.
+                    const int hv = i >> 1;
+                    if (hv == 0 && !mbar_wait(&bars[BAR_ACC], 0)) *sFlag = 1;
+                    tc_fence_after();
+                    const uint32_t aQK = smem_u32(sQK);
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const int ks = 4 * hv + k4;
-                        const uint64_t db = sdesc_sw128(aQK + hv * 16384 + k4 * 32);
-                        mma_bf16_ts(tmem + TD, tmem + TA + part * 64 + ks * 8, db, idesc_bf16(128, 128),
-                                    (hv | part | k4) != 0);
-                    }
-                if (hv == 1) mma_commit(&bars[BAR_X]);
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const int ks = 4 * hv + k4;
+                            const uint64_t db = sdesc_sw128(aQK + hv * 16384 + k4 * 32);
+                            mma_bf16_ts(tmem + TD, tmem + TA + part * 64 + ks * 8, db, idesc_bf16(128, 128),
+                                        (hv | part | k4) != 0);
+                        }
+                    if (hv == 1) mma_commit(&bars[BAR_X]);
+                }
             }
         }
         __syncwarp();
@@ -594,6 +606,7 @@ __global__ void __launch_bounds__(NT, 2)
     else
         group_sync(2, 128);
     if (tid == 0 || tid == 128) {
+        pdl_wait();
         tma_store_4d(solve ? &tmO : &tmU, sm + (solve ? L::OT : L::UT), 0, h, 0, b);
         bulk_commit_group();
         bulk_wait_read_all();
@@ -601,9 +614,9 @@ __global__ void __launch_bounds__(NT, 2)
     if (tid == 128 && *sFlag) {
         // a wait gave up: let the copies in flight land before leaving
         raise_err(p.err, CANOPY_DEVERR_TIMEOUT);
+        // (thread 128 issued every S0 and V copy; each wait is bounded)
         mbar_wait(&bars[BAR_QK], 0);
-        mbar_wait(&bars[BAR_S0], 0);
-        mbar_wait(&bars[BAR_S0B], 0);
+        for (int i = 0; i < 4; ++i) mbar_wait(&bars[BAR_S0 + (i & 1)], uint32_t(i >> 1));
         mbar_wait(&bars[BAR_V], 0);
     }
     tc_fence_before();
@@ -622,7 +635,7 @@ bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                 const Ws& ws, int inputs_ready, cudaStream_t st) {
+                                 const Ws& ws, int inputs_ready, int state_ready, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mo, mu, ms;
     if (!make_bf16_row_map(&mq, q, B, T, H) || !make_bf16_row_map(&mk, k, B, T, H) ||
         !make_bf16_row_map(&mv, v, B, T, H) || !make_out_map(&mo, o, B, T, H, o_bf16) ||
@@ -644,6 +657,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
     prm.inputs_ready = inputs_ready;
+    prm.state_ready = inputs_ready && state_ready;
     const int smem = tcf::Smem::TOTAL + 1024;
     static bool attr = false;
     if (!attr) {

@@ -66,6 +66,8 @@ typedef enum {
 /* Flags of canopy_tree_verify. */
 #define CANOPY_VERIFY_INPUTS_READY 0x1u  /* q, k, v, g, beta, parent are not written by the
                                             kernel launched just before this call */
+#define CANOPY_VERIFY_STATE_READY 0x2u   /* S0 is not written by the kernel launched just
+                                            before this call */
 
 /* Flags of canopy_commit. */
 #define CANOPY_COMMIT_STATE_READY 0x1u   /* S0 and accepted are not written by the kernel
@@ -105,15 +107,20 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
  * Writes o (device, o_dtype) and, into the workspace, U, l, depth, mask.
  * in_dtype CANOPY_BF16 selects the tensor-core path (tcgen05, bf16 operands,
  * fp32 accumulation); CANOPY_F32 selects the fp32 path.  S0 is read only.
- * flags: 0 or CANOPY_VERIFY_INPUTS_READY.  The tensor-core forward-
- * substitution kernel is launched with programmatic dependent launch and may
- * begin while the kernel launched just before it on `stream` finishes.  With
- * flags = 0 it touches no global memory until that kernel has completed.
- * With CANOPY_VERIFY_INPUTS_READY the caller asserts that q, k, v, g, beta
- * and parent are not written by that kernel: the call then reads them (and
- * runs tree prep and the triangular solve) while it finishes; S0, the
- * workspace and o are still touched only after it has completed.  Other
- * bits return CANOPY_ERR_ARG. */
+ * flags: 0, or CANOPY_VERIFY_INPUTS_READY, optionally with
+ * CANOPY_VERIFY_STATE_READY.  The tensor-core forward-substitution kernel is
+ * launched with programmatic dependent launch and may begin while the kernel
+ * launched just before it on `stream` finishes.  With flags = 0 it touches
+ * no global memory until that kernel has completed.  With
+ * CANOPY_VERIFY_INPUTS_READY the caller asserts that q, k, v, g, beta and
+ * parent are not written by that kernel: the call then reads them (and runs
+ * tree prep and the triangular solve) while it finishes.  Adding
+ * CANOPY_VERIFY_STATE_READY asserts the same of S0 (for instance, the
+ * preceding kernel is another layer's verify or commit): S0 is then read
+ * early too.  The workspace and o are written only after that kernel has
+ * completed, whatever the flags.  CANOPY_VERIFY_STATE_READY without
+ * CANOPY_VERIFY_INPUTS_READY has no effect; other bits return
+ * CANOPY_ERR_ARG. */
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                  const float* g, const float* beta, const float* S0,
                                  const int32_t* parent, int T, int B, int H, int dk, int dv,

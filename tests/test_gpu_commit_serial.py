@@ -159,7 +159,7 @@ def test_round_trip_fp32_20_rounds(lib):
 
 
 def test_overlapped_verify_commit_steps(lib):
-    """verify(inputs_ready) then commit(state_ready), back to back over
+    """verify(inputs_ready, state_ready) then commit(state_ready), back to back over
     rotating input sets (each kernel may start while the one before it
     finishes), give the same bits as the waiting calls."""
     sets = []
@@ -176,7 +176,7 @@ def test_overlapped_verify_commit_steps(lib):
         for rep in range(2):
             for dev in sets:
                 o = lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"],
-                               dev["ws"], inputs_ready=overlap)
+                               dev["ws"], inputs_ready=overlap, state_ready=overlap)
                 Sn = lib.commit(dev["acc"], dev["S0"], dev["k"], dev["ws"], dev["q"].shape[1], state_ready=overlap)
                 outs.append((o, Sn))
         torch.cuda.synchronize()

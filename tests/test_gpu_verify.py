@@ -190,10 +190,12 @@ def test_deterministic_and_guarded(lib):
     assert (buf[:64] == 7.25).all() and (buf[64 + n:] == 7.25).all()
 
 
-def test_inputs_ready_overlap_back_to_back(lib):
-    """With inputs_ready, back-to-back verifies (each may start while the
-    previous one finishes, reading only its own inputs early) give the same
-    bits as calls that wait, for several input sets sharing nothing."""
+@pytest.mark.parametrize("state_ready", [False, True])
+def test_inputs_ready_overlap_back_to_back(lib, state_ready):
+    """With inputs_ready (and state_ready: S0 read early as well),
+    back-to-back verifies (each may start while the previous one finishes,
+    reading its own inputs early) give the same bits as calls that wait, for
+    several input sets sharing nothing."""
     sets = []
     for s in range(3):
         inp = synth.config_inputs(2, rnd=s)
@@ -210,7 +212,7 @@ def test_inputs_ready_overlap_back_to_back(lib):
     for rep in range(3):
         for inp, dev in sets:
             outs.append(lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"],
-                                   dev["ws"], inputs_ready=True))
+                                   dev["ws"], inputs_ready=True, state_ready=state_ready))
     torch.cuda.synchronize()
     for idx, o in enumerate(outs):
         assert torch.equal(o, ref[idx % len(sets)])
