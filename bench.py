@@ -189,7 +189,7 @@ def make_sets(nsets, rank, wl, bf16=True):
 def step(canopy, s, T, solve="fwdsub"):
     canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"], solve=solve,
                   out=s["o"])
-    canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"])
+    canopy.commit(s["acc"], s["S0"], s["k"], s["parent"], s["ws"], out=s["S_new"])
 
 
 def capture_graph(canopy, sets, T, solve, n, kind):
@@ -209,8 +209,9 @@ def capture_graph(canopy, sets, T, solve, n, kind):
                               out=s["o"], inputs_ready=True, state_ready=True)
             if kind in ("step", "commit"):
                 # the kernel before each commit (its verify, or a commit of
-                # another set) writes neither S0 nor the accepted nodes
-                canopy.commit(s["acc"], s["S0"], s["k"], s["ws"], T, out=s["S_new"], state_ready=True)
+                # another set) writes none of S0, the accepted nodes, k and
+                # parent
+                canopy.commit(s["acc"], s["S0"], s["k"], s["parent"], s["ws"], out=s["S_new"], state_ready=True)
     torch.cuda.synchronize()
     return g
 
@@ -342,7 +343,7 @@ def run_e2e(canopy, sets, T, args, world):
             dev[n].copy_(h[n], non_blocking=True)
         canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
                       solve=args.solve, out=o)
-        canopy.commit(dev["acc"], dev["S0"], dev["k"], ws, T, out=S_new)
+        canopy.commit(dev["acc"], dev["S0"], dev["k"], dev["parent"], ws, out=S_new)
         o_h.copy_(o, non_blocking=True)
         S_h.copy_(S_new, non_blocking=True)
 

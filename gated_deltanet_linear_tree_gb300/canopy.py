@@ -32,7 +32,7 @@ SIGNATURES = {
     "canopy_workspace_init": (_I, [_P, _S, _P]),
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, ctypes.c_uint, _P]),
-    "canopy_commit": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
+    "canopy_commit": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "canopy_serial_replay_static": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
@@ -144,18 +144,23 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
     return out
 
 
-def commit(accepted, S0, k, ws, T: int, out=None, state_ready: bool = False):
-    """S_new [B, H, dv, dk] for the accepted node of every stream.  state_ready:
-    S0 and accepted are not written by the kernel launched just before this
-    call on the current stream (CANOPY_COMMIT_STATE_READY)."""
-    B, H, dv, dk = S0.shape
-    _need(accepted, "accepted", torch.int32, (B,))
+def commit(accepted, S0, k, parent, ws, out=None, state_ready: bool = False):
+    """S_new [B, H, dv, dk] for the accepted node of every stream, from the
+    preceding verify call's k, parent and workspace.  state_ready: S0,
+    accepted, k and parent are not written by the kernel launched just
+    before this call on the current stream (CANOPY_COMMIT_STATE_READY)."""
     _need(S0, "S0", torch.float32)
+    _need(parent, "parent", torch.int32)
+    B, H, dv, dk = S0.shape
+    if parent.dim() != 2 or parent.shape[0] != B:
+        raise CanopyError(f"parent must have shape ({B}, T), got {tuple(parent.shape)}")
+    T = parent.shape[1]
+    _need(accepted, "accepted", torch.int32, (B,))
     _need(k, "k", None, (B, T, H, dk))
     if out is None:
         out = torch.empty_like(S0)
     _need(out, "S_new", torch.float32, S0.shape)
-    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _dt(k), T, B, H, dk, dv,
+    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _ptr(parent), _dt(k), T, B, H, dk, dv,
                               _ptr(ws), COMMIT_STATE_READY if state_ready else 0, _stream())
     _check(st, "canopy_commit")
     return out

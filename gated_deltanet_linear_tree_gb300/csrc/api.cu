@@ -14,7 +14,8 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
                                cudaStream_t st);
-cudaError_t launch_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k, int in_bf16,
+cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
+                          const void* k, int in_bf16,
                           int T, int B, int H, int d, const Ws& ws, int state_ready, cudaStream_t st);
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
                           const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int d,
@@ -87,16 +88,17 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
 }
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,
-                            canopy_dtype in_dtype, int T, int B, int H, int dk, int dv, const void* workspace,
-                            unsigned flags, void* stream) {
-    if (!aligned16(accepted) || !aligned16(S0) || !aligned16(S_new) || !aligned16(k) || !aligned16(workspace))
+                            const int32_t* parent, canopy_dtype in_dtype, int T, int B, int H, int dk, int dv,
+                            const void* workspace, unsigned flags, void* stream) {
+    if (!aligned16(accepted) || !aligned16(S0) || !aligned16(S_new) || !aligned16(k) || !aligned16(parent) ||
+        !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if (in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) return CANOPY_ERR_ARG;
     if (flags & ~CANOPY_COMMIT_STATE_READY) return CANOPY_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
     Ws ws = ws_bind(const_cast<void*>(workspace), B, T, H, dv);
-    return cuda_status(launch_commit(accepted, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, H, dk, ws,
+    return cuda_status(launch_commit(accepted, parent, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, H, dk, ws,
                                      (flags & CANOPY_COMMIT_STATE_READY) != 0, static_cast<cudaStream_t>(stream)));
 }
 

@@ -3,11 +3,11 @@
 // canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed form"
 // (last line) and "What the commit kernel stores", in the (dv, dk)
 // orientation:  S_new = gamma_a S0 + sum_{j in path(a)} exp(l_a - l_j) u_j k_j^T,
-// all in fp32, from the U, l and ancestor mask the verify call left in the
-// workspace.  Memory bound: every element of S0 is read once (one bulk copy
-// per tile) and S_new written once with 16-byte coalesced stores; the path's
-// k rows and weighted u entries are staged in shared memory 32 nodes at a
-// time.
+// all in fp32, from the U and l the verify call left in the workspace and
+// that call's k and parent.  Memory bound: every element of S0 is read once
+// (one bulk copy per tile) and S_new written once with 16-byte coalesced
+// stores; the path's k rows and weighted u entries are staged in shared
+// memory 32 nodes at a time.
 #include "common.cuh"
 
 namespace canopy {
@@ -26,15 +26,16 @@ __device__ inline float4 k4(const __nv_bfloat16* p) {
 }
 
 // One CTA rebuilds ROWS value rows of one (stream, head) state.  Its S0 tile
-// is fetched by one bulk copy into shared memory at the start, so the short
-// chain of dependent loads that finds the path (accepted node -> ancestor
-// bitmask -> k rows, u entries and gates of the path) does not queue behind
-// it.  Warp 0 turns the bitmask into a node list (one 32-bit word per lane,
-// offsets by a warp prefix sum); the path's k rows and exp(l_a - l_j) u_j
-// entries are staged in shared memory and accumulated into the tile, which
-// is stored in place of (or beside) S0.
+// is fetched by one bulk copy into shared memory at the start.  path(a) is
+// walked up the stream's parent array (an input, so with state_ready it is
+// read, and the path's k rows staged, while the preceding verify finishes);
+// after that kernel has completed, one round of loads brings l and the u
+// entries of the path, weighted by exp(l_a - l_j), and the path's rank-one
+// terms are accumulated into the tile, which is stored in place of (or
+// beside) S0.
 template <typename InT, int DK, int DV>
-__global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted, const float* S0,
+__global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted,
+                                                    const int32_t* __restrict__ parent, const float* S0,
                                                     float* S_new, const InT* __restrict__ k, int T, int H, Ws ws,
                                                     int state_ready) {
     constexpr int C4 = DK / 4;             // float4 per state row (threads per row)
@@ -45,21 +46,20 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     __shared__ __align__(128) float sS[ROWS * DK];
     __shared__ __align__(16) InT sK[CH][DK];
     __shared__ __align__(16) float sWU[CH][ROWS];
-    __shared__ int sPath[kMaxT];
-    __shared__ uint32_t sMaskB[128];   // the stream's ancestor masks when T * W <= 128
-    __shared__ float sLB[64];          // the head's log gates when T <= 64
+    __shared__ int sPar[kMaxT];        // the stream's parents
+    __shared__ int sPath[kMaxT];       // path(a), a first
     __shared__ __align__(8) uint64_t sBar;
-    __shared__ int sN;
-    __shared__ float sLa;
+    __shared__ int sN, sBad;
     const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
     const int v0 = rt * ROWS;
     // this thread: rows r0 .. r0 + F4 - 1 of the tile, float4 column c4
     const int c4 = t % C4, r0 = (t / C4) * F4;
     const size_t sbase = ((size_t(b) * H + h) * DV + v0) * DK;
 
-    // Programmatic dependent launch: with state_ready, the S0 tile and the
-    // accepted node are read while the preceding kernel finishes; the
-    // workspace and S_new only after it has completed.
+    // Programmatic dependent launch: with state_ready, the S0 tile, the
+    // accepted node, the parents and the path's k rows are read while the
+    // preceding kernel finishes; the workspace and S_new only after it has
+    // completed.
     if (!state_ready) pdl_wait();
     pdl_trigger();
     if (t == 0) {
@@ -68,67 +68,61 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
         mbar_expect_tx(&sBar, TILE);
         bulk_load(sS, S0 + sbase, TILE, &sBar);
     }
-    const int a_in = (t < 32) ? accepted[b] : -1;
-    if (state_ready) pdl_wait();
-    // T <= 64: the stream's masks and the head's gates are read together with
-    // the accepted node, so the path costs one dependent round trip less
-    const bool spec = T <= 64;
     if (t < 32) {
-        if (spec) {
-            for (int w = t; w < T * ws.W; w += 32) sMaskB[w] = ws.mask[size_t(b) * T * ws.W + w];
-            for (int j = t; j < T; j += 32) sLB[j] = ws.l[(size_t(b) * T + j) * H + h];
-        }
-        int a = a_in;
-        if (a < -1 || a >= T) {
-            if (t == 0 && h == 0 && rt == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
-            a = -1;
-        }
-        int n = 0;
-        float la = 0.f;
+        for (int j = t; j < T; j += 32) sPar[j] = parent[size_t(b) * T + j];
+        int a = accepted[b];
         __syncwarp();
-        if (a >= 0) {
-            uint32_t word = 0u;
-            if (t < ws.W) word = spec ? sMaskB[a * ws.W + t] : ws.mask[(size_t(b) * T + a) * ws.W + t];
-            const int c = __popc(word);
-            int off = c;
-#pragma unroll
-            for (int sh = 1; sh < 32; sh <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, off, sh);
-                if (t >= sh) off += y;
-            }
-            n = __shfl_sync(0xffffffffu, off, 31) + 1;
-            off -= c;
-            for (uint32_t bits = word; bits; bits &= bits - 1) sPath[off++] = 32 * t + __ffs(bits) - 1;
-            la = spec ? sLB[a] : ws.l[(size_t(b) * T + a) * H + h];
-            if (t == 0) sPath[n - 1] = a;
-        }
         if (t == 0) {
+            const int bad = (a < -1 || a >= T) ? 1 : 0;
+            if (bad) a = -1;
+            // path(a) from a up to the root, parents sanitised as the verify
+            // sanitises them (node 0 is the root; a parent outside [0, j)
+            // reads as 0), so the walk ends within a + 1 steps
+            int n = 0;
+            for (int j = a; j >= 0;) {
+                sPath[n++] = j;
+                const int pj = sPar[j];
+                j = (j == 0) ? -1 : ((pj >= 0 && pj < j) ? pj : 0);
+            }
             sN = n;
-            sLa = la;
+            sBad = bad;
         }
     }
     __syncthreads();
     const int n = sN;
-    const float la = sLa;
-    const float gamma_a = (n > 0) ? expf(la) : 1.f;
+    // k rows of the first chunk of the path (an input)
+    {
+        const int cn = min(CH, n);
+        for (int e = t; e < cn * (DK / KV); e += NT) {
+            const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[r];
+            *reinterpret_cast<uint4*>(&sK[r][c]) =
+                *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * H + h) * DK + c);
+        }
+    }
+    if (state_ready) pdl_wait();
+    if (sBad && t == 0 && h == 0 && rt == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
+    const float la = (n > 0) ? ws.l[(size_t(b) * T + sPath[0]) * H + h] : 0.f;
 
     float4 acc[F4];
     bool have_tile = false;
     for (int c0 = 0; c0 == 0 || c0 < n; c0 += CH) {
         const int cn = max(0, min(CH, n - c0));
-        if (c0) __syncthreads();
-        for (int e = t; e < cn * (DK / KV); e += NT) {
-            const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[c0 + r];
-            *reinterpret_cast<uint4*>(&sK[r][c]) =
-                *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * H + h) * DK + c);
+        if (c0) {
+            __syncthreads();
+            for (int e = t; e < cn * (DK / KV); e += NT) {
+                const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[c0 + r];
+                *reinterpret_cast<uint4*>(&sK[r][c]) =
+                    *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * H + h) * DK + c);
+            }
         }
         for (int e = t; e < cn * ROWS; e += NT) {
             const int r = e / ROWS, c = e % ROWS, j = sPath[c0 + r];
             const size_t nh = (size_t(b) * T + j) * H + h;
-            sWU[r][c] = expf(la - (spec ? sLB[j] : ws.l[nh])) * ws.U[nh * DV + v0 + c];
+            sWU[r][c] = expf(la - ws.l[nh]) * ws.U[nh * DV + v0 + c];
         }
         if (!have_tile) {
             if (!mbar_wait(&sBar, 0) && t == 0) raise_err(ws.err, CANOPY_DEVERR_TIMEOUT);
+            const float gamma_a = (n > 0) ? expf(la) : 1.f;
 #pragma unroll
             for (int u = 0; u < F4; ++u) {
                 const float4 s = *reinterpret_cast<const float4*>(&sS[((r0 + u) * C4 + c4) * 4]);
@@ -163,21 +157,24 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
 }  // namespace cm
 
 template <typename InT, int D>
-static cudaError_t launch_commit_typed(const int32_t* accepted, const float* S0, float* S_new, const void* k,
-                                       int T, int B, int H, const Ws& ws, int state_ready, cudaStream_t st) {
+static cudaError_t launch_commit_typed(const int32_t* accepted, const int32_t* parent, const float* S0,
+                                       float* S_new, const void* k, int T, int B, int H, const Ws& ws,
+                                       int state_ready, cudaStream_t st) {
     dim3 grid(D / cm::ROWS, H, B);
-    return launch_pdl(cm::commit_kernel<InT, D, D>, grid, dim3(cm::NT), 0, st, accepted, S0, S_new,
+    return launch_pdl(cm::commit_kernel<InT, D, D>, grid, dim3(cm::NT), 0, st, accepted, parent, S0, S_new,
                       static_cast<const InT*>(k), T, H, ws, state_ready);
 }
 
-cudaError_t launch_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k, int in_bf16,
-                          int T, int B, int H, int d, const Ws& ws, int state_ready, cudaStream_t st) {
+cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
+                          const void* k, int in_bf16, int T, int B, int H, int d, const Ws& ws, int state_ready,
+                          cudaStream_t st) {
+    using bf = __nv_bfloat16;
     if (d == 128) {
-        if (in_bf16) return launch_commit_typed<__nv_bfloat16, 128>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
-        return launch_commit_typed<float, 128>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
+        if (in_bf16) return launch_commit_typed<bf, 128>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
+        return launch_commit_typed<float, 128>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
     }
-    if (in_bf16) return launch_commit_typed<__nv_bfloat16, 32>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
-    return launch_commit_typed<float, 32>(accepted, S0, S_new, k, T, B, H, ws, state_ready, st);
+    if (in_bf16) return launch_commit_typed<bf, 32>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
+    return launch_commit_typed<float, 32>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
 }
 
 }  // namespace canopy

@@ -70,8 +70,8 @@ typedef enum {
                                             before this call */
 
 /* Flags of canopy_commit. */
-#define CANOPY_COMMIT_STATE_READY 0x1u   /* S0 and accepted are not written by the kernel
-                                            launched just before this call */
+#define CANOPY_COMMIT_STATE_READY 0x1u   /* S0, accepted, k and parent are not written by
+                                            the kernel launched just before this call */
 
 /* Bits of the device error word. */
 #define CANOPY_DEVERR_TREE     0x1  /* parent[b][0] != -1 or parent[b][i] not in [0,i) */
@@ -130,22 +130,23 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
 /* Commit (canopy page, "The tree closed form", last line, and "What the
  * commit kernel stores"): for every stream b with accepted node a = accepted[b],
  *   S_new = gamma_a S0 + sum_{j in path(a)} exp(l_a - l_j) u_j k_j^T      (fp32)
- * using U, l and the ancestor mask that the preceding verify call left in
- * the workspace (same parent, g and T).  a = -1 means nothing accepted:
- * S_new = S0.  S_new may alias S0 (the update is elementwise in S0).
+ * using U and l that the preceding verify call left in the workspace, and
+ * that call's k and parent (path(a) is walked up the parent array, parents
+ * sanitised as the verify does).  a = -1 means nothing accepted: S_new = S0.
+ * S_new may alias S0 (the update is elementwise in S0).
  * flags: 0 or CANOPY_COMMIT_STATE_READY.  The kernel is launched with
  * programmatic dependent launch; with flags = 0 it touches no global memory
  * until the kernel launched just before it on `stream` has completed.  With
- * CANOPY_COMMIT_STATE_READY the caller asserts that S0 and accepted are not
- * written by that kernel (a verify call only reads S0): the commit then
- * requests its S0 tiles and reads accepted while that kernel finishes; the
- * workspace and S_new are touched only after it has completed.  Other bits
- * return CANOPY_ERR_ARG.
+ * CANOPY_COMMIT_STATE_READY the caller asserts that S0, accepted, k and
+ * parent are not written by that kernel (a verify call only reads them):
+ * the commit then requests its S0 tiles, walks the accepted path and stages
+ * its k rows while that kernel finishes; the workspace and S_new are touched
+ * only after it has completed.  Other bits return CANOPY_ERR_ARG.
  *   accepted device int32 [B]; S0, S_new device fp32 [B][H][dv][dk];
- *   k device [B][T][H][dk] in in_dtype (the verify call's k). */
+ *   k device [B][T][H][dk] in in_dtype; parent device int32 [B][T]. */
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new,
-                            const void* k, canopy_dtype in_dtype, int T, int B, int H,
-                            int dk, int dv, const void* workspace, unsigned flags, void* stream);
+                            const void* k, const int32_t* parent, canopy_dtype in_dtype, int T, int B,
+                            int H, int dk, int dv, const void* workspace, unsigned flags, void* stream);
 
 /* Bytes of the per-node snapshot buffer of the serial replay:
  * fp32 [B][T][H][dv][dk]. */

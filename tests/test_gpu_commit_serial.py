@@ -34,7 +34,7 @@ def test_commit_matches_replay_state(lib, T, fam, bf16):
     for trial in range(3):
         acc = np.array([rng.choice(trees.leaves(inp["parent"][b])) if trial < 2 else rng.integers(0, T)
                         for b in range(B)], dtype=np.int32)
-        S_new = lib.commit(torch.from_numpy(acc).cuda(), dev["S0"], dev["k"], ws, T)
+        S_new = lib.commit(torch.from_numpy(acc).cuda(), dev["S0"], dev["k"], dev["parent"], ws)
         assert lib.read_device_error(ws) == 0
         ref = np.stack([S_ref[b, acc[b]] for b in range(B)])
         assert rel_err(S_new.cpu().numpy(), ref) <= (TOL_BF16 if bf16 else TOL_F32)
@@ -45,13 +45,13 @@ def test_commit_nothing_accepted_and_in_place(lib):
     dev = to_device(inp, True)
     o, ws, err = run_verify(lib, dev)
     acc = torch.full((3,), -1, dtype=torch.int32, device="cuda")
-    S_new = lib.commit(acc, dev["S0"], dev["k"], ws, 32)
+    S_new = lib.commit(acc, dev["S0"], dev["k"], dev["parent"], ws)
     assert torch.equal(S_new, dev["S0"])
     # in place: S_new aliases S0
     _, S_ref = oracle_outputs(inp, keep_states=True)
     acc = torch.tensor([5, 9, 31], dtype=torch.int32, device="cuda")
     S = dev["S0"].clone()
-    lib.commit(acc, S, dev["k"], ws, 32, out=S)
+    lib.commit(acc, S, dev["k"], dev["parent"], ws, out=S)
     ref = np.stack([S_ref[b, a] for b, a in enumerate([5, 9, 31])])
     assert rel_err(S.cpu().numpy(), ref) <= TOL_BF16
 
@@ -101,11 +101,33 @@ def test_device_error_flags(lib, T):
     _, ws, err = run_verify(lib, dev)
     assert err == 0
     acc = torch.tensor([T, -5], dtype=torch.int32, device="cuda")
-    lib.commit(acc, dev["S0"], dev["k"], ws, T)
+    lib.commit(acc, dev["S0"], dev["k"], dev["parent"], ws)
     assert lib.read_device_error(ws) & 0x4
     s = lib.workspace(2, T, 4, 128)
     lib.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], bad, s)
     assert lib.read_device_error(s) & 0x1
+
+
+@pytest.mark.parametrize("T", [16, 64, 200])
+def test_commit_on_sanitised_tree(lib, T):
+    """A tree with bad parents is reported by the verify and read as the
+    sanitised tree (a parent outside [0, i) becomes 0); the commit walks the
+    same sanitised path, so its state is the oracle's for that tree."""
+    inp = _inputs(T, "chain" if T == 200 else "random", B=2)
+    bad = inp["parent"].copy()
+    bad[0, T - 1] = T + 7                                  # out of range
+    bad[1, T // 2] = T // 2                                # parent[i] = i
+    fixed = bad.copy()
+    fixed[0, T - 1] = 0
+    fixed[1, T // 2] = 0
+    dev = to_device(dict(inp, parent=bad), True)
+    _, ws, err = run_verify(lib, dev)
+    assert err & 0x1
+    _, S_ref = oracle_outputs(dict(inp, parent=fixed), keep_states=True)
+    acc = np.array([T - 1, T - 1], dtype=np.int32)
+    S_new = lib.commit(torch.from_numpy(acc).cuda(), dev["S0"], dev["k"], dev["parent"], ws)
+    ref = np.stack([S_ref[b, acc[b]] for b in range(2)])
+    assert rel_err(S_new.cpu().numpy(), ref) <= TOL_BF16
 
 
 def _round_trip(lib, B, T, H, rounds, bf16, check_streams):
@@ -126,7 +148,7 @@ def _round_trip(lib, B, T, H, rounds, bf16, check_streams):
         o = lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], S_dev, dev["parent"], ws)
         rng = synth.stream_seed(4, r, 999)
         acc = np.array([rng.choice(trees.leaves(inp["parent"][b])) for b in range(B)], dtype=np.int32)
-        lib.commit(torch.from_numpy(acc).cuda(), S_dev, dev["k"], ws, T, out=S_dev)
+        lib.commit(torch.from_numpy(acc).cuda(), S_dev, dev["k"], dev["parent"], ws, out=S_dev)
         assert lib.read_device_error(ws) == 0
         on = o.cpu().numpy()
         for b in check_streams(r):
@@ -177,7 +199,7 @@ def test_overlapped_verify_commit_steps(lib):
             for dev in sets:
                 o = lib.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"],
                                dev["ws"], inputs_ready=overlap, state_ready=overlap)
-                Sn = lib.commit(dev["acc"], dev["S0"], dev["k"], dev["ws"], dev["q"].shape[1], state_ready=overlap)
+                Sn = lib.commit(dev["acc"], dev["S0"], dev["k"], dev["parent"], dev["ws"], state_ready=overlap)
                 outs.append((o, Sn))
         torch.cuda.synchronize()
         return outs

@@ -83,7 +83,7 @@ def test_neumann_variant(lib, fam, T):
     assert rel_err(on.cpu().numpy(), o_ref) <= TOL_BF16
     B = dev["q"].shape[0]
     acc = torch.full((B,), T - 1, dtype=torch.int32, device="cuda")
-    Sn = lib.commit(acc, dev["S0"], dev["k"], ws_n, T)
+    Sn = lib.commit(acc, dev["S0"], dev["k"], dev["parent"], ws_n)
     assert lib.read_device_error(ws_n) == 0
     assert rel_err(Sn.cpu().numpy(), S_ref[:, T - 1]) <= TOL_BF16
 

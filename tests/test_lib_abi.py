@@ -74,9 +74,12 @@ def test_host_argument_errors(lib):
     assert _verify(lib, good, solve=5) == 1
     assert _verify(lib, good, flags=4) == 1                         # unknown flag
     assert _verify(lib, good, flags=8) == 1
-    assert lib.canopy_commit(None, good[1], good[2], good[3], 1, 64, 1, 1, 128, 128, good[4], 0, None) == 1
-    assert lib.canopy_commit(good[0], good[1], good[2], good[3], 1, 300, 1, 1, 128, 128, good[4], 0, None) == 3
-    assert lib.canopy_commit(good[0], good[1], good[2], good[3], 1, 64, 1, 1, 128, 128, good[4], 4, None) == 1
+    assert lib.canopy_commit(None, good[1], good[2], good[3], good[5], 1, 64, 1, 1, 128, 128, good[4], 0, None) == 1
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], None, 1, 64, 1, 1, 128, 128, good[4], 0, None) == 1
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], 1, 300, 1, 1, 128, 128, good[4], 0,
+                             None) == 3
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], 1, 64, 1, 1, 128, 128, good[4], 4,
+                             None) == 1
     assert lib.canopy_tree_prep(good[0], good[1], 0, 1, 1, good[2], None) == 3
     err = ctypes.c_int32(0)
     assert lib.canopy_read_device_error(None, ctypes.byref(err), None) == 1
