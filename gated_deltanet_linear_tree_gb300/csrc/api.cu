@@ -4,7 +4,7 @@
 
 namespace canopy {
 cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
-                             cudaStream_t st);
+                             int with_order, cudaStream_t st);
 cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                   const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
                                   const Ws& ws, cudaStream_t st);
@@ -13,7 +13,9 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
                                  const Ws& ws, int inputs_ready, int state_ready, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
-                               cudaStream_t st);
+                               int gram_done, cudaStream_t st);
+cudaError_t launch_gram_tc(const void* q, const void* k, const void* v, const float* beta, const float* S0, int T,
+                           int B, int H, const Ws& ws, cudaStream_t st);
 cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
                           const void* k, int in_bf16,
                           int T, int B, int H, int d, const Ws& ws, int state_ready, cudaStream_t st);
@@ -56,7 +58,7 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int
     if (!aligned16(parent) || !aligned16(g) || !aligned16(workspace)) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, H)) return CANOPY_ERR_UNSUPPORTED;
     Ws ws = ws_bind(workspace, B, T, H, 32);  // tree-prep regions do not depend on dv
-    return cuda_status(launch_tree_prep(parent, g, T, B, H, ws, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_tree_prep(parent, g, T, B, H, ws, 1, static_cast<cudaStream_t>(stream)));
 }
 
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
@@ -82,9 +84,15 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws,
                                                 (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
                                                 (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
-    cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, st);
+    cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, 0, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
-    return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, st));
+    // bf16 inputs beyond one 64-node block: the Gram products on tcgen05
+    const bool gram_tc = in_bf16 && dk == 128 && T > 64;
+    if (gram_tc) {
+        e = launch_gram_tc(q, k, v, beta, S0, T, B, H, ws, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, gram_tc, st));
 }
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,

@@ -12,7 +12,8 @@ namespace canopy {
 namespace prep {
 
 __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restrict__ parent,
-                                                        const float* __restrict__ g, int T, int H, Ws ws) {
+                                                        const float* __restrict__ g, int T, int H, Ws ws,
+                                                        int with_order) {
     __shared__ int sPtr[kMaxT];
     __shared__ int sLen[kMaxT];
     __shared__ int sPar[kMaxT];
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     // DFS pre-order (children in index order): subtree sizes bottom-up, then
     // each child takes the next free slot after its parent.
     __syncthreads();
-    if (!lead) return;
+    if (!lead || !with_order) return;
     if (i == 0) {
         for (int n = 0; n < T; ++n) sSize[n] = 1;
         for (int n = T - 1; n >= 1; --n) sSize[sPar[n]] += sSize[n];
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
 }  // namespace prep
 
 cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
-                             cudaStream_t st) {
-    prep::tree_prep_kernel<<<dim3(B, (H + 15) / 16), 256, 0, st>>>(parent, g, T, H, ws);
+                             int with_order, cudaStream_t st) {
+    prep::tree_prep_kernel<<<dim3(B, (H + 15) / 16), 256, 0, st>>>(parent, g, T, H, ws, with_order);
     return cudaGetLastError();
 }
 

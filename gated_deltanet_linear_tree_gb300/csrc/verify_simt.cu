@@ -148,12 +148,13 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
 }
 
 constexpr int SOLVE_NT = 512;  // threads of the solve kernel
-constexpr int CHN = 16;        // nodes of one level staged at a time
+constexpr int CHN = 16;        // nodes staged at a time (in level order)
 constexpr int PSTRIDE = 256;   // staged path entries per node (kMaxT)
 
 // Shared-memory bytes of solve_level_kernel for T nodes and DV value columns.
 __host__ __device__ constexpr size_t solve_smem(int T, int DV) {
-    return size_t(T) * DV * 4 + size_t(3 * kMaxT + 1) * 4 + size_t(CHN) * 8 + size_t(CHN) * PSTRIDE * 12;
+    return size_t(T) * DV * 4 + size_t(3 * kMaxT + 1) * 4 + size_t(CHN) * 8 + size_t(CHN) * PSTRIDE * 12 + 16 +
+           size_t(CHN) * DV * 8;
 }
 
 // Forward substitution level by level: all nodes of one depth depend only on
@@ -162,8 +163,9 @@ __host__ __device__ constexpr size_t solve_smem(int T, int DV) {
 //   o_i = gamma_i X_Q,i + sum_{j in path(i)} C_ij u_j.
 // One CTA per (stream, head): SOLVE_NT / DV groups of DV threads (one per
 // value column); U of every solved node stays in shared memory.  Per chunk
-// of a level, one warp per node turns its ancestor bitmask into a list and
-// stages (j, G_ij, C_ij); then each group takes nodes of the chunk.
+// of CHN nodes in level order, one warp per node turns its ancestor bitmask
+// into a list and stages (j, G_ij, C_ij); then the chunk's nodes are solved
+// level by level, each group taking nodes of the level.
 template <typename OutT, int DV>
 __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict__ o, int T, int H, Ws ws) {
     constexpr int NG = SOLVE_NT / DV;
@@ -177,6 +179,9 @@ __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict_
     int* sJ = sLen + CHN;                                   // [CHN][PSTRIDE]
     float* sG = reinterpret_cast<float*>(sJ + CHN * PSTRIDE);   // [CHN][PSTRIDE]
     float* sC = sG + CHN * PSTRIDE;                         // [CHN][PSTRIDE]; entry PSTRIDE-1 unused
+    // [CHN][DV] R rows of the chunk (16-byte aligned for vector stores)
+    float* sRr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sC + CHN * PSTRIDE) + 15) & ~uintptr_t(15));
+    float* sXq = sRr + CHN * DV;                            // [CHN][DV] gamma X_Q rows of the chunk
     __shared__ float sCii[CHN];
     __shared__ int sMaxD;
     __shared__ float2 sPart[SOLVE_NT];  // per-thread partial sums when groups share a node
@@ -212,74 +217,103 @@ __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict_
     const int c = t % DV, grp = t / DV;
     const float* gsb = ws.gs + bh * T * T;
     const float* csb = ws.cs + bh * T * T;
-    for (int lv = 0; lv <= maxd; ++lv) {
-        for (int c0 = sOff[lv]; c0 < sOff[lv + 1]; c0 += CHN) {
-            const int cn = min(CHN, sOff[lv + 1] - c0);
-            // stage the chunk's ancestor lists and coefficients (one warp per node)
-            if (warp < cn) {
-                const int e = warp, i = sOrder[c0 + e];
-                const uint32_t word = (lane < ws.W) ? ws.mask[(size_t(b) * T + i) * ws.W + lane] : 0u;
-                const int cntw = __popc(word);
-                int off = cntw;
+    // Chunks of CHN nodes in level order, across level boundaries: a chunk's
+    // ancestor lists and coefficients are staged in one round (they depend
+    // on nothing solved yet), then its nodes are solved level by level.
+    int lv = 0;
+    for (int c0 = 0; c0 < T; c0 += CHN) {
+        const int cn = min(CHN, T - c0);
+        // stage the chunk's ancestor lists and coefficients (one warp per node)
+        if (warp < cn) {
+            const int e = warp, i = sOrder[c0 + e];
+            const uint32_t word = (lane < ws.W) ? ws.mask[(size_t(b) * T + i) * ws.W + lane] : 0u;
+            const int cntw = __popc(word);
+            int off = cntw;
 #pragma unroll
-                for (int sh = 1; sh < 32; sh <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, off, sh);
-                    if (lane >= sh) off += y;
-                }
-                const int n = __shfl_sync(0xffffffffu, off, 31);
-                off -= cntw;
-                int* jrow = sJ + e * PSTRIDE;
-                for (uint32_t bits = word; bits; bits &= bits - 1) jrow[off++] = 32 * lane + __ffs(bits) - 1;
-                __syncwarp();
-                const float* grow = gsb + size_t(i) * T;
-                const float* crow = csb + size_t(i) * T;
-                // all of a lane's loads in flight at once (paths up to 256 long)
-                for (int p0 = lane; p0 < n; p0 += 32 * 8) {
-                    int jj[8];
-                    float gv[8], cv[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) jj[u] = (p0 + 32 * u < n) ? jrow[p0 + 32 * u] : i;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        gv[u] = grow[jj[u]];
-                        cv[u] = crow[jj[u]];
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (p0 + 32 * u < n) {
-                            sG[e * PSTRIDE + p0 + 32 * u] = gv[u];
-                            sC[e * PSTRIDE + p0 + 32 * u] = cv[u];
-                        }
-                }
-                if (lane == 0) {
-                    sNode[e] = i;
-                    sLen[e] = n;
-                    sCii[e] = crow[i];
-                }
+            for (int sh = 1; sh < 32; sh <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, off, sh);
+                if (lane >= sh) off += y;
             }
-            __syncthreads();
-            // groups per node: several groups share a node when the chunk has
-            // fewer nodes than groups (deep trees: few nodes per level, long
-            // paths); their partial sums meet in shared memory
+            const int n = __shfl_sync(0xffffffffu, off, 31);
+            off -= cntw;
+            int* jrow = sJ + e * PSTRIDE;
+            for (uint32_t bits = word; bits; bits &= bits - 1) jrow[off++] = 32 * lane + __ffs(bits) - 1;
+            __syncwarp();
+            const float* grow = gsb + size_t(i) * T;
+            const float* crow = csb + size_t(i) * T;
+            // all of a lane's loads in flight at once (paths up to 256 long)
+            for (int p0 = lane; p0 < n; p0 += 32 * 8) {
+                int jj[8];
+                float gv[8], cv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) jj[u] = (p0 + 32 * u < n) ? jrow[p0 + 32 * u] : i;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    gv[u] = grow[jj[u]];
+                    cv[u] = crow[jj[u]];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (p0 + 32 * u < n) {
+                        sG[e * PSTRIDE + p0 + 32 * u] = gv[u];
+                        sC[e * PSTRIDE + p0 + 32 * u] = cv[u];
+                    }
+            }
+            if (lane == 0) {
+                sNode[e] = i;
+                sLen[e] = n;
+                sCii[e] = crow[i];
+            }
+            // the node's R and gamma X_Q rows
+            const size_t ni = (size_t(b) * T + i) * H + h;
+            for (int cc = lane * 4; cc < DV; cc += 128) {
+                *reinterpret_cast<float4*>(sRr + e * DV + cc) = *reinterpret_cast<const float4*>(ws.rr + ni * DV + cc);
+                *reinterpret_cast<float4*>(sXq + e * DV + cc) = *reinterpret_cast<const float4*>(ws.xq + ni * DV + cc);
+            }
+        }
+        __syncthreads();
+        // the chunk's levels in order: positions [s0, s1) of level lv
+        for (int s0 = 0; s0 < cn;) {
+            while (sOff[lv + 1] <= c0 + s0) ++lv;
+            const int s1 = min(cn, sOff[lv + 1] - c0);
+            const int sn = s1 - s0;
+            // groups per node: several groups share a node when the level
+            // segment has fewer nodes than groups (deep trees: few nodes per
+            // level, long paths); their partial sums meet in shared memory
             int gpn = 1;
-            while (gpn * 2 * cn <= NG) gpn *= 2;
+            while (gpn * 2 * sn <= NG) gpn *= 2;
             if (gpn > 1) {
-                const int e = grp / gpn, sub = grp % gpn;
+                const int e = s0 + grp / gpn, sub = grp % gpn;
                 float acc = 0.f, out = 0.f;
-                if (e < cn) {
+                if (e < s1) {
                     const int n = sLen[e];
                     const int* jrow = sJ + e * PSTRIDE;
                     const float* gr = sG + e * PSTRIDE;
                     const float* cr = sC + e * PSTRIDE;
-                    for (int p = sub; p < n; p += gpn) {
-                        const float u0 = sU[jrow[p] * DV + c];
-                        acc -= gr[p] * u0;
-                        out += cr[p] * u0;
+                    float a4[4] = {0.f, 0.f, 0.f, 0.f}, o4[4] = {0.f, 0.f, 0.f, 0.f};
+                    int p = sub;
+                    for (; p + 3 * gpn < n; p += 4 * gpn) {
+                        int jq[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) jq[q] = jrow[p + q * gpn];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float u0 = sU[jq[q] * DV + c];
+                            a4[q] -= gr[p + q * gpn] * u0;
+                            o4[q] += cr[p + q * gpn] * u0;
+                        }
                     }
+                    for (; p < n; p += gpn) {
+                        const float u0 = sU[jrow[p] * DV + c];
+                        a4[0] -= gr[p] * u0;
+                        o4[0] += cr[p] * u0;
+                    }
+                    acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+                    out = (o4[0] + o4[1]) + (o4[2] + o4[3]);
                 }
                 sPart[t] = make_float2(acc, out);
                 __syncthreads();
-                if (e < cn && sub == 0) {
+                if (e < s1 && sub == 0) {
                     for (int q = 1; q < gpn; ++q) {
                         const float2 pq = sPart[t + q * DV];
                         acc += pq.x;
@@ -287,20 +321,20 @@ __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict_
                     }
                     const int i = sNode[e];
                     const size_t ni = (size_t(b) * T + i) * H + h;
-                    acc += ws.rr[ni * DV + c];
-                    out += ws.xq[ni * DV + c] + sCii[e] * acc;
+                    acc += sRr[e * DV + c];
+                    out += sXq[e * DV + c] + sCii[e] * acc;
                     sU[i * DV + c] = acc;
                     ws.U[ni * DV + c] = acc;
                     store_out(o + ni * DV + c, out);
                 }
             } else {
-                for (int e = grp; e < cn; e += NG) {
+                for (int e = s0 + grp; e < s1; e += NG) {
                     const int i = sNode[e], n = sLen[e];
                     const size_t ni = (size_t(b) * T + i) * H + h;
                     const int* jrow = sJ + e * PSTRIDE;
                     const float* gr = sG + e * PSTRIDE;
                     const float* cr = sC + e * PSTRIDE;
-                    float acc = ws.rr[ni * DV + c], out = ws.xq[ni * DV + c];
+                    float acc = sRr[e * DV + c], out = sXq[e * DV + c];
                     float acc2 = 0.f, out2 = 0.f;
                     int p = 0;
                     for (; p + 1 < n; p += 2) {
@@ -323,6 +357,7 @@ __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict_
                 }
             }
             __syncthreads();
+            s0 = s1;
         }
     }
 }
@@ -332,12 +367,15 @@ __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict_
 template <typename InT, int DK, int DV>
 static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v, const float* beta,
                                      const float* S0, int T, int B, int H, void* o, int o_bf16, const Ws& ws,
-                                     cudaStream_t st) {
-    dim3 g1((T + simt::ROWS - 1) / simt::ROWS, H, B);
-    simt::gram_kernel<InT, DK, DV><<<g1, 256, 0, st>>>(static_cast<const InT*>(q), static_cast<const InT*>(k),
-                                                      static_cast<const InT*>(v), beta, S0, T, H, ws);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+                                     int gram_done, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
+    if (!gram_done) {
+        dim3 g1((T + simt::ROWS - 1) / simt::ROWS, H, B);
+        simt::gram_kernel<InT, DK, DV><<<g1, 256, 0, st>>>(static_cast<const InT*>(q), static_cast<const InT*>(k),
+                                                          static_cast<const InT*>(v), beta, S0, T, H, ws);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const size_t smem = simt::solve_smem(T, DV);
     const size_t smem_max = simt::solve_smem(kMaxT, DV);
     dim3 g2(H, B);
@@ -366,14 +404,14 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
 
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
-                               cudaStream_t st) {
+                               int gram_done, cudaStream_t st) {
+    using bf = __nv_bfloat16;
     if (d == 128) {
-        if (in_bf16)
-            return launch_simt_typed<__nv_bfloat16, 128, 128>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, st);
-        return launch_simt_typed<float, 128, 128>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, st);
+        if (in_bf16) return launch_simt_typed<bf, 128, 128>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
+        return launch_simt_typed<float, 128, 128>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
     }
-    if (in_bf16) return launch_simt_typed<__nv_bfloat16, 32, 32>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, st);
-    return launch_simt_typed<float, 32, 32>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, st);
+    if (in_bf16) return launch_simt_typed<bf, 32, 32>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
+    return launch_simt_typed<float, 32, 32>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
 }
 
 }  // namespace canopy
