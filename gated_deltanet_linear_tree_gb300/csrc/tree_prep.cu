@@ -4,12 +4,14 @@
 // canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed form"
 // (A(i), path(i), depth, l_i = log alpha_i + l_parent(i)) and "Design
 // decisions" (DFS pre-order keeps subtrees contiguous; a T x T bitmask).
-// One CTA of 256 threads per (stream, group of 16 heads); T <= 256.
+// One CTA of 256 threads per (stream, group of HC heads); T <= 256.
 #include "common.cuh"
 
 namespace canopy {
 
 namespace prep {
+
+constexpr int HC = 4;  // heads per CTA
 
 __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restrict__ parent,
                                                         const float* __restrict__ g, int T, int H, Ws ws,
@@ -21,11 +23,11 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     __shared__ uint64_t sM[kMaxT * 4];
     __shared__ int sSize[kMaxT];
     __shared__ int sPos[kMaxT];
-    __shared__ double sLg[kMaxT * 16];  // log gates, then cumulative sums, for 16 heads (summed in
+    __shared__ double sLg[kMaxT * HC];  // log gates, then cumulative sums, for HC heads (summed in
                                         // fp64: l_i - l_j must stay accurate over deep paths)
     __shared__ int sJp[kMaxT];         // jump pointers
     const int b = blockIdx.x, i = threadIdx.x;
-    const int hc = blockIdx.y;            // this CTA's 16 heads
+    const int hc = blockIdx.y;            // this CTA's HC heads
     const bool lead = hc == 0;            // writes the per-stream outputs
     int bad = 0;
     if (i < T) {
@@ -54,10 +56,10 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     }
 
     // cumulative log gates l_n = log g_n + l_parent(n) for every head, by
-    // pointer jumping over 16 heads at a time (ceil(log2 T) rounds)
+    // pointer jumping over HC heads at a time (ceil(log2 T) rounds)
     int badg = 0;
-    for (int h0 = 16 * hc; h0 < min(H, 16 * hc + 16); h0 += 16) {
-        const int hn = min(16, H - h0);
+    for (int h0 = HC * hc; h0 < min(H, HC * hc + HC); h0 += HC) {
+        const int hn = min(HC, H - h0);
         __syncthreads();
         for (int e = i; e < T * hn; e += blockDim.x) {
             const int n = e / hn, hh = e % hn;
@@ -66,35 +68,35 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
                 badg = CANOPY_DEVERR_GATE;
                 a = 1.f;
             }
-            sLg[n * 16 + hh] = double(logf(a));  // fp32 log, fp64 sums
+            sLg[n * HC + hh] = double(logf(a));  // fp32 log, fp64 sums
         }
         if (i < T) sJp[i] = sPar[i];
         __syncthreads();
         for (int span = 1; span < T; span *= 2) {
-            double nv[16];
+            double nv[HC];
             int np = -1;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < HC; ++u) {
                 const int e = i + u * 256;
                 nv[u] = 0.0;
                 if (e < T * hn) {
                     const int n = e / hn, hh = e % hn, pn = sJp[n];
-                    nv[u] = sLg[n * 16 + hh] + ((pn >= 0) ? sLg[pn * 16 + hh] : 0.0);
+                    nv[u] = sLg[n * HC + hh] + ((pn >= 0) ? sLg[pn * HC + hh] : 0.0);
                 }
             }
             if (i < T) np = (sJp[i] >= 0) ? sJp[sJp[i]] : -1;
             __syncthreads();
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < HC; ++u) {
                 const int e = i + u * 256;
-                if (e < T * hn) sLg[(e / hn) * 16 + e % hn] = nv[u];
+                if (e < T * hn) sLg[(e / hn) * HC + e % hn] = nv[u];
             }
             if (i < T) sJp[i] = np;
             __syncthreads();
         }
         for (int e = i; e < T * hn; e += blockDim.x) {
             const int n = e / hn, hh = e % hn;
-            ws.l[(size_t(b) * T + n) * H + h0 + hh] = float(sLg[n * 16 + hh]);
+            ws.l[(size_t(b) * T + n) * H + h0 + hh] = float(sLg[n * HC + hh]);
         }
     }
     if (badg) raise_err(ws.err, badg);
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
 
 cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
                              int with_order, cudaStream_t st) {
-    prep::tree_prep_kernel<<<dim3(B, (H + 15) / 16), 256, 0, st>>>(parent, g, T, H, ws, with_order);
+    prep::tree_prep_kernel<<<dim3(B, (H + prep::HC - 1) / prep::HC), 256, 0, st>>>(parent, g, T, H, ws, with_order);
     return cudaGetLastError();
 }
 
