@@ -9,16 +9,18 @@ from __future__ import annotations
 
 import numpy as np
 
+from .replay import value_heads
 from .tree import cumulative_log_gate, root_path, validate_parent
 
 
 def commit(parent, a: int, k, alpha, U, S0):
-    """One stream, all heads.  k [T, H, dk]; alpha [T, H]; U [T, H, dv];
-    S0 [H, dv, dk].  Returns S_a [H, dv, dk]."""
+    """One stream, all heads.  k [T, H, dk] (key heads); alpha [T, HV];
+    U [T, HV, dv]; S0 [HV, dv, dk].  Returns S_a [HV, dv, dk]; value head j
+    reads key head j // (HV / H), as in ``replay``."""
     p = validate_parent(parent)
-    l = cumulative_log_gate(p, alpha)                      # [T, H]
-    k = np.asarray(k, np.float64)
+    l = cumulative_log_gate(p, alpha)                      # [T, HV]
     U = np.asarray(U, np.float64)
+    k = value_heads(k, U.shape[1])
     S = np.exp(l[a])[:, None, None] * np.asarray(S0, np.float64)
     for j in root_path(p, a):
         w = np.exp(l[a] - l[j])                            # [H]

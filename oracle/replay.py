@@ -7,6 +7,13 @@ and tree generators" (the per-node replay).  For each node i in index order:
     o_i = S_i @ q_i
 All arithmetic in float64.  Sp @ (I - beta k k^T) is evaluated as the equal
 Sp - beta (Sp k) k^T, which avoids forming the dk x dk matrix.
+
+Heads (canopy page, "Qwen3.5-9B shapes" and "Design decisions", memory
+layout): q and k have H key heads, v, alpha, beta and S0 have HV value
+heads, HV a multiple of H, and key head h serves value heads h * HV/H ..
+(h + 1) * HV/H - 1 (grouped value attention).  q is multiplied by ``scale``
+before use (the page's "The gated delta rule": the default scale on q is
+1/sqrt(dk); 1 reproduces the unscaled rule).
 """
 
 from __future__ import annotations
@@ -16,16 +23,27 @@ import numpy as np
 from .tree import validate_parent
 
 
-def replay(parent, q, k, v, alpha, beta, S0, keep_states: bool = True):
+def value_heads(x, HV: int):
+    """[T, H, d] per key head -> [T, HV, d] per value head: value head j reads
+    key head j // (HV / H)."""
+    x = np.asarray(x, np.float64)
+    H = x.shape[1]
+    if HV % H:
+        raise ValueError(f"value heads {HV} are not a multiple of key heads {H}")
+    return np.repeat(x, HV // H, axis=1)
+
+
+def replay(parent, q, k, v, alpha, beta, S0, keep_states: bool = True, scale: float = 1.0):
     """One stream, all heads.
 
-    parent [T]; q, k [T, H, dk]; v [T, H, dv]; alpha, beta [T, H];
-    S0 [H, dv, dk].  Returns (o [T, H, dv], S [T, H, dv, dk] or None).
+    parent [T]; q, k [T, H, dk]; v [T, HV, dv]; alpha, beta [T, HV];
+    S0 [HV, dv, dk].  Returns (o [T, HV, dv], S [T, HV, dv, dk] or None).
     """
     p = validate_parent(parent)
-    q = np.asarray(q, np.float64)
-    k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
+    HV = v.shape[1]
+    q = value_heads(q, HV) * float(scale)
+    k = value_heads(k, HV)
     a = np.asarray(alpha, np.float64)
     b = np.asarray(beta, np.float64)
     S0 = np.asarray(S0, np.float64)
@@ -54,11 +72,11 @@ def replay(parent, q, k, v, alpha, beta, S0, keep_states: bool = True):
     return o, S_all
 
 
-def replay_batch(parent, q, k, v, alpha, beta, S0, keep_states: bool = False):
+def replay_batch(parent, q, k, v, alpha, beta, S0, keep_states: bool = False, scale: float = 1.0):
     """B streams (one tree each); shapes as in ``replay`` with a leading B."""
     outs, states = [], []
     for bb in range(len(parent)):
-        o, S = replay(parent[bb], q[bb], k[bb], v[bb], alpha[bb], beta[bb], S0[bb], keep_states)
+        o, S = replay(parent[bb], q[bb], k[bb], v[bb], alpha[bb], beta[bb], S0[bb], keep_states, scale)
         outs.append(o)
         states.append(S)
     return np.stack(outs), (np.stack(states) if keep_states else None)

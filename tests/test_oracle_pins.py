@@ -172,3 +172,46 @@ def test_commit_every_leaf_equals_replay_state():
         for node in range(T):
             Sa = oracle.commit(p, node, k, a, U, S0)
             assert np.abs(Sa - S[node]).max() <= 1e-10
+
+
+def test_grouped_value_heads_read_their_key_head():
+    """HV value heads on H key heads (page: "Qwen3.5-9B shapes", grouped value
+    attention): value head j is the single-head rule run with key head
+    j // (HV / H); its state and output match a run of that head alone."""
+    rng = np.random.default_rng(21)
+    T, H, HV, dk, dv = 30, 2, 6, 16, 8
+    p = trees.family("random", T, rng)
+    q, k, _, _, _, _ = _inputs(rng, T, H, dk, dv)
+    _, _, v, a, b, S0 = _inputs(rng, T, HV, dk, dv)
+    o, S = oracle.replay(p, q, k, v, a, b, S0)
+    assert o.shape == (T, HV, dv) and S.shape == (T, HV, dv, dk)
+    for j in range(HV):
+        h = j // (HV // H)
+        oj, Sj = oracle.replay(p, q[:, [h]], k[:, [h]], v[:, [j]], a[:, [j]], b[:, [j]], S0[[j]])
+        assert np.abs(o[:, j] - oj[:, 0]).max() <= 1e-13
+        assert np.abs(S[:, j] - Sj[:, 0]).max() <= 1e-13
+    # two value heads of one key head with the same values, gates and state agree
+    v2, a2, b2, S02 = v.copy(), a.copy(), b.copy(), S0.copy()
+    v2[:, 1], a2[:, 1], b2[:, 1], S02[1] = v[:, 0], a[:, 0], b[:, 0], S0[0]
+    o2, _ = oracle.replay(p, q, k, v2, a2, b2, S02)
+    assert np.array_equal(o2[:, 0], o2[:, 1])
+    # and the commit of every node reads the same key heads
+    U = np.stack([oracle.closed_form(p, q[:, j // 3], k[:, j // 3], v[:, j], a[:, j], b[:, j], S0[j])[1]
+                  for j in range(HV)], axis=1)
+    for node in (0, T // 2, T - 1):
+        assert np.abs(oracle.commit(p, node, k, a, U, S0) - S[node]).max() <= 1e-10
+    with pytest.raises(ValueError):
+        oracle.replay(p, q, k, v[:, :5], a[:, :5], b[:, :5], S0[:5])
+
+
+def test_q_scale_scales_the_output_only():
+    """o_i = S_i (s q_i) is linear in q while the states do not depend on q
+    (page: "The gated delta rule", the scale on q)."""
+    rng = np.random.default_rng(22)
+    T, H, dk, dv = 25, 2, 16, 8
+    p = trees.family("top2", T, rng)
+    q, k, v, a, b, S0 = _inputs(rng, T, H, dk, dv)
+    o1, S1 = oracle.replay(p, q, k, v, a, b, S0)
+    o2, S2 = oracle.replay(p, q, k, v, a, b, S0, scale=1.0 / np.sqrt(dk))
+    assert np.abs(o2 - o1 / np.sqrt(dk)).max() <= 1e-13
+    assert np.array_equal(S1, S2)
