@@ -26,16 +26,19 @@ VERIFY_STATE_READY = 0x2
 COMMIT_STATE_READY = 0x1
 
 # name -> (restype, argtypes); mirrors include/canopy.h
-_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_P, _I, _S, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
 SIGNATURES = {
     "canopy_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_workspace_init": (_I, [_P, _S, _P]),
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
-    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P, ctypes.c_uint, _P]),
-    "canopy_commit": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
+    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
+                                ctypes.c_uint, _P]),
+    "canopy_commit": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
-    "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
-    "canopy_serial_replay_static": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P]),
+    "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
+                                  _P]),
+    "canopy_serial_replay_static": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P,
+                                         _P]),
     "canopy_read_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "canopy_status_string": (ctypes.c_char_p, [_I]),
     "canopy_version": (_I, []),
@@ -96,12 +99,13 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
         raise CanopyError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
-def workspace_bytes(B: int, T: int, H: int, d: int) -> int:
-    return int(load().canopy_workspace_bytes(B, T, H, d, d))
+def workspace_bytes(B: int, T: int, HV: int, d: int) -> int:
+    """Workspace bytes for B streams of T nodes and HV value heads."""
+    return int(load().canopy_workspace_bytes(B, T, HV, d, d))
 
 
-def workspace(B: int, T: int, H: int, d: int, device="cuda") -> torch.Tensor:
-    n = workspace_bytes(B, T, H, d)
+def workspace(B: int, T: int, HV: int, d: int, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(B, T, HV, d)
     if n == 0:
         raise CanopyError("unsupported sizes for the workspace")
     ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -111,33 +115,47 @@ def workspace(B: int, T: int, H: int, d: int, device="cuda") -> torch.Tensor:
 
 def tree_prep(parent, g, ws):
     B, T = parent.shape
-    H = g.shape[-1]
+    HV = g.shape[-1]
     _need(parent, "parent", torch.int32)
-    _need(g, "g", torch.float32, (B, T, H))
-    _check(load().canopy_tree_prep(_ptr(parent), _ptr(g), T, B, H, _ptr(ws), _stream()), "canopy_tree_prep")
+    _need(g, "g", torch.float32, (B, T, HV))
+    _check(load().canopy_tree_prep(_ptr(parent), _ptr(g), T, B, HV, _ptr(ws), _stream()), "canopy_tree_prep")
+
+
+def _heads(q, k, v, g, beta, S0, parent):
+    """Check the shapes of one verify call's inputs: q, k [B, T, H, dk]
+    (key heads), v [B, T, HV, dv], g, beta [B, T, HV], S0 [B, HV, dv, dk]."""
+    _need(q, "q")
+    B, T, H, dk = q.shape
+    _need(k, "k", q.dtype, q.shape)
+    _need(v, "v", q.dtype)
+    if v.dim() != 4 or v.shape[:2] != q.shape[:2]:
+        raise CanopyError(f"v must have shape ({B}, {T}, HV, dv), got {tuple(v.shape)}")
+    HV, dv = v.shape[2], v.shape[3]
+    if HV % H:
+        raise CanopyError(f"value heads {HV} are not a multiple of key heads {H}")
+    _need(g, "g", torch.float32, (B, T, HV))
+    _need(beta, "beta", torch.float32, (B, T, HV))
+    _need(S0, "S0", torch.float32, (B, HV, dv, dk))
+    _need(parent, "parent", torch.int32, (B, T))
+    return B, T, H, HV, dk, dv
 
 
 def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None,
-           inputs_ready: bool = False, state_ready: bool = False):
-    """o [B, T, H, dv] for every node of every stream's tree.  inputs_ready:
-    q, k, v, g, beta and parent are not written by the kernel launched just
-    before this call on the current stream (CANOPY_VERIFY_INPUTS_READY);
-    state_ready (with inputs_ready): nor is S0 (CANOPY_VERIFY_STATE_READY)."""
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    _need(q, "q")
-    _need(k, "k", q.dtype, q.shape)
-    _need(v, "v", q.dtype, (B, T, H, dv))
-    _need(g, "g", torch.float32, (B, T, H))
-    _need(beta, "beta", torch.float32, (B, T, H))
-    _need(S0, "S0", torch.float32, (B, H, dv, dk))
-    _need(parent, "parent", torch.int32, (B, T))
+           inputs_ready: bool = False, state_ready: bool = False, scale: float = 1.0):
+    """o [B, T, HV, dv] for every node of every stream's tree; q and k carry
+    H key heads, v, g, beta and S0 HV value heads (a multiple of H), and
+    scale multiplies q.  inputs_ready: q, k, v, g, beta and parent are not
+    written by the kernel launched just before this call on the current
+    stream (CANOPY_VERIFY_INPUTS_READY); state_ready (with inputs_ready): nor
+    is S0 (CANOPY_VERIFY_STATE_READY)."""
+    B, T, H, HV, dk, dv = _heads(q, k, v, g, beta, S0, parent)
     _need(ws, "workspace", torch.uint8)
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
-    _need(out, "o", None, (B, T, H, dv))
+        out = torch.empty((B, T, HV, dv), dtype=o_dtype, device=q.device)
+    _need(out, "o", None, (B, T, HV, dv))
     st = load().canopy_tree_verify(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
-                                   _ptr(parent), T, B, H, dk, dv, SOLVE[solve], _ptr(out), _dt(out),
+                                   _ptr(parent), T, B, H, HV, dk, dv, float(scale), SOLVE[solve], _ptr(out),
+                                   _dt(out),
                                    _ptr(ws), (VERIFY_INPUTS_READY if inputs_ready else 0)
                                    | (VERIFY_STATE_READY if state_ready else 0), _stream())
     _check(st, "canopy_tree_verify")
@@ -145,70 +163,64 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
 
 
 def commit(accepted, S0, k, parent, ws, out=None, state_ready: bool = False):
-    """S_new [B, H, dv, dk] for the accepted node of every stream, from the
-    preceding verify call's k, parent and workspace.  state_ready: S0,
-    accepted, k and parent are not written by the kernel launched just
-    before this call on the current stream (CANOPY_COMMIT_STATE_READY)."""
+    """S_new [B, HV, dv, dk] for the accepted node of every stream, from the
+    preceding verify call's k (H key heads), parent and workspace.
+    state_ready: S0, accepted, k and parent are not written by the kernel
+    launched just before this call on the current stream
+    (CANOPY_COMMIT_STATE_READY)."""
     _need(S0, "S0", torch.float32)
     _need(parent, "parent", torch.int32)
-    B, H, dv, dk = S0.shape
+    _need(k, "k")
+    B, HV, dv, dk = S0.shape
     if parent.dim() != 2 or parent.shape[0] != B:
         raise CanopyError(f"parent must have shape ({B}, T), got {tuple(parent.shape)}")
     T = parent.shape[1]
+    if k.dim() != 4 or k.shape[0] != B or k.shape[1] != T or k.shape[3] != dk or HV % k.shape[2]:
+        raise CanopyError(f"k must have shape ({B}, {T}, H, {dk}) with H dividing {HV}, got {tuple(k.shape)}")
+    H = k.shape[2]
     _need(accepted, "accepted", torch.int32, (B,))
-    _need(k, "k", None, (B, T, H, dk))
     if out is None:
         out = torch.empty_like(S0)
     _need(out, "S_new", torch.float32, S0.shape)
-    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _ptr(parent), _dt(k), T, B, H, dk, dv,
+    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _ptr(parent), _dt(k), T, B, H, HV, dk,
+                              dv,
                               _ptr(ws), COMMIT_STATE_READY if state_ready else 0, _stream())
     _check(st, "canopy_commit")
     return out
 
 
-def snapshot_bytes(B: int, T: int, H: int, d: int) -> int:
-    return int(load().canopy_snapshot_bytes(B, T, H, d, d))
+def snapshot_bytes(B: int, T: int, HV: int, d: int) -> int:
+    return int(load().canopy_snapshot_bytes(B, T, HV, d, d))
 
 
-def serial_replay(q, k, v, g, beta, S0, parent, ws, snapshot=None, o_dtype=torch.float32, out=None):
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    _need(q, "q")
-    _need(k, "k", q.dtype, q.shape)
-    _need(v, "v", q.dtype, (B, T, H, dv))
-    _need(g, "g", torch.float32, (B, T, H))
-    _need(beta, "beta", torch.float32, (B, T, H))
-    _need(S0, "S0", torch.float32, (B, H, dv, dk))
-    _need(parent, "parent", torch.int32, (B, T))
+def serial_replay(q, k, v, g, beta, S0, parent, ws, snapshot=None, o_dtype=torch.float32, out=None,
+                  scale: float = 1.0):
+    B, T, H, HV, dk, dv = _heads(q, k, v, g, beta, S0, parent)
     if snapshot is None:
-        snapshot = torch.empty(snapshot_bytes(B, T, H, dk), dtype=torch.uint8, device=q.device)
+        snapshot = torch.empty(snapshot_bytes(B, T, HV, dk), dtype=torch.uint8, device=q.device)
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+        out = torch.empty((B, T, HV, dv), dtype=o_dtype, device=q.device)
+    _need(out, "o", None, (B, T, HV, dv))
     st = load().canopy_serial_replay(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
-                                     _ptr(parent), T, B, H, dk, dv, _ptr(out), _dt(out), _ptr(snapshot),
-                                     _ptr(ws), _stream())
+                                     _ptr(parent), T, B, H, HV, dk, dv, float(scale), _ptr(out), _dt(out),
+                                     _ptr(snapshot), _ptr(ws), _stream())
     _check(st, "canopy_serial_replay")
     return out
 
 
-def serial_replay_static(q, k, v, g, beta, S0, parent, err=None, o_dtype=torch.float32, out=None):
+def serial_replay_static(q, k, v, g, beta, S0, parent, err=None, o_dtype=torch.float32, out=None,
+                         scale: float = 1.0):
     """Serial replay whose snapshots live in the library's fixed device array
     (no workspace, no snapshot buffer); err is an optional int32 CUDA tensor
     of one element that receives the device error bits (OR-ed)."""
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    _need(q, "q")
-    _need(k, "k", q.dtype, q.shape)
-    _need(v, "v", q.dtype, (B, T, H, dv))
-    _need(g, "g", torch.float32, (B, T, H))
-    _need(beta, "beta", torch.float32, (B, T, H))
-    _need(S0, "S0", torch.float32, (B, H, dv, dk))
-    _need(parent, "parent", torch.int32, (B, T))
+    B, T, H, HV, dk, dv = _heads(q, k, v, g, beta, S0, parent)
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=o_dtype, device=q.device)
+        out = torch.empty((B, T, HV, dv), dtype=o_dtype, device=q.device)
+    _need(out, "o", None, (B, T, HV, dv))
     errp = _ptr(err) if err is not None else None
     st = load().canopy_serial_replay_static(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
-                                            _ptr(parent), T, B, H, dk, dv, _ptr(out), _dt(out), errp, _stream())
+                                            _ptr(parent), T, B, H, HV, dk, dv, float(scale), _ptr(out), _dt(out),
+                                            errp, _stream())
     _check(st, "canopy_serial_replay_static")
     return out
 

@@ -1,27 +1,32 @@
 // extern "C" entry points of libcanopy.so: argument checks, workspace
 // binding and kernel dispatch.  See include/canopy.h for the contract.
+#include <cmath>
+
 #include "common.cuh"
 
 namespace canopy {
+// Launchers take H = value heads (the units: v, g, beta, S0, o, workspace)
+// and HK = key heads (q, k); value head h reads key head h / (H / HK).
 cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
                              int with_order, cudaStream_t st);
 cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                  const Ws& ws, cudaStream_t st);
+                                  const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
+                                  int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                 const Ws& ws, int inputs_ready, int state_ready, cudaStream_t st);
+                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
+                                 int o_bf16, float scale, const Ws& ws, int inputs_ready, int state_ready,
+                                 cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
-                               const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
-                               int gram_done, cudaStream_t st);
+                               const float* S0, int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale,
+                               const Ws& ws, int gram_done, cudaStream_t st);
 cudaError_t launch_gram_tc(const void* q, const void* k, const void* v, const float* beta, const float* S0, int T,
-                           int B, int H, const Ws& ws, cudaStream_t st);
+                           int B, int H, int HK, const Ws& ws, cudaStream_t st);
 cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
-                          const void* k, int in_bf16,
-                          int T, int B, int H, int d, const Ws& ws, int state_ready, cudaStream_t st);
+                          const void* k, int in_bf16, int T, int B, int H, int HK, int d, const Ws& ws,
+                          int state_ready, cudaStream_t st);
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
-                          const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int d,
-                          void* o, int o_bf16, float* snap, int32_t* err, cudaStream_t st);
+                          const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
+                          int d, void* o, int o_bf16, float scale, float* snap, int32_t* err, cudaStream_t st);
 }  // namespace canopy
 
 using namespace canopy;
@@ -32,15 +37,18 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 
 bool sizes_ok(int B, int T, int H) { return B >= 1 && H >= 1 && T >= 1 && T <= kMaxT; }
 
+// key heads H, value heads HV: HV a positive multiple of H
+bool heads_ok(int H, int HV) { return H >= 1 && HV >= H && HV % H == 0; }
+
 canopy_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CANOPY_OK : CANOPY_ERR_CUDA; }
 
 }  // namespace
 
 extern "C" {
 
-size_t canopy_workspace_bytes(int B, int T, int H, int dk, int dv) {
-    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return 0;
-    return ws_layout(B, T, H, dv).total;
+size_t canopy_workspace_bytes(int B, int T, int HV, int dk, int dv) {
+    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return 0;
+    return ws_layout(B, T, HV, dv).total;
 }
 
 canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -48,82 +56,86 @@ canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream)
     return cuda_status(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));
 }
 
-size_t canopy_snapshot_bytes(int B, int T, int H, int dk, int dv) {
-    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return 0;
-    return size_t(B) * T * H * dv * dk * 4;
+size_t canopy_snapshot_bytes(int B, int T, int HV, int dk, int dv) {
+    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return 0;
+    return size_t(B) * T * HV * dv * dk * 4;
 }
 
-canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, void* workspace,
+canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int B, int HV, void* workspace,
                                void* stream) {
     if (!aligned16(parent) || !aligned16(g) || !aligned16(workspace)) return CANOPY_ERR_ARG;
-    if (!sizes_ok(B, T, H)) return CANOPY_ERR_UNSUPPORTED;
-    Ws ws = ws_bind(workspace, B, T, H, 32);  // tree-prep regions do not depend on dv
-    return cuda_status(launch_tree_prep(parent, g, T, B, H, ws, 1, static_cast<cudaStream_t>(stream)));
+    if (!sizes_ok(B, T, HV)) return CANOPY_ERR_UNSUPPORTED;
+    Ws ws = ws_bind(workspace, B, T, HV, 32);  // tree-prep regions do not depend on dv
+    return cuda_status(launch_tree_prep(parent, g, T, B, HV, ws, 1, static_cast<cudaStream_t>(stream)));
 }
 
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                  const float* g, const float* beta, const float* S0, const int32_t* parent, int T,
-                                 int B, int H, int dk, int dv, canopy_solve solve, void* o, canopy_dtype o_dtype,
-                                 void* workspace, unsigned flags, void* stream) {
+                                 int B, int H, int HV, int dk, int dv, float scale, canopy_solve solve, void* o,
+                                 canopy_dtype o_dtype, void* workspace, unsigned flags, void* stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
         !aligned16(parent) || !aligned16(o) || !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
-        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN) || (flags & ~(CANOPY_VERIFY_INPUTS_READY | CANOPY_VERIFY_STATE_READY)))
+        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN) ||
+        (flags & ~(CANOPY_VERIFY_INPUTS_READY | CANOPY_VERIFY_STATE_READY)) || !std::isfinite(scale))
         return CANOPY_ERR_ARG;
-    if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
-    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    Ws ws = ws_bind(workspace, B, T, H, dv);
+    Ws ws = ws_bind(workspace, B, T, HV, dv);
     const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
     const bool tc = in_bf16 && dk == 128 && T <= 64;
     if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
     if (tc && solve == CANOPY_SOLVE_NEUMANN)
-        return cuda_status(launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws, st));
+        return cuda_status(
+            launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
     if (tc)
-        return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, H, o, o_bf16, ws,
+        return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws,
                                                 (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
                                                 (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
-    cudaError_t e = launch_tree_prep(parent, g, T, B, H, ws, 0, st);
+    cudaError_t e = launch_tree_prep(parent, g, T, B, HV, ws, 0, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     // bf16 inputs beyond one 64-node block: the Gram products on tcgen05
     const bool gram_tc = in_bf16 && dk == 128 && T > 64;
     if (gram_tc) {
-        e = launch_gram_tc(q, k, v, beta, S0, T, B, H, ws, st);
+        e = launch_gram_tc(q, k, v, beta, S0, T, B, HV, H, ws, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, H, dk, o, o_bf16, ws, gram_tc, st));
+    return cuda_status(
+        launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, HV, H, dk, o, o_bf16, scale, ws, gram_tc, st));
 }
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,
-                            const int32_t* parent, canopy_dtype in_dtype, int T, int B, int H, int dk, int dv,
-                            const void* workspace, unsigned flags, void* stream) {
+                            const int32_t* parent, canopy_dtype in_dtype, int T, int B, int H, int HV, int dk,
+                            int dv, const void* workspace, unsigned flags, void* stream) {
     if (!aligned16(accepted) || !aligned16(S0) || !aligned16(S_new) || !aligned16(k) || !aligned16(parent) ||
         !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if (in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) return CANOPY_ERR_ARG;
     if (flags & ~CANOPY_COMMIT_STATE_READY) return CANOPY_ERR_ARG;
-    if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
-    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
-    Ws ws = ws_bind(const_cast<void*>(workspace), B, T, H, dv);
-    return cuda_status(launch_commit(accepted, parent, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, H, dk, ws,
+    if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    Ws ws = ws_bind(const_cast<void*>(workspace), B, T, HV, dv);
+    return cuda_status(launch_commit(accepted, parent, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, HV, H, dk, ws,
                                      (flags & CANOPY_COMMIT_STATE_READY) != 0, static_cast<cudaStream_t>(stream)));
 }
 
 canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                    const float* g, const float* beta, const float* S0, const int32_t* parent, int T,
-                                   int B, int H, int dk, int dv, void* o, canopy_dtype o_dtype, void* snapshot,
-                                   void* workspace, void* stream) {
+                                   int B, int H, int HV, int dk, int dv, float scale, void* o, canopy_dtype o_dtype,
+                                   void* snapshot, void* workspace, void* stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
         !aligned16(parent) || !aligned16(o) || !aligned16(snapshot) || !aligned16(workspace))
         return CANOPY_ERR_ARG;
-    if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16))
+    if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
+        !std::isfinite(scale))
         return CANOPY_ERR_ARG;
-    if (B <= 0 || H <= 0 || T <= 0) return CANOPY_ERR_ARG;
-    if (!sizes_ok(B, T, H) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
-    Ws ws = ws_bind(workspace, B, T, H, dv);
-    return cuda_status(launch_serial(q, k, v, in_dtype == CANOPY_BF16, g, beta, S0, parent, T, B, H, dk, o,
-                                     o_dtype == CANOPY_BF16, static_cast<float*>(snapshot), ws.err,
+    if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    Ws ws = ws_bind(workspace, B, T, HV, dv);
+    return cuda_status(launch_serial(q, k, v, in_dtype == CANOPY_BF16, g, beta, S0, parent, T, B, HV, H, dk, o,
+                                     o_dtype == CANOPY_BF16, scale, static_cast<float*>(snapshot), ws.err,
                                      static_cast<cudaStream_t>(stream)));
 }
 

@@ -36,8 +36,8 @@ __device__ inline float4 k4(const __nv_bfloat16* p) {
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted,
                                                     const int32_t* __restrict__ parent, const float* S0,
-                                                    float* S_new, const InT* __restrict__ k, int T, int H, Ws ws,
-                                                    int state_ready) {
+                                                    float* S_new, const InT* __restrict__ k, int T, int H, int HK,
+                                                    Ws ws, int state_ready) {
     constexpr int C4 = DK / 4;             // float4 per state row (threads per row)
     constexpr int F4 = ROWS * C4 / NT;     // float4 per thread = rows per thread
     constexpr int KV = 16 / sizeof(InT);   // k elements per 16-byte load
@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     __shared__ int sN, sBad;
     const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
     const int v0 = rt * ROWS;
+    const int hk = h / (H / HK);  // the key head this value head reads
     // this thread: rows r0 .. r0 + F4 - 1 of the tile, float4 column c4
     const int c4 = t % C4, r0 = (t / C4) * F4;
     const size_t sbase = ((size_t(b) * H + h) * DV + v0) * DK;
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
         for (int e = t; e < cn * (DK / KV); e += NT) {
             const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[r];
             *reinterpret_cast<uint4*>(&sK[r][c]) =
-                *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * H + h) * DK + c);
+                *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
         }
     }
     if (state_ready) pdl_wait();
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
             for (int e = t; e < cn * (DK / KV); e += NT) {
                 const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[c0 + r];
                 *reinterpret_cast<uint4*>(&sK[r][c]) =
-                    *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * H + h) * DK + c);
+                    *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
             }
         }
         for (int e = t; e < cn * ROWS; e += NT) {
@@ -158,23 +159,24 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
 
 template <typename InT, int D>
 static cudaError_t launch_commit_typed(const int32_t* accepted, const int32_t* parent, const float* S0,
-                                       float* S_new, const void* k, int T, int B, int H, const Ws& ws,
+                                       float* S_new, const void* k, int T, int B, int H, int HK, const Ws& ws,
                                        int state_ready, cudaStream_t st) {
     dim3 grid(D / cm::ROWS, H, B);
     return launch_pdl(cm::commit_kernel<InT, D, D>, grid, dim3(cm::NT), 0, st, accepted, parent, S0, S_new,
-                      static_cast<const InT*>(k), T, H, ws, state_ready);
+                      static_cast<const InT*>(k), T, H, HK, ws, state_ready);
 }
 
 cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
-                          const void* k, int in_bf16, int T, int B, int H, int d, const Ws& ws, int state_ready,
-                          cudaStream_t st) {
+                          const void* k, int in_bf16, int T, int B, int H, int HK, int d, const Ws& ws,
+                          int state_ready, cudaStream_t st) {
     using bf = __nv_bfloat16;
+    const int sr = state_ready;
     if (d == 128) {
-        if (in_bf16) return launch_commit_typed<bf, 128>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
-        return launch_commit_typed<float, 128>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
+        if (in_bf16) return launch_commit_typed<bf, 128>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
+        return launch_commit_typed<float, 128>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
     }
-    if (in_bf16) return launch_commit_typed<bf, 32>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
-    return launch_commit_typed<float, 32>(accepted, parent, S0, S_new, k, T, B, H, ws, state_ready, st);
+    if (in_bf16) return launch_commit_typed<bf, 32>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
+    return launch_commit_typed<float, 32>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
 }
 
 }  // namespace canopy

@@ -72,7 +72,7 @@ __device__ inline void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
 __global__ void __launch_bounds__(NT, 1)
     gram_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
-                   const float* __restrict__ beta, int T, int H, Ws ws) {
+                   const float* __restrict__ beta, int T, int H, int HK, Ws ws) {
     using L = Smem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int quad = warp & 3;  // TMEM lane quadrant of this warp
     const int r = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int n0 = TP * r;      // first node of the block
+    const int hk = h / (H / HK);  // the key head this value head reads
     uint8_t* sQK = sm + L::QK;
 
     if (tid == 0) {
@@ -94,15 +95,15 @@ __global__ void __launch_bounds__(NT, 1)
         fence_mbar_init();
         *sFlag = 0;
         mbar_expect_tx(&bars[BAR_QK], 4 * TP * 64 * 2);
-        tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, h, n0, b);
-        tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, h, n0, b);
-        tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, h, n0, b);
-        tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, h, n0, b);
+        tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, hk, n0, b);
+        tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, hk, n0, b);
+        tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, hk, n0, b);
+        tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, hk, n0, b);
         if (r > 0) {
             mbar_expect_tx(&bars[BAR_KS], r * L::KS_TILE);
             for (int s = 0; s < r; ++s) {
-                tma_load_4d(sm + L::KS + s * L::KS_TILE, &tmK, &bars[BAR_KS], 0, h, TP * s, b);
-                tma_load_4d(sm + L::KS + s * L::KS_TILE + 8192, &tmK, &bars[BAR_KS], 64, h, TP * s, b);
+                tma_load_4d(sm + L::KS + s * L::KS_TILE, &tmK, &bars[BAR_KS], 0, hk, TP * s, b);
+                tma_load_4d(sm + L::KS + s * L::KS_TILE + 8192, &tmK, &bars[BAR_KS], 64, hk, TP * s, b);
             }
         }
         for (int i = 0; i < 2; ++i) {
@@ -293,9 +294,9 @@ bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H);
 bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_gram_tc(const void* q, const void* k, const void* v, const float* beta, const float* S0, int T,
-                           int B, int H, const Ws& ws, cudaStream_t st) {
+                           int B, int H, int HK, const Ws& ws, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ms;
-    if (!make_bf16_row_map(&mq, q, B, T, H) || !make_bf16_row_map(&mk, k, B, T, H) ||
+    if (!make_bf16_row_map(&mq, q, B, T, HK) || !make_bf16_row_map(&mk, k, B, T, HK) ||
         !make_bf16_row_map(&mv, v, B, T, H) || !make_state_map(&ms, S0, B, H))
         return cudaErrorInvalidValue;
     const int smem = gtc::Smem::TOTAL + 1024;
@@ -306,7 +307,7 @@ cudaError_t launch_gram_tc(const void* q, const void* k, const void* v, const fl
         attr = true;
     }
     dim3 grid((T + gtc::TP - 1) / gtc::TP, H, B);
-    gtc::gram_tc_kernel<<<grid, gtc::NT, smem, st>>>(mq, mk, mv, ms, beta, T, H, ws);
+    gtc::gram_tc_kernel<<<grid, gtc::NT, smem, st>>>(mq, mk, mv, ms, beta, T, H, HK, ws);
     return cudaGetLastError();
 }
 

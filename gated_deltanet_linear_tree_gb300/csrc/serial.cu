@@ -5,7 +5,7 @@
 // value tile) walks the nodes in index order, takes its parent's state from
 // a per-node snapshot buffer (or S0 for the root), applies one step of the
 // gated delta rule in fp32,
-//     S_i = alpha_i S_p (I - beta_i k_i k_i^T) + beta_i v_i k_i^T,  o_i = S_i q_i,
+//     S_i = alpha_i S_p (I - beta_i k_i k_i^T) + beta_i v_i k_i^T,  o_i = S_i (scale q_i),
 // and writes the node's output.  Two choices keep it an honest opponent:
 // the state of node i-1 stays in registers, so a node whose parent is i-1
 // reads nothing back, and a snapshot is written only for nodes that have a
@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) replay_kernel(const InT* __restrict__ q, 
                                                      const InT* __restrict__ v, const float* __restrict__ g,
                                                      const float* __restrict__ beta, const float* __restrict__ S0,
                                                      const int32_t* __restrict__ parent, OutT* __restrict__ o,
-                                                     float* snap, int T, int H, int32_t* err) {
+                                                     float* snap, int T, int H, int HK, float scale, int32_t* err) {
     constexpr int C4 = DK / 32;  // float4 chunks per lane
     __shared__ int sPar[kMaxT];
     __shared__ int sSnap[kMaxT];
@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(128) replay_kernel(const InT* __restrict__ q, 
     const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
     const int row = t >> 3, gl = t & 7;  // state row within the tile, lane within the row group
     const int vr = rt * ROWS + row;
+    const int hk = h / (H / HK);  // the key head this value head reads
 
     int bad = 0;
     for (int i = t; i < T; i += blockDim.x) {
@@ -68,11 +69,12 @@ __global__ void __launch_bounds__(128) replay_kernel(const InT* __restrict__ q, 
             for (int c = 0; c < C4; ++c) s[c] = *reinterpret_cast<const float4*>(src + (c * 8 + gl) * 4);
         }
         const size_t nrow = (size_t(b) * T + i) * H + h;
+        const size_t krow = (size_t(b) * T + i) * HK + hk;
         float4 kk[C4], qq[C4];
 #pragma unroll
         for (int c = 0; c < C4; ++c) {
-            kk[c] = load4(k + nrow * DK + (c * 8 + gl) * 4);
-            qq[c] = load4(q + nrow * DK + (c * 8 + gl) * 4);
+            kk[c] = load4(k + krow * DK + (c * 8 + gl) * 4);
+            qq[c] = load4(q + krow * DK + (c * 8 + gl) * 4);
         }
         const float a = sA[i], be = sB[i];
         const float vv = to_f(v[nrow * DV + vr]);
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(128) replay_kernel(const InT* __restrict__ q, 
         oo += __shfl_xor_sync(0xffffffffu, oo, 4);
         oo += __shfl_xor_sync(0xffffffffu, oo, 2);
         oo += __shfl_xor_sync(0xffffffffu, oo, 1);
-        if (gl == 0) store_out(o + nrow * DV + vr, oo);
+        if (gl == 0) store_out(o + nrow * DV + vr, scale * oo);
         if (sSnap[i]) {
             float* dst = snap + ((nrow)*DV + vr) * DK;
 #pragma unroll
@@ -110,19 +112,20 @@ __global__ void __launch_bounds__(128) replay_kernel(const InT* __restrict__ q, 
 template <typename InT, typename OutT, int D>
 static cudaError_t launch_serial_typed(const void* q, const void* k, const void* v, const float* g,
                                        const float* beta, const float* S0, const int32_t* parent, int T, int B,
-                                       int H, void* o, float* snap, int32_t* err, cudaStream_t st) {
+                                       int H, int HK, void* o, float scale, float* snap, int32_t* err,
+                                       cudaStream_t st) {
     dim3 grid(D / serial::ROWS, H, B);
     serial::replay_kernel<InT, OutT, D, D><<<grid, 128, 0, st>>>(
         static_cast<const InT*>(q), static_cast<const InT*>(k), static_cast<const InT*>(v), g, beta, S0, parent,
-        static_cast<OutT*>(o), snap, T, H, err);
+        static_cast<OutT*>(o), snap, T, H, HK, scale, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
-                          const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int d,
-                          void* o, int o_bf16, float* snap, int32_t* err, cudaStream_t st) {
+                          const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
+                          int d, void* o, int o_bf16, float scale, float* snap, int32_t* err, cudaStream_t st) {
 #define CANOPY_SERIAL(IT, OT, D) \
-    return launch_serial_typed<IT, OT, D>(q, k, v, g, beta, S0, parent, T, B, H, o, snap, err, st)
+    return launch_serial_typed<IT, OT, D>(q, k, v, g, beta, S0, parent, T, B, H, HK, o, scale, snap, err, st)
     if (d == 128) {
         if (in_bf16) {
             if (o_bf16) CANOPY_SERIAL(__nv_bfloat16, __nv_bfloat16, 128);

@@ -41,7 +41,7 @@ __device__ inline void load8(const float* p, float (&x)[8]) {
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, const InT* __restrict__ k,
                                                    const InT* __restrict__ v, const float* __restrict__ beta,
-                                                   const float* __restrict__ S0, int T, int H, Ws ws) {
+                                                   const float* __restrict__ S0, int T, int H, int HK, Ws ws) {
     constexpr int GROUPS = 256 / DV;          // row groups for the S0 products
     constexpr int RPG = ROWS / GROUPS;        // rows per group
     __shared__ float sq[ROWS][DK];
@@ -50,13 +50,14 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
     __shared__ int sPathList[8][kMaxT];
     const int i0 = blockIdx.x * ROWS, h = blockIdx.y, b = blockIdx.z;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const size_t rowstride = size_t(H) * DK;
+    const size_t rowstride = size_t(HK) * DK;   // q and k rows: key heads
+    const int hk = h / (H / HK);                // the key head this value head reads
 
     for (int e = t; e < ROWS * DK; e += 256) {
         const int r = e / DK, d = e % DK, i = i0 + r;
         float xq = 0.f, xk = 0.f;
         if (i < T) {
-            const size_t off = (size_t(b) * T + i) * rowstride + size_t(h) * DK + d;
+            const size_t off = (size_t(b) * T + i) * rowstride + size_t(hk) * DK + d;
             xq = to_f(q[off]);
             xk = to_f(k[off]);
         }
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
         float* Crow = ws.cs + ((size_t(b) * H + h) * T + i) * T;
         for (int p = lane; p < n; p += 32) {
             const int j = plist[p];
-            const InT* kj = k + (size_t(b) * T + j) * rowstride + size_t(h) * DK;
+            const InT* kj = k + (size_t(b) * T + j) * rowstride + size_t(hk) * DK;
             float kk0 = 0.f, kk1 = 0.f, qk0 = 0.f, qk1 = 0.f;
 #pragma unroll 2
             for (int d = 0; d < DK; d += 8) {
@@ -169,7 +170,7 @@ __host__ __device__ constexpr size_t solve_smem(int T, int DV) {
 // into a list and stages (j, G_ij, C_ij); then the chunk's nodes are solved
 // level by level, each group taking nodes of the level.
 template <typename OutT, int DV>
-__device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, const Ws& ws) {
+__device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, const Ws& ws, float scale) {
     constexpr int NG = SOLVE_NT / DV;
     extern __shared__ float smem[];
     float* sU = smem;                                       // [T][DV]
@@ -327,7 +328,7 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
                     out += sXq[e * DV + c] + sCii[e] * acc;
                     sU[i * DV + c] = acc;
                     ws.U[ni * DV + c] = acc;
-                    store_out(o + ni * DV + c, out);
+                    store_out(o + ni * DV + c, scale * out);
                 }
             } else {
                 for (int e = s0 + grp; e < s1; e += NG) {
@@ -355,7 +356,7 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
                     out += out2 + sCii[e] * acc;
                     sU[i * DV + c] = acc;
                     ws.U[ni * DV + c] = acc;
-                    store_out(o + ni * DV + c, out);
+                    store_out(o + ni * DV + c, scale * out);
                 }
             }
             __syncthreads();
@@ -365,8 +366,9 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
 }
 
 template <typename OutT, int DV>
-__global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict__ o, int T, int H, Ws ws) {
-    level_solve<OutT, DV>(o, T, H, ws);
+__global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict__ o, int T, int H, Ws ws,
+                                                               float scale) {
+    level_solve<OutT, DV>(o, T, H, ws, scale);
 }
 
 // Blocked forward substitution over 64-node diagonal blocks (canopy page,
@@ -421,7 +423,8 @@ __device__ __forceinline__ void tile_mac(float (&acc)[4][4], const float* a, con
 }
 
 template <typename OutT, int DV>
-__global__ void __launch_bounds__(BLK_NT, 1) solve_block_kernel(OutT* __restrict__ o, int T, int H, Ws ws) {
+__global__ void __launch_bounds__(BLK_NT, 1) solve_block_kernel(OutT* __restrict__ o, int T, int H, Ws ws,
+                                                                float scale) {
     static_assert(DV == 128 && BLK_NT == 512 && SOLVE_NT == BLK_NT,
                   "thread tile: 16 row groups x 32 column groups of 4 x 4");
     __shared__ int sDepth;
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(BLK_NT, 1) solve_block_kernel(OutT* __restrict
     for (int i = threadIdx.x; i < T; i += BLK_NT) atomicMax(&sDepth, ws.depth[size_t(blockIdx.y) * T + i]);
     __syncthreads();
     if (sDepth < BLOCK_MIN_DEPTH) {
-        level_solve<OutT, DV>(o, T, H, ws);
+        level_solve<OutT, DV>(o, T, H, ws, scale);
         return;
     }
     extern __shared__ float smem[];
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(BLK_NT, 1) solve_block_kernel(OutT* __restrict
             if (i < T) {
                 OutT* op = o + ((size_t(b) * T + i) * H + h) * DV + 4 * cg;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) store_out(op + cc, accO[q][cc]);
+                for (int cc = 0; cc < 4; ++cc) store_out(op + cc, scale * accO[q][cc]);
             }
         }
     }
@@ -552,13 +555,13 @@ __global__ void __launch_bounds__(BLK_NT, 1) solve_block_kernel(OutT* __restrict
 
 template <typename InT, int DK, int DV>
 static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v, const float* beta,
-                                     const float* S0, int T, int B, int H, void* o, int o_bf16, const Ws& ws,
-                                     int gram_done, cudaStream_t st) {
+                                     const float* S0, int T, int B, int H, int HK, void* o, int o_bf16, float scale,
+                                     const Ws& ws, int gram_done, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
     if (!gram_done) {
         dim3 g1((T + simt::ROWS - 1) / simt::ROWS, H, B);
         simt::gram_kernel<InT, DK, DV><<<g1, 256, 0, st>>>(static_cast<const InT*>(q), static_cast<const InT*>(k),
-                                                          static_cast<const InT*>(v), beta, S0, T, H, ws);
+                                                          static_cast<const InT*>(v), beta, S0, T, H, HK, ws);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -580,7 +583,7 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
                     attr = true;
                 }
                 simt::solve_block_kernel<__nv_bfloat16, DV><<<g2, simt::BLK_NT, smem, st>>>(
-                    static_cast<__nv_bfloat16*>(o), T, H, ws);
+                    static_cast<__nv_bfloat16*>(o), T, H, ws, scale);
             } else {
                 static bool attr = false;
                 if (!attr) {
@@ -589,7 +592,8 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
                     if (e != cudaSuccess) return e;
                     attr = true;
                 }
-                simt::solve_block_kernel<float, DV><<<g2, simt::BLK_NT, smem, st>>>(static_cast<float*>(o), T, H, ws);
+                simt::solve_block_kernel<float, DV><<<g2, simt::BLK_NT, smem, st>>>(static_cast<float*>(o), T, H, ws,
+                                                                                    scale);
             }
             return cudaGetLastError();
         }
@@ -605,7 +609,7 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
             attr = true;
         }
         simt::solve_level_kernel<__nv_bfloat16, DV><<<g2, simt::SOLVE_NT, smem, st>>>(
-            static_cast<__nv_bfloat16*>(o), T, H, ws);
+            static_cast<__nv_bfloat16*>(o), T, H, ws, scale);
     } else {
         static bool attr = false;
         if (!attr) {
@@ -614,21 +618,25 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        simt::solve_level_kernel<float, DV><<<g2, simt::SOLVE_NT, smem, st>>>(static_cast<float*>(o), T, H, ws);
+        simt::solve_level_kernel<float, DV><<<g2, simt::SOLVE_NT, smem, st>>>(static_cast<float*>(o), T, H, ws,
+                                                                              scale);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
-                               const float* S0, int T, int B, int H, int d, void* o, int o_bf16, const Ws& ws,
-                               int gram_done, cudaStream_t st) {
+                               const float* S0, int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale,
+                               const Ws& ws, int gram_done, cudaStream_t st) {
     using bf = __nv_bfloat16;
+#define CANOPY_SIMT(IT, D) \
+    return launch_simt_typed<IT, D, D>(q, k, v, beta, S0, T, B, H, HK, o, o_bf16, scale, ws, gram_done, st)
     if (d == 128) {
-        if (in_bf16) return launch_simt_typed<bf, 128, 128>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
-        return launch_simt_typed<float, 128, 128>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
+        if (in_bf16) CANOPY_SIMT(bf, 128);
+        CANOPY_SIMT(float, 128);
     }
-    if (in_bf16) return launch_simt_typed<bf, 32, 32>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
-    return launch_simt_typed<float, 32, 32>(q, k, v, beta, S0, T, B, H, o, o_bf16, ws, gram_done, st);
+    if (in_bf16) CANOPY_SIMT(bf, 32);
+    CANOPY_SIMT(float, 32);
+#undef CANOPY_SIMT
 }
 
 }  // namespace canopy

@@ -102,6 +102,8 @@ struct Params {
     uint32_t* mask;
     int32_t* err;
     int B, T, H, W, o_bf16;
+    int HK;       // key heads: value head h reads q and k of key head h / (H / HK)
+    float scale;  // factor on q (applied to o)
 };
 
 __device__ inline float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -221,10 +223,11 @@ __global__ void __launch_bounds__(NT, 2)
     uint8_t* sQK = sm + L::QK;
     if (tid == 0) {
         mbar_expect_tx(&bars[0], 4 * 64 * 64 * 2);
-        tma_load_4d(sQK + 0, &tmQ, &bars[0], 0, h, 0, b);
-        tma_load_4d(sQK + 16384, &tmQ, &bars[0], 64, h, 0, b);
-        tma_load_4d(sQK + 8192, &tmK, &bars[0], 0, h, 0, b);
-        tma_load_4d(sQK + 24576, &tmK, &bars[0], 64, h, 0, b);
+        const int hk = h / (H / p.HK);
+        tma_load_4d(sQK + 0, &tmQ, &bars[0], 0, hk, 0, b);
+        tma_load_4d(sQK + 16384, &tmQ, &bars[0], 64, hk, 0, b);
+        tma_load_4d(sQK + 8192, &tmK, &bars[0], 0, hk, 0, b);
+        tma_load_4d(sQK + 24576, &tmK, &bars[0], 64, hk, 0, b);
     }
 
     // Tree prep (threads 0..63 own nodes; the whole CTA takes the barriers).
@@ -579,6 +582,7 @@ __global__ void __launch_bounds__(NT, 2)
         const int i = qrow ? row : row - 64;
         const bool live = i < T;
         const size_t nb = ((size_t(b) * T + (live ? i : 0)) * H + h) * DV + 64 * half;
+        const float sc = qrow ? p.scale : 1.f;  // o carries the scale on q, U does not
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
             uint32_t r[16];
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const __nv_bfloat162 pr =
-                        __floats2bfloat162_rn(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                        __floats2bfloat162_rn(sc * __uint_as_float(r[2 * e]), sc * __uint_as_float(r[2 * e + 1]));
                     w[e] = *reinterpret_cast<const uint32_t*>(&pr);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + nb + cb * 16);
@@ -601,8 +605,8 @@ __global__ void __launch_bounds__(NT, 2)
                 float4* dst = reinterpret_cast<float4*>(base + nb + cb * 16);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                         __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+                    dst[e] = make_float4(sc * __uint_as_float(r[4 * e]), sc * __uint_as_float(r[4 * e + 1]),
+                                         sc * __uint_as_float(r[4 * e + 2]), sc * __uint_as_float(r[4 * e + 3]));
             }
         }
     }
@@ -690,7 +694,7 @@ bool make_state_map(CUtensorMap* m, const float* base, int B, int H) {
 
 static cudaError_t launch_neumann(const void* q, const void* k, const tc::Params& prm, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
-    if (!make_bf16_row_map(&mq, q, prm.B, prm.T, prm.H) || !make_bf16_row_map(&mk, k, prm.B, prm.T, prm.H) ||
+    if (!make_bf16_row_map(&mq, q, prm.B, prm.T, prm.HK) || !make_bf16_row_map(&mk, k, prm.B, prm.T, prm.HK) ||
         !make_bf16_row_map(&mv, prm.v, prm.B, prm.T, prm.H))
         return cudaErrorInvalidValue;
     const int smem = tc::Smem::TOTAL_NEU + 1024;
@@ -707,8 +711,8 @@ static cudaError_t launch_neumann(const void* q, const void* k, const tc::Params
 }
 
 cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                  const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                  const Ws& ws, cudaStream_t st) {
+                                  const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
+                                  int o_bf16, float scale, const Ws& ws, cudaStream_t st) {
     tc::Params prm;
     prm.v = static_cast<const __nv_bfloat16*>(v);
     prm.g = g;
@@ -726,6 +730,8 @@ cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, c
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
+    prm.HK = HK;
+    prm.scale = scale;
     return launch_neumann(q, k, prm, st);
 }
 

@@ -100,6 +100,8 @@ struct Params {
     uint32_t* mask;
     int32_t* err;
     int B, T, H, W, o_bf16;
+    int HK;       // key heads: value head h reads q and k of key head h / (H / HK)
+    float scale;  // factor on q (applied to o)
     int inputs_ready;  // the inputs other than S0 may be read before the preceding kernel completes
     int state_ready;   // with inputs_ready: S0 too
 };
@@ -206,10 +208,11 @@ __global__ void __launch_bounds__(NT, 2)
         *sNmax = 0;
         // Q and K next: the solve path waits on them
         mbar_expect_tx(&bars[BAR_QK], 4 * 64 * 64 * 2);
-        tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, h, 0, b);
-        tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, h, 0, b);
-        tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, h, 0, b);
-        tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, h, 0, b);
+        const int hk = h / (H / p.HK);
+        tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, hk, 0, b);
+        tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, hk, 0, b);
+        tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, hk, 0, b);
+        tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, hk, 0, b);
     }
     if (warp == 0) {
         tmem_alloc(sTmem, kTmemCols);
@@ -586,6 +589,7 @@ __global__ void __launch_bounds__(NT, 2)
         float* tile = reinterpret_cast<float*>(sm + (solve ? L::OT : L::UT));
         __nv_bfloat16* tile16 = reinterpret_cast<__nv_bfloat16*>(sm + L::OT);
         const bool o16 = solve && p.o_bf16;
+        const float sc = solve ? p.scale : 1.f;  // o carries the scale on q, U does not
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
             uint32_t y[16];
@@ -593,10 +597,11 @@ __global__ void __launch_bounds__(NT, 2)
             tmem_wait_ld();
             if (o16) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) tile16[(blk * 16 + e) * DV + c] = __float2bfloat16_rn(__uint_as_float(y[e]));
+                for (int e = 0; e < 16; ++e)
+                    tile16[(blk * 16 + e) * DV + c] = __float2bfloat16_rn(sc * __uint_as_float(y[e]));
             } else {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) tile[(blk * 16 + e) * DV + c] = __uint_as_float(y[e]);
+                for (int e = 0; e < 16; ++e) tile[(blk * 16 + e) * DV + c] = sc * __uint_as_float(y[e]);
             }
         }
         fence_proxy_async_smem();
@@ -634,10 +639,11 @@ bool make_out_map(CUtensorMap* m, void* base, int B, int T, int H, int bf16);
 bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const float* S0, const int32_t* parent, int T, int B, int H, void* o, int o_bf16,
-                                 const Ws& ws, int inputs_ready, int state_ready, cudaStream_t st) {
+                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
+                                 int o_bf16, float scale, const Ws& ws, int inputs_ready, int state_ready,
+                                 cudaStream_t st) {
     CUtensorMap mq, mk, mv, mo, mu, ms;
-    if (!make_bf16_row_map(&mq, q, B, T, H) || !make_bf16_row_map(&mk, k, B, T, H) ||
+    if (!make_bf16_row_map(&mq, q, B, T, HK) || !make_bf16_row_map(&mk, k, B, T, HK) ||
         !make_bf16_row_map(&mv, v, B, T, H) || !make_out_map(&mo, o, B, T, H, o_bf16) ||
         !make_out_map(&mu, ws.U, B, T, H, 0) || !make_state_map(&ms, S0, B, H))
         return cudaErrorInvalidValue;
@@ -656,6 +662,8 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
+    prm.HK = HK;
+    prm.scale = scale;
     prm.inputs_ready = inputs_ready;
     prm.state_ready = inputs_ready && state_ready;
     const int smem = tcf::Smem::TOTAL + 1024;

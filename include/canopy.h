@@ -10,8 +10,13 @@
  * state is rebuilt (commit).  In this library's orientation the state is
  * S[dv][dk] and the rule ("The gated delta rule", TreeWY's form) is
  *     S_i = g_i * S_parent(i) * (I - beta_i k_i k_i^T) + beta_i v_i k_i^T
- *     o_i = S_i q_i                     (S_parent(0) = S0, no scale on q)
- * with g_i the decay gate alpha_i in (0, 1].
+ *     o_i = S_i (scale * q_i)           (S_parent(0) = S0)
+ * with g_i the decay gate alpha_i in (0, 1].  Heads ("Qwen3.5-9B shapes"
+ * and "Design decisions", memory layout): q and k have H key heads; v, g,
+ * beta, S0, o and the workspace have HV value heads, HV a multiple of H, and
+ * value head j reads key head j / (HV / H) (grouped value attention; HV = H
+ * is one q/k per head).  scale is the factor on q (1/sqrt(dk) in FLA; 1 for
+ * the plain rule).
  *
  * Conventions for every entry point:
  *   - Pointers marked "device" are CUDA device pointers; the caller owns and
@@ -19,12 +24,12 @@
  *     synchronises inside a compute call; work is enqueued on `stream`
  *     (a cudaStream_t passed as void*, NULL = legacy default stream).
  *   - All arrays are dense, row-major, with the last index fastest:
- *       q, k     [B][T][H][dk]   bf16 or fp32 (in_dtype)
- *       v        [B][T][H][dv]   bf16 or fp32 (in_dtype)
- *       g, beta  [B][T][H]       fp32 (g = decay gate alpha, linear space)
- *       S0       [B][H][dv][dk]  fp32
- *       parent   [B][T]          int32, parent[b][0] = -1, 0 <= parent[b][i] < i
- *       o        [B][T][H][dv]   fp32 or bf16 (o_dtype)
+ *       q, k     [B][T][H][dk]    bf16 or fp32 (in_dtype)
+ *       v        [B][T][HV][dv]   bf16 or fp32 (in_dtype)
+ *       g, beta  [B][T][HV]       fp32 (g = decay gate alpha, linear space)
+ *       S0       [B][HV][dv][dk]  fp32
+ *       parent   [B][T]           int32, parent[b][0] = -1, 0 <= parent[b][i] < i
+ *       o        [B][T][HV][dv]   fp32 or bf16 (o_dtype)
  *   - Device pointers must be 16-byte aligned (vector and TMA loads).
  *   - Argument errors are detected on the host and returned before anything
  *     is enqueued.  Errors that depend on device data (a malformed tree, a
@@ -32,7 +37,8 @@
  *     wait that timed out) set bits in a sticky device error word inside the
  *     workspace; the outputs of that call are then undefined.  Read and clear
  *     the word with canopy_read_device_error().  No kernel traps or asserts.
- *   - Sizes supported: 1 <= T <= 256, B >= 1, H >= 1, dk = dv = 128 for every
+ *   - Sizes supported: 1 <= T <= 256, B >= 1, H >= 1, HV a multiple of H
+ *     (HV = H where an entry point takes one head count), dk = dv = 128 for every
  *     entry point; dk = dv = 32 additionally for the fp32 (tier A) and serial
  *     paths.  Other values return CANOPY_ERR_UNSUPPORTED.
  */
@@ -79,13 +85,13 @@ typedef enum {
 #define CANOPY_DEVERR_ACCEPTED 0x4  /* commit: accepted node not in [-1, T)             */
 #define CANOPY_DEVERR_TIMEOUT  0x8  /* an internal bounded wait gave up                 */
 
-/* Size in bytes of the workspace one verify/commit pair needs.  It holds the
- * pseudo-values U fp32 [B][T][H][dv], the cumulative log gates
- * l fp32 [B][T][H] (l_i = sum of log g over path(i)), node depths int32
+/* Size in bytes of the workspace one verify/commit pair needs, for HV value
+ * heads.  It holds the pseudo-values U fp32 [B][T][HV][dv], the cumulative
+ * log gates l fp32 [B][T][HV] (l_i = sum of log g over path(i)), node depths int32
  * [B][T], the strict-ancestor bitmask uint32 [B][T][ceil(T/32)], the DFS
  * pre-order int32 [B][T], the device error word, and the scratch of the fp32
  * path.  Returns 0 for unsupported sizes. */
-size_t canopy_workspace_bytes(int B, int T, int H, int dk, int dv);
+size_t canopy_workspace_bytes(int B, int T, int HV, int dk, int dv);
 
 /* Zero the workspace (including the error word); call once after allocating
  * it.  Enqueued on `stream`. */
@@ -96,9 +102,9 @@ canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream)
  * writes depth, the strict-ancestor bitmask, the DFS pre-order and the
  * cumulative log gates l into the workspace.  The verify entry point does the
  * same work inside its own kernels; this call exposes it on its own.
- *   parent device int32 [B][T]; g device fp32 [B][T][H]. */
+ *   parent device int32 [B][T]; g device fp32 [B][T][HV]. */
 canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
-                               int T, int B, int H, void* workspace, void* stream);
+                               int T, int B, int HV, void* workspace, void* stream);
 
 /* Closed-form tree verify (canopy page, "The tree closed form"):
  *   A_ij = [j in A(i)] exp(l_i - l_j) k_i.k_j,  C_ij = [j in path(i)] exp(l_i - l_j) q_i.k_j
@@ -123,8 +129,8 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
  * CANOPY_ERR_ARG. */
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                  const float* g, const float* beta, const float* S0,
-                                 const int32_t* parent, int T, int B, int H, int dk, int dv,
-                                 canopy_solve solve, void* o, canopy_dtype o_dtype,
+                                 const int32_t* parent, int T, int B, int H, int HV, int dk, int dv,
+                                 float scale, canopy_solve solve, void* o, canopy_dtype o_dtype,
                                  void* workspace, unsigned flags, void* stream);
 
 /* Commit (canopy page, "The tree closed form", last line, and "What the
@@ -142,15 +148,16 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
  * the commit then requests its S0 tiles, walks the accepted path and stages
  * its k rows while that kernel finishes; the workspace and S_new are touched
  * only after it has completed.  Other bits return CANOPY_ERR_ARG.
- *   accepted device int32 [B]; S0, S_new device fp32 [B][H][dv][dk];
+ *   accepted device int32 [B]; S0, S_new device fp32 [B][HV][dv][dk];
  *   k device [B][T][H][dk] in in_dtype; parent device int32 [B][T]. */
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new,
                             const void* k, const int32_t* parent, canopy_dtype in_dtype, int T, int B,
-                            int H, int dk, int dv, const void* workspace, unsigned flags, void* stream);
+                            int H, int HV, int dk, int dv, const void* workspace, unsigned flags,
+                            void* stream);
 
-/* Bytes of the per-node snapshot buffer of the serial replay:
- * fp32 [B][T][H][dv][dk]. */
-size_t canopy_snapshot_bytes(int B, int T, int H, int dk, int dv);
+/* Bytes of the per-node snapshot buffer of the serial replay for HV value
+ * heads: fp32 [B][T][HV][dv][dk]. */
+size_t canopy_snapshot_bytes(int B, int T, int HV, int dk, int dv);
 
 /* Serial parent-pointer replay, the crossover opponent (canopy page,
  * "Design decisions", serial baseline: SGLang's snapshot path).  For each
@@ -161,8 +168,8 @@ size_t canopy_snapshot_bytes(int B, int T, int H, int dk, int dv);
  * canopy_snapshot_bytes(); workspace receives only the error word. */
 canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                    const float* g, const float* beta, const float* S0,
-                                   const int32_t* parent, int T, int B, int H, int dk, int dv,
-                                   void* o, canopy_dtype o_dtype, void* snapshot,
+                                   const int32_t* parent, int T, int B, int H, int HV, int dk, int dv,
+                                   float scale, void* o, canopy_dtype o_dtype, void* snapshot,
                                    void* workspace, void* stream);
 
 /* Serial replay for callers that cannot allocate device memory.  The paper
@@ -176,8 +183,8 @@ canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, 
  *     snapshot argument.  err is an optional device int32 (may be NULL):
  *     device-side input errors (CANOPY_DEVERR_*) are OR-ed into it, so zero
  *     it before the call if you read it afterwards.
- *   - Limit: B*T*H*dk*dv*4 <= 33,554,176 bytes (32 MiB less 256 bytes), e.g.
- *     B=1, T=31, H=16 at dk=dv=128; larger calls return
+ *   - Limit: B*T*HV*dk*dv*4 <= 33,554,176 bytes (32 MiB less 256 bytes), e.g.
+ *     B=1, T=31, HV=16 at dk=dv=128; larger calls return
  *     CANOPY_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up the array's address there
  *     (cudaGetSymbolAddress, with that device current); make that first call
@@ -188,8 +195,9 @@ canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, 
  *   - Calls no cudaMalloc, cudaFree or allocating library routine. */
 canopy_status canopy_serial_replay_static(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                           const float* g, const float* beta, const float* S0,
-                                          const int32_t* parent, int T, int B, int H, int dk, int dv,
-                                          void* o, canopy_dtype o_dtype, int32_t* err, void* stream);
+                                          const int32_t* parent, int T, int B, int H, int HV, int dk,
+                                          int dv, float scale, void* o, canopy_dtype o_dtype, int32_t* err,
+                                          void* stream);
 
 /* Synchronise `stream`, copy the device error word to *err_out and clear it.
  * Returns CANOPY_ERR_CUDA if the stream reported an error. */

@@ -30,16 +30,16 @@ def to_device(inp, bf16: bool):
     return d
 
 
-def oracle_outputs(inp, keep_states=False):
+def oracle_outputs(inp, keep_states=False, scale=1.0):
     return oracle.replay_batch(inp["parent"], inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
-                               inp["S0"], keep_states=keep_states)
+                               inp["S0"], keep_states=keep_states, scale=scale)
 
 
-def run_verify(canopy, dev, solve="fwdsub", o_dtype=torch.float32, ws=None):
-    B, T, H, d = dev["q"].shape
+def run_verify(canopy, dev, solve="fwdsub", o_dtype=torch.float32, ws=None, scale=1.0):
+    B, T, HV, d = dev["v"].shape
     if ws is None:
-        ws = canopy.workspace(B, T, H, d)
+        ws = canopy.workspace(B, T, HV, d)
     o = canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
-                      solve=solve, o_dtype=o_dtype)
+                      solve=solve, o_dtype=o_dtype, scale=scale)
     err = canopy.read_device_error(ws)
     return o, ws, err

@@ -220,3 +220,65 @@ def test_inputs_ready_overlap_back_to_back(lib, state_ready):
         assert lib.read_device_error(dev["ws"]) == 0
     o_ref, _ = oracle_outputs(sets[0][0])
     assert rel_err(outs[0].cpu().numpy(), o_ref) <= TOL_BF16
+
+
+def _gva_inputs(T, fam, H, HV, bf16=True, B=2, seed=0):
+    """q and k for H key heads, v, g, beta and S0 for HV value heads (the
+    canopy page's grouped value attention layout)."""
+    rng = np.random.default_rng(seed + 131 * T)
+    parents = [trees.family(fam, T, rng) for _ in range(B)]
+    ik = synth.make_inputs(parents, H, 128, 128, bf16, case=92, rnd=seed)
+    iv = synth.make_inputs(parents, HV, 128, 128, bf16, case=93, rnd=seed)
+    return dict(iv, q=ik["q"], k=ik["k"])
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("T,fam", [(16, "top4"), (64, "random"), (100, "chain"), (256, "random")])
+def test_grouped_value_heads_and_scale(lib, T, fam, bf16):
+    """HV = 2H value heads on H key heads and the FLA scale 1/sqrt(dk) on q:
+    o and, through the commit, the accepted state match the oracle."""
+    H, HV = 2, 4
+    inp = _gva_inputs(T, fam, H, HV, bf16)
+    sc = 1.0 / np.sqrt(128.0)
+    o_ref, S_ref = oracle_outputs(inp, keep_states=True, scale=sc)
+    dev = to_device(inp, bf16)
+    o, ws, err = run_verify(lib, dev, scale=sc)
+    assert err == 0
+    tol = TOL_BF16 if bf16 else TOL_F32
+    assert rel_err(o.cpu().numpy(), o_ref) <= tol
+    acc = torch.tensor([T - 1, T // 2], dtype=torch.int32, device="cuda")
+    Sn = lib.commit(acc, dev["S0"], dev["k"], dev["parent"], ws)
+    assert lib.read_device_error(ws) == 0
+    ref = np.stack([S_ref[0, T - 1], S_ref[1, T // 2]])
+    assert rel_err(Sn.cpu().numpy(), ref) <= tol
+
+
+@pytest.mark.parametrize("T", [8, 64])
+def test_grouped_value_heads_neumann_and_serial(lib, T):
+    H, HV = 1, 4
+    inp = _gva_inputs(T, "top2", H, HV, True, seed=1)
+    sc = 0.5
+    o_ref, _ = oracle_outputs(inp, scale=sc)
+    dev = to_device(inp, True)
+    on, _, err = run_verify(lib, dev, solve="neumann", scale=sc)
+    assert err == 0
+    assert rel_err(on.cpu().numpy(), o_ref) <= TOL_BF16
+    ws = lib.workspace(2, T, HV, 128)
+    os_ = lib.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
+                            scale=sc)
+    assert lib.read_device_error(ws) == 0
+    assert rel_err(os_.cpu().numpy(), o_ref) <= TOL_F32
+    if T <= 16:  # the library's fixed snapshot array holds 32 MiB
+        ost = lib.serial_replay_static(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"],
+                                       dev["parent"], scale=sc)
+        assert torch.equal(ost, os_)
+
+
+def test_grouped_value_heads_bad_shapes_refused(lib):
+    inp = _gva_inputs(16, "top4", 2, 4, True)
+    dev = to_device(inp, True)
+    ws = lib.workspace(2, 16, 4, 128)
+    v3 = dev["v"][:, :, :3].contiguous()
+    with pytest.raises(lib.CanopyError):
+        lib.verify(dev["q"], dev["k"], v3, dev["g"][:, :, :3].contiguous(), dev["beta"][:, :, :3].contiguous(),
+                   dev["S0"][:, :3].contiguous(), dev["parent"], ws)

@@ -46,6 +46,6 @@ def test_static_serial_rejects_sizes_beyond_its_array(lib):
     L = lib.load()
     p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
     # 1 x 32 x 16 states of 128 x 128 fp32 = 32 MiB: over the limit, refused on the host
-    st = L.canopy_serial_replay_static(p[0], p[1], p[2], 1, p[3], p[4], p[5], p[6], 32, 1, 16, 128, 128,
-                                       p[7], 0, None, None)
+    st = L.canopy_serial_replay_static(p[0], p[1], p[2], 1, p[3], p[4], p[5], p[6], 32, 1, 16, 16, 128, 128,
+                                       1.0, p[7], 0, None, None)
     assert st == 3
