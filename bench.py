@@ -497,6 +497,83 @@ def run_sweep(args):
         out.close()
 
 
+def run_layer_shape(args):
+    """One GDN layer at the shape the canopy page gives for Qwen3.5-9B (16 key
+    heads, 32 value heads of 128 x 128, scale 1/sqrt(128) on q), for the
+    batch-1 (4, 2, 1) tree of 16 nodes and for random trees of 64 nodes at
+    batch 1 and 16: median (p10, p90) us of the verify alone, of verify +
+    commit, and of the serial replay, each timed alone after an L2 flush."""
+    import torch
+
+    import synth
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    from synth import configs, trees
+    bld.build()
+    canopy.load()
+    H, HV, d = 16, 32, 128
+    scale = 1.0 / np.sqrt(d)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    for B, T, fam in ((1, 16, "schedule421"), (1, 64, "random"), (16, 64, "random")):
+        rng = np.random.default_rng(7000 + 100 * B + T)
+        parents = [configs.make_tree(fam, T, rng) for _ in range(B)]
+        ik = synth.make_inputs(parents, H, d, d, True, case=94, rnd=T)
+        iv = synth.make_inputs(parents, HV, d, d, True, case=95, rnd=T)
+        dev = {"q": torch.from_numpy(ik["q"]).to("cuda", torch.bfloat16),
+               "k": torch.from_numpy(ik["k"]).to("cuda", torch.bfloat16),
+               "v": torch.from_numpy(iv["v"]).to("cuda", torch.bfloat16)}
+        for n in ("g", "beta", "S0"):
+            dev[n] = torch.from_numpy(iv[n]).cuda()
+        dev["parent"] = torch.from_numpy(iv["parent"]).cuda()
+        rng2 = np.random.default_rng(B * T)
+        dev["acc"] = torch.tensor([int(rng2.choice(trees.leaves(p))) for p in parents], dtype=torch.int32,
+                                  device="cuda")
+        ws = canopy.workspace(B, T, HV, d)
+        snap = torch.empty(canopy.snapshot_bytes(B, T, HV, d), dtype=torch.uint8, device="cuda")
+        o = torch.empty((B, T, HV, d), dtype=torch.float32, device="cuda")
+        S_new = torch.empty_like(dev["S0"])
+
+        def ver():
+            canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
+                          out=o, scale=scale)
+
+        def step():
+            ver()
+            canopy.commit(dev["acc"], dev["S0"], dev["k"], dev["parent"], ws, out=S_new)
+
+        def ser():
+            canopy.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
+                                 snapshot=snap, out=o, scale=scale)
+
+        calls = {"verify": ver, "verify_commit": step, "serial": ser}
+        times = {k: [] for k in calls}
+        for it in range(args.sweep_warmup + args.sweep_reps):
+            for name, fn in calls.items():
+                flush.fill_(float(it))
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                if it >= args.sweep_warmup:
+                    times[name].append((a, b))
+        torch.cuda.synchronize()
+        assert canopy.read_device_error(ws) == 0
+        rec = {"layer": "H=16 key heads, HV=32 value heads, dk=dv=128, scale 1/sqrt(128)", "B": B, "T": T,
+               "tree": fam, "depth": int(max(trees.tree_depth(p) for p in parents))}
+        for name, evs in times.items():
+            us = [1e3 * a.elapsed_time(b) for a, b in evs]
+            rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
+                         "p90": float(np.percentile(us, 90))}
+        rec["speedup_verify"] = rec["serial"]["p50"] / rec["verify"]["p50"]
+        line = json.dumps(rec)
+        print(line, flush=True)
+        if out:
+            out.write(line + "\n")
+    if out:
+        out.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,6 +588,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="crossover map vs the serial replay kernel")
+    ap.add_argument("--layer-shape", action="store_true",
+                    help="one GDN layer at 16 key / 32 value heads with the 1/sqrt(dk) q scale")
     ap.add_argument("--sweep-b", default="")
     ap.add_argument("--sweep-t", default="")
     ap.add_argument("--sweep-fam", default="")
@@ -518,6 +597,9 @@ def main():
     ap.add_argument("--sweep-warmup", type=int, default=10)
     ap.add_argument("--sweep-out", default="")
     args = ap.parse_args()
+    if args.layer_shape:
+        run_layer_shape(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -100,8 +100,8 @@ struct Params {
     uint32_t* mask;
     int32_t* err;
     int B, T, H, W, o_bf16;
-    int HK;       // key heads: value head h reads q and k of key head h / (H / HK)
-    float scale;  // factor on q (applied to o)
+    int ratio;    // value heads per key head: value head h reads q and k of key head h / ratio
+    float scale;  // factor on q: folded into gamma of the X_Q columns and into the M rows
     int inputs_ready;  // the inputs other than S0 may be read before the preceding kernel completes
     int state_ready;   // with inputs_ready: S0 too
 };
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(NT, 2)
         *sNmax = 0;
         // Q and K next: the solve path waits on them
         mbar_expect_tx(&bars[BAR_QK], 4 * 64 * 64 * 2);
-        const int hk = h / (H / p.HK);
+        const int hk = (p.ratio == 1) ? h : h / p.ratio;
         tma_load_4d(sQK + 0, &tmQ, &bars[BAR_QK], 0, hk, 0, b);
         tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, hk, 0, b);
         tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, hk, 0, b);
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(NT, 2)
             const int i = tid;
             sL2[i] = myl2;  // every walk has read the per-node gates by now
             const float gm = exp2f(myl2);
-            sGam[i] = gm;
+            sGam[i] = p.scale * gm;  // o = scale (gamma X_Q + M R): the X_Q columns' factor
             sBG[i] = make_float2(sBeta[i], sBeta[i] * gm);  // zero for padded nodes
             if (i < T) {
                 int d = 0;
@@ -411,9 +411,10 @@ __global__ void __launch_bounds__(NT, 2)
                 *reinterpret_cast<uint4*>(bh + ((c ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4*>(bl + ((c ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
             }
+            const float msc = qrow ? p.scale : 1.f;  // M rows carry the scale on q, W rows do not
             for (int d = 0; d < n; ++d) {
                 const int j = pl[d];
-                const float x = xr[d];
+                const float x = msc * xr[d];
                 const uint32_t hb = hi_bits(x);
                 const int off = ((((j >> 3) ^ (r & 7))) << 4) + ((j & 7) << 1);
                 *reinterpret_cast<uint16_t*>(bh + off) = uint16_t(hb >> 16);
@@ -589,7 +590,6 @@ __global__ void __launch_bounds__(NT, 2)
         float* tile = reinterpret_cast<float*>(sm + (solve ? L::OT : L::UT));
         __nv_bfloat16* tile16 = reinterpret_cast<__nv_bfloat16*>(sm + L::OT);
         const bool o16 = solve && p.o_bf16;
-        const float sc = solve ? p.scale : 1.f;  // o carries the scale on q, U does not
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
             uint32_t y[16];
@@ -598,10 +598,10 @@ __global__ void __launch_bounds__(NT, 2)
             if (o16) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    tile16[(blk * 16 + e) * DV + c] = __float2bfloat16_rn(sc * __uint_as_float(y[e]));
+                    tile16[(blk * 16 + e) * DV + c] = __float2bfloat16_rn(__uint_as_float(y[e]));
             } else {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) tile[(blk * 16 + e) * DV + c] = sc * __uint_as_float(y[e]);
+                for (int e = 0; e < 16; ++e) tile[(blk * 16 + e) * DV + c] = __uint_as_float(y[e]);
             }
         }
         fence_proxy_async_smem();
@@ -662,7 +662,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
     prm.H = H;
     prm.W = ws.W;
     prm.o_bf16 = o_bf16;
-    prm.HK = HK;
+    prm.ratio = H / HK;
     prm.scale = scale;
     prm.inputs_ready = inputs_ready;
     prm.state_ready = inputs_ready && state_ready;
