@@ -574,6 +574,30 @@ def run_layer_shape(args):
         out.close()
 
 
+def run_memory(args):
+    """Transient memory of one tree verify per GDN layer and sequence at the
+    canopy page's model shape (32 value heads of 128 x 128), for the serial
+    replay's per-node snapshots and for this library: the pseudo-values and
+    log gates the commit reads, and the whole workspace as allocated (with
+    the T x T scratch of the paths beyond 64 nodes).  Host arithmetic through
+    the library's own size functions; no GPU needed."""
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    bld.build()
+    canopy.load()
+    HV, d, layers = 32, 128, 24
+    mib = float(1 << 20)
+    for T in (16, 64, 100, 128, 256):
+        snap = canopy.snapshot_bytes(1, T, HV, d)
+        ws = canopy.workspace_bytes(1, T, HV, d)
+        factors = T * HV * d * 4 + T * HV * 4          # U and l, what the commit reads
+        rec = {"per": "one GDN layer, one sequence (HV=32 value heads, dk=dv=128)", "T": T,
+               "snapshots_MiB": snap / mib, "U_and_l_MiB": factors / mib, "workspace_MiB": ws / mib,
+               "ratio_snapshots_to_U_and_l": snap / factors, "ratio_snapshots_to_workspace": snap / ws,
+               "all_24_layers": {"snapshots_MiB": layers * snap / mib, "workspace_MiB": layers * ws / mib}}
+        print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -588,6 +612,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="crossover map vs the serial replay kernel")
+    ap.add_argument("--memory", action="store_true",
+                    help="transient memory per layer: serial snapshots vs this library's workspace")
     ap.add_argument("--layer-shape", action="store_true",
                     help="one GDN layer at 16 key / 32 value heads with the 1/sqrt(dk) q scale")
     ap.add_argument("--sweep-b", default="")
@@ -597,6 +623,9 @@ def main():
     ap.add_argument("--sweep-warmup", type=int, default=10)
     ap.add_argument("--sweep-out", default="")
     args = ap.parse_args()
+    if args.memory:
+        run_memory(args)
+        return
     if args.layer_shape:
         run_layer_shape(args)
         return
