@@ -27,6 +27,7 @@ Modules
                level-synchronous), fp64, plus an fp32 twin and the naive-ratio
                twin used by the stability pin
   commit       the accepted node's state from the pseudo-values
+  conv         the tree-aware short causal convolution and its state commit
 
 Pins (tests/test_oracle_*.py, run with -m "not gpu"): chain = sequential
 recurrence; brute force on every tree of at most 8 nodes; closed form = replay
@@ -52,3 +53,4 @@ from .closed_form import (  # noqa: F401
     SOLVERS,
 )
 from .commit import commit, commit_batch  # noqa: F401
+from .conv import tree_conv, tree_conv_batch, conv_commit, conv_commit_batch  # noqa: F401
