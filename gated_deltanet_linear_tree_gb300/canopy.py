@@ -24,6 +24,7 @@ DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 VERIFY_INPUTS_READY = 0x1
 VERIFY_STATE_READY = 0x2
 COMMIT_STATE_READY = 0x1
+ACT = {"none": 0, "silu": 1}
 
 # name -> (restype, argtypes); mirrors include/canopy.h
 _P, _I, _S, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
@@ -39,6 +40,8 @@ SIGNATURES = {
                                   _P]),
     "canopy_serial_replay_static": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P,
                                          _P]),
+    "canopy_tree_conv": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "canopy_conv_commit": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "canopy_read_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "canopy_status_string": (ctypes.c_char_p, [_I]),
     "canopy_version": (_I, []),
@@ -222,6 +225,51 @@ def serial_replay_static(q, k, v, g, beta, S0, parent, err=None, o_dtype=torch.f
                                             _ptr(parent), T, B, H, HV, dk, dv, float(scale), _ptr(out), _dt(out),
                                             errp, _stream())
     _check(st, "canopy_serial_replay_static")
+    return out
+
+
+def tree_conv(x, conv_state, weight, parent, bias=None, act: str = "silu", err=None, out=None):
+    """Tree-aware short causal convolution: y [B, T, C] in x's dtype.
+    x [B, T, C] (bf16 or fp32); conv_state fp32 [B, C, K-1]; weight fp32
+    [C, K]; bias fp32 [C] or None; parent int32 [B, T]; err an optional int32
+    CUDA tensor of one element that receives device error bits (OR-ed)."""
+    _need(x, "x")
+    B, T, C = x.shape
+    _need(weight, "weight", torch.float32)
+    if weight.dim() != 2 or weight.shape[0] != C:
+        raise CanopyError(f"weight must have shape ({C}, K), got {tuple(weight.shape)}")
+    K = weight.shape[1]
+    _need(conv_state, "conv_state", torch.float32, (B, C, K - 1))
+    _need(parent, "parent", torch.int32, (B, T))
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (C,))
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "y", x.dtype, x.shape)
+    st = load().canopy_tree_conv(_ptr(x), _dt(x), _ptr(conv_state), _ptr(weight),
+                                 _ptr(bias) if bias is not None else None, _ptr(parent), T, B, C, K, ACT[act],
+                                 _ptr(out), _ptr(err) if err is not None else None, _stream())
+    _check(st, "canopy_tree_conv")
+    return out
+
+
+def conv_commit(accepted, x, parent, conv_state, out=None, err=None):
+    """The convolution state after accepting node accepted[b] of every
+    stream's tree: [B, C, K-1] fp32 (out may be conv_state itself)."""
+    _need(x, "x")
+    B, T, C = x.shape
+    _need(conv_state, "conv_state", torch.float32)
+    if conv_state.dim() != 3 or conv_state.shape[:2] != (B, C):
+        raise CanopyError(f"conv_state must have shape ({B}, {C}, K-1), got {tuple(conv_state.shape)}")
+    K = conv_state.shape[2] + 1
+    _need(accepted, "accepted", torch.int32, (B,))
+    _need(parent, "parent", torch.int32, (B, T))
+    if out is None:
+        out = torch.empty_like(conv_state)
+    _need(out, "conv_state_new", torch.float32, conv_state.shape)
+    st = load().canopy_conv_commit(_ptr(accepted), _ptr(x), _dt(x), _ptr(parent), _ptr(conv_state), _ptr(out), T, B,
+                                   C, K, _ptr(err) if err is not None else None, _stream())
+    _check(st, "canopy_conv_commit")
     return out
 
 

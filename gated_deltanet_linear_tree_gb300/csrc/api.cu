@@ -27,6 +27,12 @@ cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const 
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
                           const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
                           int d, void* o, int o_bf16, float scale, float* snap, int32_t* err, cudaStream_t st);
+cudaError_t launch_tree_conv(const void* x, int bf16, const float* state, const float* w, const float* bias,
+                             const int32_t* parent, int T, int B, int C, int K, int silu, void* y, int32_t* err,
+                             cudaStream_t st);
+cudaError_t launch_conv_commit(const int32_t* accepted, const void* x, int bf16, const int32_t* parent,
+                               const float* state, float* state_new, int T, int B, int C, int K, int32_t* err,
+                               cudaStream_t st);
 }  // namespace canopy
 
 using namespace canopy;
@@ -137,6 +143,33 @@ canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, 
     return cuda_status(launch_serial(q, k, v, in_dtype == CANOPY_BF16, g, beta, S0, parent, T, B, HV, H, dk, o,
                                      o_dtype == CANOPY_BF16, scale, static_cast<float*>(snapshot), ws.err,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+canopy_status canopy_tree_conv(const void* x, canopy_dtype dtype, const float* conv_state, const float* weight,
+                               const float* bias, const int32_t* parent, int T, int B, int C, int K,
+                               canopy_activation act, void* y, int32_t* err, void* stream) {
+    if (!aligned16(x) || !aligned16(conv_state) || !aligned16(weight) || !aligned16(parent) || !aligned16(y) ||
+        (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) || (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
+        return CANOPY_ERR_ARG;
+    if ((dtype != CANOPY_F32 && dtype != CANOPY_BF16) || (act != CANOPY_ACT_NONE && act != CANOPY_ACT_SILU))
+        return CANOPY_ERR_ARG;
+    if (B <= 0 || T <= 0 || C <= 0 || K < 2) return CANOPY_ERR_ARG;
+    if (T > kMaxT || K > 8 || C % 4 != 0) return CANOPY_ERR_UNSUPPORTED;
+    return cuda_status(launch_tree_conv(x, dtype == CANOPY_BF16, conv_state, weight, bias, parent, T, B, C, K,
+                                        act == CANOPY_ACT_SILU, y, err, static_cast<cudaStream_t>(stream)));
+}
+
+canopy_status canopy_conv_commit(const int32_t* accepted, const void* x, canopy_dtype dtype, const int32_t* parent,
+                                 const float* conv_state, float* conv_state_new, int T, int B, int C, int K,
+                                 int32_t* err, void* stream) {
+    if (!aligned16(accepted) || !aligned16(x) || !aligned16(parent) || !aligned16(conv_state) ||
+        !aligned16(conv_state_new) || (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
+        return CANOPY_ERR_ARG;
+    if (dtype != CANOPY_F32 && dtype != CANOPY_BF16) return CANOPY_ERR_ARG;
+    if (B <= 0 || T <= 0 || C <= 0 || K < 2) return CANOPY_ERR_ARG;
+    if (T > kMaxT || K > 8 || C % 4 != 0) return CANOPY_ERR_UNSUPPORTED;
+    return cuda_status(launch_conv_commit(accepted, x, dtype == CANOPY_BF16, parent, conv_state, conv_state_new, T,
+                                          B, C, K, err, static_cast<cudaStream_t>(stream)));
 }
 
 canopy_status canopy_read_device_error(void* workspace, int32_t* err_out, void* stream) {

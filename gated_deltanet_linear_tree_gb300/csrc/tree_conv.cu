@@ -1,0 +1,215 @@
+// Tree-aware short causal convolution and its state commit.
+//
+// canopy page (projects.dotslasha.me/p/canopy.md), "M7: Benchmarks, the
+// crossover, and the stretch goal": the short causal convolution (kernel 4)
+// before each GDN layer follows each node's root path, and commit updates
+// the convolution state with the accepted tokens.  Depthwise, per channel c:
+//     y_i[c] = act(bias[c] + sum_j w[c][j] X(i, K-1-j)[c]),
+// X(i, m) the input m steps up i's root path, or the committed state once
+// the path has passed the root.  Memory bound: one CTA per (stream, block of
+// 4 NT channels), four channels per thread (8- or 16-byte loads, coalesced
+// across the warp); the window walks the sanitised parent array in shared
+// memory, the state and the weights of the thread's channels stay in
+// registers.
+#include "common.cuh"
+
+namespace canopy {
+
+namespace conv {
+
+constexpr int NT = 256;
+
+__device__ inline void load4c(const float* p, float (&v)[4]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ inline void load4c(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+__device__ inline void store4c(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ inline void store4c(__nv_bfloat16* p, const float (&v)[4]) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2*>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
+// The stream's parents into shared memory, sanitised as the verify does (a
+// parent outside [0, i) reads as 0, the root's as -1); a bad tree is
+// reported once per stream.
+__device__ inline void load_parents(const int32_t* parent, int b, int T, int* sPar, int32_t* err, bool report) {
+    int bad = 0;
+    for (int i = threadIdx.x; i < T; i += NT) {
+        int p = parent[size_t(b) * T + i];
+        if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) {
+            bad = CANOPY_DEVERR_TREE;
+            p = (i == 0) ? -1 : 0;
+        }
+        sPar[i] = p;
+    }
+    if (bad && report && err) raise_err(err, bad);
+}
+
+template <typename T_, int K>
+__global__ void __launch_bounds__(NT) tree_conv_kernel(const T_* __restrict__ x, const float* __restrict__ state,
+                                                       const float* __restrict__ w, const float* __restrict__ bias,
+                                                       const int32_t* __restrict__ parent, int T, int C, int silu,
+                                                       T_* __restrict__ y, int32_t* err) {
+    __shared__ int sPar[kMaxT];
+    const int b = blockIdx.y;
+    const int c0 = 4 * (blockIdx.x * NT + threadIdx.x);
+    load_parents(parent, b, T, sPar, err, blockIdx.x == 0);
+    __syncthreads();
+    if (c0 >= C) return;
+    // weights, bias and committed state of this thread's four channels
+    float wv[K][4], sv[K - 1][4], bv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        bv[e] = bias ? bias[c0 + e] : 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) wv[j][e] = w[(c0 + e) * K + j];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) sv[j][e] = state[(size_t(b) * C + c0 + e) * (K - 1) + j];
+    }
+    for (int i = 0; i < T; ++i) {
+        float acc[4] = {bv[0], bv[1], bv[2], bv[3]};
+        // taps m = 0 .. K-1 (weight K-1-m) walk up the root path; once the
+        // walk has passed the root after n path nodes, tap m reads the state
+        // entry K-2-(m-n) (the newest first)
+        int node = i, n = 0;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+            float v[4];
+            if (node >= 0) {
+                load4c(x + (size_t(b) * T + node) * C + c0, v);
+                node = sPar[node];
+                ++n;
+            } else {
+                const int s = K - 2 - (m - n);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = 0.f;
+#pragma unroll
+                for (int ss = 0; ss < K - 1; ++ss)
+                    if (ss == s)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[e] = sv[ss][e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += wv[K - 1 - m][e] * v[e];
+        }
+        if (silu) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = acc[e] / (1.f + __expf(-acc[e]));
+        }
+        store4c(y + (size_t(b) * T + i) * C + c0, acc);
+    }
+}
+
+template <typename T_, int K>
+__global__ void __launch_bounds__(NT) conv_commit_kernel(const int32_t* __restrict__ accepted, const T_* __restrict__ x,
+                                                         const int32_t* __restrict__ parent, const float* state,
+                                                         float* state_new, int T, int C, int32_t* err) {
+    __shared__ int sPar[kMaxT];
+    const int b = blockIdx.y;
+    const int c0 = 4 * (blockIdx.x * NT + threadIdx.x);
+    load_parents(parent, b, T, sPar, nullptr, false);
+    __syncthreads();
+    if (c0 >= C) return;
+    int a = accepted[b];
+    if (a < -1 || a >= T) {
+        if (err && c0 == 0) raise_err(err, CANOPY_DEVERR_ACCEPTED);
+        a = -1;
+    }
+    float old[K - 1][4], nw[K - 1][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) old[j][e] = state[(size_t(b) * C + c0 + e) * (K - 1) + j];
+    // newest first (position K - 2 - m): the accepted path from a up to the
+    // root, then the old state from its newest entry
+    int node = a, n = 0;  // n: path nodes used
+#pragma unroll
+    for (int m = 0; m < K - 1; ++m) {
+        if (node >= 0) {
+            float v[4];
+            load4c(x + (size_t(b) * T + node) * C + c0, v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) nw[K - 2 - m][e] = v[e];
+            node = sPar[node];
+            ++n;
+        } else {
+            const int s = K - 2 - (m - n);
+#pragma unroll
+            for (int ss = 0; ss < K - 1; ++ss)
+                if (ss == s)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) nw[K - 2 - m][e] = old[ss][e];
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) state_new[(size_t(b) * C + c0 + e) * (K - 1) + j] = nw[j][e];
+}
+
+}  // namespace conv
+
+template <typename T_, int K>
+static void tree_conv_typed(dim3 grid, const void* x, const float* state, const float* w, const float* bias,
+                            const int32_t* parent, int T, int C, int silu, void* y, int32_t* err, cudaStream_t st) {
+    conv::tree_conv_kernel<T_, K><<<grid, conv::NT, 0, st>>>(static_cast<const T_*>(x), state, w, bias, parent, T,
+                                                            C, silu, static_cast<T_*>(y), err);
+}
+
+template <typename T_, int K>
+static void conv_commit_typed(dim3 grid, const int32_t* accepted, const void* x, const int32_t* parent,
+                              const float* state, float* state_new, int T, int C, int32_t* err, cudaStream_t st) {
+    conv::conv_commit_kernel<T_, K><<<grid, conv::NT, 0, st>>>(accepted, static_cast<const T_*>(x), parent, state,
+                                                              state_new, T, C, err);
+}
+
+cudaError_t launch_tree_conv(const void* x, int bf16, const float* state, const float* w, const float* bias,
+                             const int32_t* parent, int T, int B, int C, int K, int silu, void* y, int32_t* err,
+                             cudaStream_t st) {
+    dim3 grid((C / 4 + conv::NT - 1) / conv::NT, B);
+#define CANOPY_CONV(KK)                                                                              \
+    case KK:                                                                                         \
+        if (bf16)                                                                                    \
+            tree_conv_typed<__nv_bfloat16, KK>(grid, x, state, w, bias, parent, T, C, silu, y, err, st); \
+        else                                                                                         \
+            tree_conv_typed<float, KK>(grid, x, state, w, bias, parent, T, C, silu, y, err, st);         \
+        break;
+    switch (K) {
+        CANOPY_CONV(2) CANOPY_CONV(3) CANOPY_CONV(4) CANOPY_CONV(5) CANOPY_CONV(6) CANOPY_CONV(7) CANOPY_CONV(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef CANOPY_CONV
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_commit(const int32_t* accepted, const void* x, int bf16, const int32_t* parent,
+                               const float* state, float* state_new, int T, int B, int C, int K, int32_t* err,
+                               cudaStream_t st) {
+    dim3 grid((C / 4 + conv::NT - 1) / conv::NT, B);
+#define CANOPY_CCOMMIT(KK)                                                                                \
+    case KK:                                                                                              \
+        if (bf16)                                                                                         \
+            conv_commit_typed<__nv_bfloat16, KK>(grid, accepted, x, parent, state, state_new, T, C, err, st); \
+        else                                                                                              \
+            conv_commit_typed<float, KK>(grid, accepted, x, parent, state, state_new, T, C, err, st);         \
+        break;
+    switch (K) {
+        CANOPY_CCOMMIT(2) CANOPY_CCOMMIT(3) CANOPY_CCOMMIT(4) CANOPY_CCOMMIT(5) CANOPY_CCOMMIT(6)
+        CANOPY_CCOMMIT(7) CANOPY_CCOMMIT(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef CANOPY_CCOMMIT
+    return cudaGetLastError();
+}
+
+}  // namespace canopy

@@ -155,6 +155,38 @@ canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_n
                             int H, int HV, int dk, int dv, const void* workspace, unsigned flags,
                             void* stream);
 
+/* Activation after the short convolution. */
+typedef enum { CANOPY_ACT_NONE = 0, CANOPY_ACT_SILU = 1 } canopy_activation;
+
+/* Tree-aware short causal convolution (canopy page, "M7: Benchmarks, the
+ * crossover, and the stretch goal": the kernel-4 convolution before each
+ * GDN layer follows each node's root path).  Per stream b, node i and
+ * channel c, with a_0(i) = i, a_m(i) = parent(a_{m-1}(i)) and depth(i) the
+ * number of edges from the root:
+ *   y_i[c] = act(bias[c] + sum_{j=0..K-1} w[c][j] X(i, K-1-j)[c]),
+ *   X(i, m) = x_{a_m(i)} for m <= depth(i), else
+ *             conv_state[c][K-1-(m-depth(i))] (the committed inputs before
+ *             the root, [K-2] the newest).
+ *   x, y device [B][T][C] in dtype (bf16 or fp32; fp32 arithmetic);
+ *   conv_state device fp32 [B][C][K-1]; weight device fp32 [C][K]; bias
+ *   device fp32 [C] or NULL; parent device int32 [B][T] (sanitised as the
+ *   verify sanitises it; a bad tree sets CANOPY_DEVERR_TREE in *err).
+ *   2 <= K <= 8; C a multiple of 4; err an optional device int32 (OR-ed).
+ * Enqueued on `stream`; no allocation. */
+canopy_status canopy_tree_conv(const void* x, canopy_dtype dtype, const float* conv_state, const float* weight,
+                               const float* bias, const int32_t* parent, int T, int B, int C, int K,
+                               canopy_activation act, void* y, int32_t* err, void* stream);
+
+/* Convolution-state commit (same passage: commit updates the convolution
+ * state with the accepted tokens): for accepted node a = accepted[b] the new
+ * state is the last K-1 inputs of (conv_state ++ x over path(a), root
+ * first); a = -1 keeps the state, a outside [-1, T) sets
+ * CANOPY_DEVERR_ACCEPTED in *err and keeps it.  conv_state_new may alias
+ * conv_state.  Shapes as in canopy_tree_conv; accepted device int32 [B]. */
+canopy_status canopy_conv_commit(const int32_t* accepted, const void* x, canopy_dtype dtype, const int32_t* parent,
+                                 const float* conv_state, float* conv_state_new, int T, int B, int C, int K,
+                                 int32_t* err, void* stream);
+
 /* Bytes of the per-node snapshot buffer of the serial replay for HV value
  * heads: fp32 [B][T][HV][dv][dk]. */
 size_t canopy_snapshot_bytes(int B, int T, int HV, int dk, int dv);

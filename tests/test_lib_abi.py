@@ -91,6 +91,19 @@ def test_host_argument_errors(lib):
     assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], 1, 64, 1, 4, 6, 128, 128, good[4], 0,
                              None) == 1
     assert lib.canopy_tree_prep(good[0], good[1], 0, 1, 1, good[2], None) == 3
+    # tree convolution (x, dtype, state, weight, bias, parent, T, B, C, K, act, y, err): every case is
+    # refused on the host before a launch
+    assert lib.canopy_tree_conv(None, 1, good[1], good[2], None, good[3], 16, 2, 64, 4, 1, good[4], None, None) == 1
+    assert lib.canopy_tree_conv(good[0], 1, good[1], good[2], None, good[3], 16, 2, 64, 4, 7, good[4], None,
+                                None) == 1                                          # bad activation
+    assert lib.canopy_tree_conv(good[0], 1, good[1], good[2], None, good[3], 16, 2, 62, 4, 1, good[4], None,
+                                None) == 3                                          # C not a multiple of 4
+    assert lib.canopy_tree_conv(good[0], 1, good[1], good[2], None, good[3], 16, 2, 64, 9, 1, good[4], None,
+                                None) == 3                                          # K > 8
+    assert lib.canopy_tree_conv(good[0], 1, good[1], good[2], None, good[3], 16, 2, 64, 1, 1, good[4], None,
+                                None) == 1                                          # K < 2
+    assert lib.canopy_conv_commit(good[0], good[1], 1, good[2], good[3], good[4], 300, 2, 64, 4, None, None) == 3
+    assert lib.canopy_conv_commit(good[0], None, 1, good[2], good[3], good[4], 16, 2, 64, 4, None, None) == 1
     err = ctypes.c_int32(0)
     assert lib.canopy_read_device_error(None, ctypes.byref(err), None) == 1
     assert lib.canopy_workspace_init(None, 16, None) == 1
