@@ -443,7 +443,9 @@ def run_sweep(args):
     bld.build()
     canopy.load()
     H, d = 16, 128
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    # 1 GiB: larger than L2, and long enough (about 0.15 ms) that the host has
+    # queued the timed call before the GPU reaches it
+    flush = torch.empty(1024 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     Bs = [int(x) for x in args.sweep_b.split(",")] if args.sweep_b else configs.SWEEP_B
     Ts = [int(x) for x in args.sweep_t.split(",")] if args.sweep_t else configs.SWEEP_T
     fams = args.sweep_fam.split(",") if args.sweep_fam else configs.SWEEP_FAMILIES
@@ -513,7 +515,9 @@ def run_layer_shape(args):
     canopy.load()
     H, HV, d = 16, 32, 128
     scale = 1.0 / np.sqrt(d)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    # 1 GiB: larger than L2, and long enough (about 0.15 ms) that the host has
+    # queued the timed call before the GPU reaches it
+    flush = torch.empty(1024 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     out = open(args.sweep_out, "w") if args.sweep_out else None
     for B, T, fam in ((1, 16, "schedule421"), (1, 64, "random"), (16, 64, "random")):
         rng = np.random.default_rng(7000 + 100 * B + T)
@@ -546,7 +550,17 @@ def run_layer_shape(args):
             canopy.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
                                  snapshot=snap, out=o, scale=scale)
 
-        calls = {"verify": ver, "verify_commit": step, "serial": ser}
+        # the short convolution before the layer over q, k and v channels
+        C = 2 * H * d + HV * d
+        xc = torch.randn((B, T, C), device="cuda").to(torch.bfloat16)
+        cst = torch.randn((B, C, 3), device="cuda")
+        cw = 0.5 * torch.randn((C, 4), device="cuda")
+        yc = torch.empty_like(xc)
+
+        def conv():
+            canopy.tree_conv(xc, cst, cw, dev["parent"], act="silu", out=yc)
+
+        calls = {"verify": ver, "verify_commit": step, "serial": ser, "tree_conv": conv}
         times = {k: [] for k in calls}
         for it in range(args.sweep_warmup + args.sweep_reps):
             for name, fn in calls.items():
@@ -566,6 +580,9 @@ def run_layer_shape(args):
             rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
                          "p90": float(np.percentile(us, 90))}
         rec["speedup_verify"] = rec["serial"]["p50"] / rec["verify"]["p50"]
+        conv_bytes = 2 * B * T * C * 2 + B * C * 3 * 4 + C * 4 * 4
+        rec["tree_conv_channels"] = C
+        rec["tree_conv_GBps"] = conv_bytes / (rec["tree_conv"]["p50"] * 1e3)
         line = json.dumps(rec)
         print(line, flush=True)
         if out:

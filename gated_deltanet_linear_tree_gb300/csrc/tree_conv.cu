@@ -7,10 +7,10 @@
 //     y_i[c] = act(bias[c] + sum_j w[c][j] X(i, K-1-j)[c]),
 // X(i, m) the input m steps up i's root path, or the committed state once
 // the path has passed the root.  Memory bound: one CTA per (stream, block of
-// 4 NT channels), four channels per thread (8- or 16-byte loads, coalesced
-// across the warp); the window walks the sanitised parent array in shared
-// memory, the state and the weights of the thread's channels stay in
-// registers.
+// CB channels) stages the stream's whole block of x (T rows of CB channels)
+// and its parents in shared memory in one round of coalesced loads, then
+// eight node lanes of 32 threads (four channels each) read every tap from
+// shared memory and write y coalesced.
 #include "common.cuh"
 
 namespace canopy {
@@ -29,6 +29,13 @@ __device__ inline void load4c(const __nv_bfloat16* p, float (&v)[4]) {
     v[1] = __uint_as_float(w.x & 0xFFFF0000u);
     v[2] = __uint_as_float(w.y << 16);
     v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+// Four elements' bits, unchanged (8 bytes of bf16 or 16 of fp32).
+__device__ inline void copy4c(__nv_bfloat16* d, const __nv_bfloat16* s) {
+    *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(s);
+}
+__device__ inline void copy4c(float* d, const float* s) {
+    *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(s);
 }
 __device__ inline void store4c(float* p, const float (&v)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
@@ -55,38 +62,52 @@ __device__ inline void load_parents(const int32_t* parent, int b, int T, int* sP
     if (bad && report && err) raise_err(err, bad);
 }
 
+constexpr int CB = 128;            // channels per CTA of the convolution
+constexpr int CT = CB / 4;         // channel threads (four channels each)
+constexpr int NL = NT / CT;        // node lanes
+
+__host__ __device__ constexpr size_t conv_smem(int T, int es) { return size_t(T) * CB * es + size_t(T) * 4; }
+
 template <typename T_, int K>
 __global__ void __launch_bounds__(NT) tree_conv_kernel(const T_* __restrict__ x, const float* __restrict__ state,
                                                        const float* __restrict__ w, const float* __restrict__ bias,
                                                        const int32_t* __restrict__ parent, int T, int C, int silu,
                                                        T_* __restrict__ y, int32_t* err) {
-    __shared__ int sPar[kMaxT];
-    const int b = blockIdx.y;
-    const int c0 = 4 * (blockIdx.x * NT + threadIdx.x);
+    extern __shared__ __align__(16) uint8_t conv_smem_raw[];
+    T_* sX = reinterpret_cast<T_*>(conv_smem_raw);                         // [T][CB]
+    int* sPar = reinterpret_cast<int*>(conv_smem_raw + size_t(T) * CB * sizeof(T_));
+    const int b = blockIdx.y, cb0 = blockIdx.x * CB;
+    const int ct = threadIdx.x % CT, nl = threadIdx.x / CT;  // channel thread, node lane
+    const int c = cb0 + 4 * ct;                              // first of this thread's four channels
+    const bool live = c < C;
+    // the stream's block of x (all rows, this CTA's channels), its parents
+    // (sanitised), and this thread's weights, bias and committed state: one
+    // round of independent loads
+    if (live)
+        for (int r = nl; r < T; r += NL) copy4c(sX + size_t(r) * CB + 4 * ct, x + (size_t(b) * T + r) * C + c);
     load_parents(parent, b, T, sPar, err, blockIdx.x == 0);
-    __syncthreads();
-    if (c0 >= C) return;
-    // weights, bias and committed state of this thread's four channels
     float wv[K][4], sv[K - 1][4], bv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        bv[e] = bias ? bias[c0 + e] : 0.f;
+        bv[e] = (live && bias) ? bias[c + e] : 0.f;
 #pragma unroll
-        for (int j = 0; j < K; ++j) wv[j][e] = w[(c0 + e) * K + j];
+        for (int j = 0; j < K; ++j) wv[j][e] = live ? w[(c + e) * K + j] : 0.f;
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j) sv[j][e] = state[(size_t(b) * C + c0 + e) * (K - 1) + j];
+        for (int j = 0; j < K - 1; ++j) sv[j][e] = live ? state[(size_t(b) * C + c + e) * (K - 1) + j] : 0.f;
     }
-    for (int i = 0; i < T; ++i) {
+    __syncthreads();
+    if (!live) return;
+    // taps m = 0 .. K-1 (weight K-1-m) walk up i's root path in shared
+    // memory; once the walk has passed the root after n path nodes, tap m
+    // reads the state entry K-2-(m-n), the newest first
+    for (int i = nl; i < T; i += NL) {
         float acc[4] = {bv[0], bv[1], bv[2], bv[3]};
-        // taps m = 0 .. K-1 (weight K-1-m) walk up the root path; once the
-        // walk has passed the root after n path nodes, tap m reads the state
-        // entry K-2-(m-n) (the newest first)
         int node = i, n = 0;
 #pragma unroll
         for (int m = 0; m < K; ++m) {
             float v[4];
             if (node >= 0) {
-                load4c(x + (size_t(b) * T + node) * C + c0, v);
+                load4c(sX + size_t(node) * CB + 4 * ct, v);
                 node = sPar[node];
                 ++n;
             } else {
@@ -104,9 +125,9 @@ __global__ void __launch_bounds__(NT) tree_conv_kernel(const T_* __restrict__ x,
         }
         if (silu) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = acc[e] / (1.f + __expf(-acc[e]));
+            for (int e = 0; e < 4; ++e) acc[e] = __fdividef(acc[e], 1.f + __expf(-acc[e]));
         }
-        store4c(y + (size_t(b) * T + i) * C + c0, acc);
+        store4c(y + (size_t(b) * T + i) * C + c, acc);
     }
 }
 
@@ -160,10 +181,20 @@ __global__ void __launch_bounds__(NT) conv_commit_kernel(const int32_t* __restri
 }  // namespace conv
 
 template <typename T_, int K>
-static void tree_conv_typed(dim3 grid, const void* x, const float* state, const float* w, const float* bias,
-                            const int32_t* parent, int T, int C, int silu, void* y, int32_t* err, cudaStream_t st) {
-    conv::tree_conv_kernel<T_, K><<<grid, conv::NT, 0, st>>>(static_cast<const T_*>(x), state, w, bias, parent, T,
-                                                            C, silu, static_cast<T_*>(y), err);
+static cudaError_t tree_conv_typed(dim3 grid, const void* x, const float* state, const float* w, const float* bias,
+                                   const int32_t* parent, int T, int C, int silu, void* y, int32_t* err,
+                                   cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(conv::tree_conv_kernel<T_, K>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(conv::conv_smem(kMaxT, sizeof(T_))));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    conv::tree_conv_kernel<T_, K><<<grid, conv::NT, conv::conv_smem(T, sizeof(T_)), st>>>(
+        static_cast<const T_*>(x), state, w, bias, parent, T, C, silu, static_cast<T_*>(y), err);
+    return cudaGetLastError();
 }
 
 template <typename T_, int K>
@@ -176,20 +207,16 @@ static void conv_commit_typed(dim3 grid, const int32_t* accepted, const void* x,
 cudaError_t launch_tree_conv(const void* x, int bf16, const float* state, const float* w, const float* bias,
                              const int32_t* parent, int T, int B, int C, int K, int silu, void* y, int32_t* err,
                              cudaStream_t st) {
-    dim3 grid((C / 4 + conv::NT - 1) / conv::NT, B);
-#define CANOPY_CONV(KK)                                                                              \
-    case KK:                                                                                         \
-        if (bf16)                                                                                    \
-            tree_conv_typed<__nv_bfloat16, KK>(grid, x, state, w, bias, parent, T, C, silu, y, err, st); \
-        else                                                                                         \
-            tree_conv_typed<float, KK>(grid, x, state, w, bias, parent, T, C, silu, y, err, st);         \
-        break;
+    dim3 grid((C + conv::CB - 1) / conv::CB, B);
+#define CANOPY_CONV(KK)                                                                                        \
+    case KK:                                                                                                   \
+        return bf16 ? tree_conv_typed<__nv_bfloat16, KK>(grid, x, state, w, bias, parent, T, C, silu, y, err, st) \
+                    : tree_conv_typed<float, KK>(grid, x, state, w, bias, parent, T, C, silu, y, err, st);
     switch (K) {
         CANOPY_CONV(2) CANOPY_CONV(3) CANOPY_CONV(4) CANOPY_CONV(5) CANOPY_CONV(6) CANOPY_CONV(7) CANOPY_CONV(8)
         default: return cudaErrorInvalidValue;
     }
 #undef CANOPY_CONV
-    return cudaGetLastError();
 }
 
 cudaError_t launch_conv_commit(const int32_t* accepted, const void* x, int bf16, const int32_t* parent,
