@@ -27,6 +27,9 @@ cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const 
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
                           const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
                           int d, void* o, int o_bf16, float scale, float* snap, int32_t* err, cudaStream_t st);
+cudaError_t launch_path_replay(const void* q, const void* k, const void* v, int in_bf16, const float* g,
+                               const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
+                               int d, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 cudaError_t launch_tree_conv(const void* x, int bf16, const float* state, const float* w, const float* bias,
                              const int32_t* parent, int T, int B, int C, int K, int silu, void* y, int32_t* err,
                              cudaStream_t st);
@@ -42,6 +45,19 @@ namespace {
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool sizes_ok(int B, int T, int H) { return B >= 1 && H >= 1 && T >= 1 && T <= kMaxT; }
+
+// Dispatch below the crossover (canopy page, "Design decisions": the serial
+// path below it, the closed form above): replaying each node's root path
+// from S0 beats the closed form's fixed chain of stages for single-node
+// trees, and for two- and three-node trees while there are few (stream,
+// value head) pairs to spread over the GPU.  Measured on GB300 at 16 value
+// heads (us, replay vs closed form): T = 2: 8.2 vs 12.5 at one stream, 16.2
+// vs 16.4 at sixteen; T = 3: 10.2 vs 12.3 at one stream, about 19 vs 16.4 at
+// sixteen; the cut-offs interpolate between the two.
+bool path_replay_wins(int T, int B, int HV) {
+    const size_t units = size_t(B) * HV;
+    return T == 1 || (T == 2 && units <= 128) || (T == 3 && units <= 64);
+}
 
 // key heads H, value heads HV: HV a positive multiple of H
 bool heads_ok(int H, int HV) { return H >= 1 && HV >= H && HV % H == 0; }
@@ -93,6 +109,9 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
     const bool tc = in_bf16 && dk == 128 && T <= 64;
     if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
+    if (solve == CANOPY_SOLVE_FWDSUB && path_replay_wins(T, B, HV))
+        return cuda_status(launch_path_replay(q, k, v, in_bf16, g, beta, S0, parent, T, B, HV, H, dk, o, o_bf16,
+                                              scale, ws, st));
     if (tc && solve == CANOPY_SOLVE_NEUMANN)
         return cuda_status(
             launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));

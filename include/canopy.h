@@ -113,6 +113,10 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
  * Writes o (device, o_dtype) and, into the workspace, U, l, depth, mask.
  * in_dtype CANOPY_BF16 selects the tensor-core path (tcgen05, bf16 operands,
  * fp32 accumulation); CANOPY_F32 selects the fp32 path.  S0 is read only.
+ * With solve = CANOPY_SOLVE_FWDSUB, trees below the measured crossover (one
+ * node; two nodes with B * HV <= 128; three with B * HV <= 64) are verified by replaying
+ * each node's root path from S0 in fp32 instead (same outputs and workspace
+ * contents; canopy page, "Design decisions": serial below the crossover).
  * flags: 0, or CANOPY_VERIFY_INPUTS_READY, optionally with
  * CANOPY_VERIFY_STATE_READY.  The tensor-core forward-substitution kernel is
  * launched with programmatic dependent launch and may begin while the kernel

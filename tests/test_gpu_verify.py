@@ -282,3 +282,22 @@ def test_grouped_value_heads_bad_shapes_refused(lib):
     with pytest.raises(lib.CanopyError):
         lib.verify(dev["q"], dev["k"], v3, dev["g"][:, :, :3].contiguous(), dev["beta"][:, :, :3].contiguous(),
                    dev["S0"][:, :3].contiguous(), dev["parent"], ws)
+
+
+@pytest.mark.parametrize("B,HV", [(2, 4), (16, 16)])
+@pytest.mark.parametrize("T,fam", [(1, "chain"), (2, "chain"), (3, "top2"), (3, "chain")])
+def test_tiny_trees_both_sides_of_the_dispatch(lib, B, HV, T, fam):
+    """Below the crossover (one node, or up to three with few stream-head
+    pairs) the verify replays root paths; above it, the closed form: both
+    give the oracle's o, and the commit after either gives its state."""
+    inp = _gva_inputs(T, fam, 2, HV, True, B=B, seed=3)
+    sc = 0.25
+    o_ref, S_ref = oracle_outputs(inp, keep_states=True, scale=sc)
+    dev = to_device(inp, True)
+    o, ws, err = run_verify(lib, dev, scale=sc)
+    assert err == 0
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_BF16
+    acc = torch.full((B,), T - 1, dtype=torch.int32, device="cuda")
+    Sn = lib.commit(acc, dev["S0"], dev["k"], dev["parent"], ws)
+    assert lib.read_device_error(ws) == 0
+    assert rel_err(Sn.cpu().numpy(), S_ref[:, T - 1]) <= TOL_BF16
