@@ -499,6 +499,77 @@ def run_sweep(args):
         out.close()
 
 
+def run_solve_table(args):
+    """The solve strategies side by side (canopy page, "Design decisions":
+    blocked forward substitution, the Neumann series, the squaring form and
+    the split design; DFS against level order): for B in {1, 16}, each tree
+    family at T = 256 (or --sweep-t) under DFS pre-order and under level
+    order, median (p10, p90) µs of every strategy's verify call, timed alone
+    after an L2 flush, the strategies interleaved; the serial replay beside
+    them for scale."""
+    import torch
+
+    import synth
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    from synth import trees
+    bld.build()
+    canopy.load()
+    H, d = 16, 128
+    flush = torch.empty(1024 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    Bs = [int(x) for x in args.sweep_b.split(",")] if args.sweep_b else [1, 16]
+    Ts = [int(x) for x in args.sweep_t.split(",")] if args.sweep_t else [256]
+    fams = args.sweep_fam.split(",") if args.sweep_fam else ["top8", "top4", "top2", "random", "skewed", "chain"]
+    out = open(args.sweep_out, "w") if args.sweep_out else None
+    for B in Bs:
+        for T in Ts:
+            for fam in fams:
+                rng = np.random.default_rng(1000 * B + T)
+                base = [trees.family(fam, T, rng) for _ in range(B)]
+                for order_name, order_fn in (("dfs", trees.dfs_preorder), ("level", trees.level_order)):
+                    parents = [trees.relabel(p, order_fn(p)) for p in base]
+                    inp = synth.make_inputs(parents, H, d, d, True, case=3, rnd=T)
+                    dev = {n: torch.from_numpy(inp[n]).to("cuda", torch.bfloat16) for n in ("q", "k", "v")}
+                    for n in ("g", "beta", "S0"):
+                        dev[n] = torch.from_numpy(inp[n]).cuda()
+                    dev["parent"] = torch.from_numpy(inp["parent"]).cuda()
+                    ws = canopy.workspace(B, T, H, d)
+                    snap = torch.empty(canopy.snapshot_bytes(B, T, H, d), dtype=torch.uint8, device="cuda")
+                    o = torch.empty((B, T, H, d), dtype=torch.float32, device="cuda")
+                    calls = {"serial": lambda: canopy.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"],
+                                                                    dev["beta"], dev["S0"], dev["parent"], ws,
+                                                                    snapshot=snap, out=o)}
+                    for sv in ("fwdsub", "neumann", "squaring", "split"):
+                        calls[sv] = (lambda sv=sv: canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"],
+                                                                 dev["beta"], dev["S0"], dev["parent"], ws,
+                                                                 solve=sv, out=o))
+                    times = {k: [] for k in calls}
+                    for it in range(args.sweep_warmup + args.sweep_reps):
+                        for name, fn in calls.items():
+                            flush.fill_(float(it))
+                            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            a.record()
+                            fn()
+                            b.record()
+                            if it >= args.sweep_warmup:
+                                times[name].append((a, b))
+                    torch.cuda.synchronize()
+                    assert canopy.read_device_error(ws) == 0
+                    rec = {"B": B, "T": T, "family": fam, "order": order_name,
+                           "depth": int(max(trees.tree_depth(p) for p in parents))}
+                    for name, evs in times.items():
+                        us = [1e3 * a.elapsed_time(b) for a, b in evs]
+                        rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
+                                     "p90": float(np.percentile(us, 90))}
+                    line = json.dumps(rec)
+                    print(line, flush=True)
+                    if out:
+                        out.write(line + "\n")
+                    del ws, snap, o, dev
+    if out:
+        out.close()
+
+
 def run_layer_shape(args):
     """One GDN layer at the shape the canopy page gives for Qwen3.5-9B (16 key
     heads, 32 value heads of 128 x 128, scale 1/sqrt(128) on q), for the
@@ -633,6 +704,8 @@ def main():
                     help="transient memory per layer: serial snapshots vs this library's workspace")
     ap.add_argument("--layer-shape", action="store_true",
                     help="one GDN layer at 16 key / 32 value heads with the 1/sqrt(dk) q scale")
+    ap.add_argument("--solve-table", action="store_true",
+                    help="solve strategies and DFS vs level order side by side (T = 256 by default)")
     ap.add_argument("--sweep-b", default="")
     ap.add_argument("--sweep-t", default="")
     ap.add_argument("--sweep-fam", default="")
@@ -648,6 +721,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.solve_table:
+        run_solve_table(args)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

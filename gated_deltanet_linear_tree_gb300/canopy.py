@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libcanopy.so")
 
 OK, ERR_ARG, ERR_TREE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
-SOLVE = {"fwdsub": 0, "neumann": 1}
+SOLVE = {"fwdsub": 0, "neumann": 1, "squaring": 2, "split": 3}
 DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 VERIFY_INPUTS_READY = 0x1
 VERIFY_STATE_READY = 0x2
@@ -147,7 +147,8 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
            inputs_ready: bool = False, state_ready: bool = False, scale: float = 1.0):
     """o [B, T, HV, dv] for every node of every stream's tree; q and k carry
     H key heads, v, g, beta and S0 HV value heads (a multiple of H), and
-    scale multiplies q.  inputs_ready: q, k, v, g, beta and parent are not
+    scale multiplies q.  solve: "fwdsub" (every size and dtype), or
+    "neumann", "squaring", "split" (bf16 q/k/v, dk = dv = 128).  inputs_ready: q, k, v, g, beta and parent are not
     written by the kernel launched just before this call on the current
     stream (CANOPY_VERIFY_INPUTS_READY); state_ready (with inputs_ready): nor
     is S0 (CANOPY_VERIFY_STATE_READY)."""

@@ -30,6 +30,8 @@ cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf
 cudaError_t launch_path_replay(const void* q, const void* k, const void* v, int in_bf16, const float* g,
                                const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
                                int d, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
+cudaError_t launch_solve_variant(int variant, int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws,
+                                 cudaStream_t st);
 cudaError_t launch_tree_conv(const void* x, int bf16, const float* state, const float* w, const float* bias,
                              const int32_t* parent, int T, int B, int C, int K, int silu, void* y, int32_t* err,
                              cudaStream_t st);
@@ -99,7 +101,8 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         !aligned16(parent) || !aligned16(o) || !aligned16(workspace))
         return CANOPY_ERR_ARG;
     if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
-        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN) ||
+        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN && solve != CANOPY_SOLVE_SQUARING &&
+         solve != CANOPY_SOLVE_SPLIT) ||
         (flags & ~(CANOPY_VERIFY_INPUTS_READY | CANOPY_VERIFY_STATE_READY)) || !std::isfinite(scale))
         return CANOPY_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
@@ -108,19 +111,26 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     Ws ws = ws_bind(workspace, B, T, HV, dv);
     const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
     const bool tc = in_bf16 && dk == 128 && T <= 64;
-    if (solve == CANOPY_SOLVE_NEUMANN && !tc) return CANOPY_ERR_UNSUPPORTED;
+    // the solve variants run on the tensor-core Gram's tiles (bf16, d = 128)
+    if (solve != CANOPY_SOLVE_FWDSUB && !(in_bf16 && dk == 128)) return CANOPY_ERR_UNSUPPORTED;
     if (solve == CANOPY_SOLVE_FWDSUB && path_replay_wins(T, B, HV))
         return cuda_status(launch_path_replay(q, k, v, in_bf16, g, beta, S0, parent, T, B, HV, H, dk, o, o_bf16,
                                               scale, ws, st));
     if (tc && solve == CANOPY_SOLVE_NEUMANN)
         return cuda_status(
             launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
-    if (tc)
+    if (tc && solve == CANOPY_SOLVE_FWDSUB)
         return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws,
                                                 (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
                                                 (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
     cudaError_t e = launch_tree_prep(parent, g, T, B, HV, ws, 0, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
+    if (solve != CANOPY_SOLVE_FWDSUB) {
+        // Neumann beyond 64 nodes, squaring and split: Gram tiles, then the solve
+        e = launch_gram_tc(q, k, v, beta, S0, T, B, HV, H, ws, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        return cuda_status(launch_solve_variant(int(solve), T, B, HV, o, o_bf16, scale, ws, st));
+    }
     // bf16 inputs beyond one 64-node block: the Gram products on tcgen05
     const bool gram_tc = in_bf16 && dk == 128 && T > 64;
     if (gram_tc) {

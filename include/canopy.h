@@ -63,10 +63,17 @@ typedef enum {
 typedef enum { CANOPY_F32 = 0, CANOPY_BF16 = 1 } canopy_dtype;
 
 /* Solve strategy for (I + diag(beta) A) U = R (canopy page, "Design
- * decisions", two solve strategies behind one interface). */
+ * decisions", solve strategies behind one interface, and "The tree closed
+ * form", nilpotency and squaring).  FWDSUB takes every size and dtype; the
+ * other three take bf16 q/k/v with dk = dv = 128 only (else
+ * CANOPY_ERR_UNSUPPORTED) and never take the path-replay dispatch below. */
 typedef enum {
-    CANOPY_SOLVE_FWDSUB = 0,   /* blocked forward substitution, 64-node blocks   */
-    CANOPY_SOLVE_NEUMANN = 1   /* finite Neumann series, d rounds (Bole's solve) */
+    CANOPY_SOLVE_FWDSUB = 0,   /* blocked forward substitution, 64-node blocks            */
+    CANOPY_SOLVE_NEUMANN = 1,  /* finite Neumann series, d rounds (Bole's solve)          */
+    CANOPY_SOLVE_SQUARING = 2, /* (I - G)(I + G^2)(I + G^4)..., ceil(log2(d + 1)) factors  */
+    CANOPY_SOLVE_SPLIT = 3     /* (I + G)^-1 once per (stream, value head) in the
+                                  workspace, then applied per 64-node block and 64 value
+                                  columns (two launches)                                  */
 } canopy_solve;
 
 /* Flags of canopy_tree_verify. */

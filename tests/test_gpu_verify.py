@@ -88,13 +88,6 @@ def test_neumann_variant(lib, fam, T):
     assert rel_err(Sn.cpu().numpy(), S_ref[:, T - 1]) <= TOL_BF16
 
 
-def test_neumann_unsupported_beyond_64(lib):
-    inp = _inputs(65, "random")
-    dev = to_device(inp, bf16=True)
-    with pytest.raises(lib.CanopyError):
-        run_verify(lib, dev, solve="neumann")
-
-
 @pytest.mark.parametrize("fam", ["chain", "top4", "random"])
 @pytest.mark.parametrize("T", [1, 3, 17, 64, 65, 256])
 def test_shapes_fp32(lib, fam, T):

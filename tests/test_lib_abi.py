@@ -74,6 +74,10 @@ def test_host_argument_errors(lib):
     assert _verify(lib, good, d=64) == 3                            # unsupported head size
     assert _verify(lib, good, in_dt=7) == 1                         # bad enum
     assert _verify(lib, good, solve=5) == 1
+    assert _verify(lib, good, solve=4) == 1
+    for solve in (1, 2, 3):                                         # variants: bf16 and d = 128 only
+        assert _verify(lib, good, solve=solve, in_dt=0) == 3
+        assert _verify(lib, good, solve=solve, d=32) == 3
     assert _verify(lib, good, flags=4) == 1                         # unknown flag
     assert _verify(lib, good, flags=8) == 1
     assert _verify(lib, good, H=2, HV=3) == 1                       # value heads not a multiple of key heads
