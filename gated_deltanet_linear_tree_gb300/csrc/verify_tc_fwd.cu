@@ -20,10 +20,10 @@
 //   state warps 4-7:  S0 rows -> bf16 hi + lo in tensor memory (the A
 //       operand); X^T = S0 [Q;K]^T on tcgen05 (value columns on the TMEM
 //       lanes, nodes on the columns); R^T = beta (V - gamma X_K)^T as bf16
-//       hi + lo into tensor memory; the X_Q columns scaled by gamma.
-// Then Y^T = [gamma X_Q^T | 0] + R^T [M; W]^T by three bf16 products
-// (hi*hi + hi*lo + lo*hi, ~15 mantissa bits each side), and each warp stores
-// 32 value columns of o (warps 0-3) or U (warps 4-7) for every node.
+//       hi + lo into tensor memory.
+// Then R^T [M; W]^T by three bf16 products (hi*hi + hi*lo + lo*hi, ~15
+// mantissa bits each side), and each warp stores 32 value columns of
+// o = gamma X_Q + M R (warps 0-3) or U = W R (warps 4-7) for every node.
 // Decay ratios are only ever 2^(l2_i - l2_j) with j on i's root path, so they
 // lie in (0, 1] and never overflow ("Hard constraints", log-space gates).
 #include "common.cuh"
@@ -39,8 +39,10 @@ constexpr int XS = 68;        // row stride (floats) of the work vectors and Gp:
 constexpr int XS_SHORT = 36;  // the same for paths of up to 33 nodes (depth <= 32)
 constexpr uint32_t kTmemCols = 256;
 // tensor-memory columns
-constexpr uint32_t TA = 0;      // S0 as A: hi [0,64), lo [64,128); later R^T: hi [0,32), lo [32,64)
-constexpr uint32_t TD = 128;    // AC [128,192) first; then X^T / Y^T [128,256): o part [128,192), U part [192,256)
+constexpr uint32_t TA = 0;      // S0 as A: hi [0,64), lo [64,128); later R^T: hi [0,32), lo [32,64), and
+                                // the output product's o part R^T M^T at [64,128)
+constexpr uint32_t TD = 128;    // AC [128,192) first; then X^T [128,256): Q part [128,192), K part
+                                // [192,256), the latter overwritten by the U part R^T W^T
 
 struct Smem {
     static constexpr int QK = 0;                 // [Q;K] bf16, 2 atoms x 128 rows x 128 B; later [M;W] hi/lo
@@ -68,18 +70,12 @@ struct Smem {
     static constexpr int BG = BAR + 128;         // float2[64] (beta, beta gamma)
     static constexpr int PLIST = BG + 512;       // u8[64][64] path(i) from the root down
     static constexpr int TOTAL = PLIST + TP * TP;
-    // after the output product: o and U tiles [64 nodes][128 columns] for the
-    // TMA stores, clear of the [M; W] operand (the U product still reads it
-    // while the o tile is written)
-    static constexpr int UT = 32768;
-    static constexpr int OT = 65536;
     // the S0 tile (fp32, 4 boxes of [128 rows][32 columns], 128-byte
     // swizzle) passes through a two-box staging area, one slot per box;
     // V and the long-stride tables reuse it once it has been converted
     static constexpr int S0S = 32768;
     static constexpr int S0_BOX = 128 * 128;
     static_assert(S0S + 2 * S0_BOX <= XV_SHORT && S0S % 1024 == 0, "S0 staging");
-    static_assert(UT + TP * DV * 4 <= OT && OT + TP * DV * 4 <= PAR, "output tiles overlap");
     static_assert(XV % 16 == 0 && GP % 16 == 0 && BAR % 256 == 0 && BG % 16 == 0 && GAM % 16 == 0, "align");
     static_assert(NMAX + 4 <= BG, "small arrays overlap");
     static_assert(GP_SHORT + TP * XS_SHORT * 4 <= PAR, "short tables overlap the small arrays");
@@ -156,8 +152,7 @@ __device__ __forceinline__ void r_pass(int hb, const uint8_t* sm, const float2* 
 
 __global__ void __launch_bounds__(NT, 2)
     verify_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                      const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmS,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
                       Params p) {
     using L = Smem;
     extern __shared__ uint8_t smem_raw[];
@@ -524,30 +519,13 @@ __global__ void __launch_bounds__(NT, 2)
         }
         __syncwarp();
 
-        // ---- R^T = beta (V - gamma X_K)^T and gamma X_Q^T ---------------------
+        // ---- R^T = beta (V - gamma X_K)^T ---------------------------------------
         wait_or_flag(&bars[BAR_X], sFlag);
         wait_or_flag(&bars[BAR_V], sFlag);
         wait_or_flag(&bars[BAR_PREP], sFlag);
         tc_fence_after();
         {
             r_pass(0, sm, sBG, lane_base, c);
-#pragma unroll 1
-            for (int hb = 0; hb < 2; ++hb) {
-                uint32_t xq[32];
-                tmem_ld16(lane_base + TD + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
-                tmem_ld16(lane_base + TD + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
-                tmem_wait_ld();
-#pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 gm = *reinterpret_cast<const float4*>(sGam + hb * 32 + 4 * e4);
-                    xq[4 * e4] = __float_as_uint(gm.x * __uint_as_float(xq[4 * e4]));
-                    xq[4 * e4 + 1] = __float_as_uint(gm.y * __uint_as_float(xq[4 * e4 + 1]));
-                    xq[4 * e4 + 2] = __float_as_uint(gm.z * __uint_as_float(xq[4 * e4 + 2]));
-                    xq[4 * e4 + 3] = __float_as_uint(gm.w * __uint_as_float(xq[4 * e4 + 3]));
-                }
-                tmem_st16(lane_base + TD + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
-                tmem_st16(lane_base + TD + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
-            }
             r_pass(1, sm, sBG, lane_base, c);
             tmem_wait_st();
         }
@@ -555,15 +533,16 @@ __global__ void __launch_bounds__(NT, 2)
     }
     __syncthreads();
 
-    // ---- Y^T = [gamma X_Q^T | 0] + R^T [M; W]^T (bf16 x3) -------------------------
-    // o columns first, with their own commit: the o tile is written and
-    // stored while the U product runs.
+    // ---- R^T [M; W]^T (bf16 x3): o part into the free S0 columns, U part
+    // over X_K -------------------------------------------------------------------
+    // o columns first, with their own commit: o (gamma X_Q added in the
+    // epilogue) is stored while the U product runs.
     if (tid == 128) {
         tc_fence_after();
         const uint32_t bH = smem_u32(sm + L::BH), bL = smem_u32(sm + L::BL);
 #pragma unroll 1
         for (int part = 0; part < 2; ++part) {        // 0: o (M rows), 1: U (W rows)
-            const uint32_t d = tmem + TD + part * 64;
+            const uint32_t d = tmem + (part ? TD + 64 : TA + 64);
             const uint32_t rowoff = part * 64 * 128;
 #pragma unroll 1
             for (int pass = 0; pass < 3; ++pass) {    // hi*hi, hi*lo, lo*hi
@@ -572,7 +551,7 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ts(d, tmem + acol + ks * 8, sdesc_sw128(bb + ks * 32), idesc_bf16(128, 64),
-                                (part == 0) || pass != 0 || ks != 0);
+                                pass != 0 || ks != 0);
             }
             mma_commit(&bars[part ? BAR_YU : BAR_Y]);
         }
@@ -581,40 +560,55 @@ __global__ void __launch_bounds__(NT, 2)
     wait_or_flag(&bars[solve ? BAR_Y : BAR_YU], sFlag);
     tc_fence_after();
 
-    // ---- store: warps 0-3 o, warps 4-7 U (lane = value column) into shared
-    // tiles [node][column], then one TMA store per warp group (rows past T
-    // clipped) ---
+    // ---- store: warps 0-3 o = gamma X_Q + R^T M^T, warps 4-7 U (lane = value
+    // column), straight from the accumulator columns: per node row a warp
+    // writes 32 consecutive columns (128 bytes of fp32, 64 of bf16); rows past
+    // T are not written.  Writes wait until the preceding kernel has
+    // completed. ---
     {
         const int c = quad * 32 + lane;
-        const uint32_t col0 = TD + (solve ? 0 : 64);
-        float* tile = reinterpret_cast<float*>(sm + (solve ? L::OT : L::UT));
-        __nv_bfloat16* tile16 = reinterpret_cast<__nv_bfloat16*>(sm + L::OT);
-        const bool o16 = solve && p.o_bf16;
+        const uint32_t col0 = solve ? TA + 64 : TD + 64;
+        const size_t rstride = size_t(H) * DV;  // one node row of o or U
+        const size_t base = (size_t(b) * T * H + h) * DV + c;
+        pdl_wait();
 #pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-            uint32_t y[16];
-            tmem_ld16(lane_base + col0 + blk * 16, y);
-            tmem_wait_ld();
-            if (o16) {
+        for (int half = 0; half < 2; ++half) {
+            uint32_t y[32];
+            tmem_ld16(lane_base + col0 + half * 32, *reinterpret_cast<uint32_t(*)[16]>(y));
+            tmem_ld16(lane_base + col0 + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(y + 16));
+            const int e0 = half * 32;
+            if (solve) {
+                uint32_t xq[32];
+                tmem_ld16(lane_base + TD + half * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
+                tmem_ld16(lane_base + TD + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
+                tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    tile16[(blk * 16 + e) * DV + c] = __float2bfloat16_rn(__uint_as_float(y[e]));
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    // sGam carries the scale on q
+                    const float4 gm = *reinterpret_cast<const float4*>(sGam + e0 + 4 * e4);
+                    y[4 * e4] = __float_as_uint(fmaf(gm.x, __uint_as_float(xq[4 * e4]), __uint_as_float(y[4 * e4])));
+                    y[4 * e4 + 1] =
+                        __float_as_uint(fmaf(gm.y, __uint_as_float(xq[4 * e4 + 1]), __uint_as_float(y[4 * e4 + 1])));
+                    y[4 * e4 + 2] =
+                        __float_as_uint(fmaf(gm.z, __uint_as_float(xq[4 * e4 + 2]), __uint_as_float(y[4 * e4 + 2])));
+                    y[4 * e4 + 3] =
+                        __float_as_uint(fmaf(gm.w, __uint_as_float(xq[4 * e4 + 3]), __uint_as_float(y[4 * e4 + 3])));
+                }
             } else {
+                tmem_wait_ld();
+            }
+            if (solve && p.o_bf16) {
+                __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.o) + base;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) tile[(blk * 16 + e) * DV + c] = __uint_as_float(y[e]);
+                for (int e = 0; e < 32; ++e)
+                    if (e0 + e < T) op[(e0 + e) * rstride] = __float2bfloat16_rn(__uint_as_float(y[e]));
+            } else {
+                float* op = solve ? static_cast<float*>(p.o) + base : p.U + base;
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e0 + e < T) op[(e0 + e) * rstride] = __uint_as_float(y[e]);
             }
         }
-        fence_proxy_async_smem();
-    }
-    if (solve)
-        group_sync(1, 128);
-    else
-        group_sync(2, 128);
-    if (tid == 0 || tid == 128) {
-        pdl_wait();
-        tma_store_4d(solve ? &tmO : &tmU, sm + (solve ? L::OT : L::UT), 0, h, 0, b);
-        bulk_commit_group();
-        bulk_wait_read_all();
     }
     if (tid == 128 && *sFlag) {
         // a wait gave up: let the copies in flight land before leaving
@@ -635,17 +629,15 @@ __global__ void __launch_bounds__(NT, 2)
 // Host side.
 
 bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H);
-bool make_out_map(CUtensorMap* m, void* base, int B, int T, int H, int bf16);
 bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                  const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
                                  int o_bf16, float scale, const Ws& ws, int inputs_ready, int state_ready,
                                  cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mo, mu, ms;
+    CUtensorMap mq, mk, mv, ms;
     if (!make_bf16_row_map(&mq, q, B, T, HK) || !make_bf16_row_map(&mk, k, B, T, HK) ||
-        !make_bf16_row_map(&mv, v, B, T, H) || !make_out_map(&mo, o, B, T, H, o_bf16) ||
-        !make_out_map(&mu, ws.U, B, T, H, 0) || !make_state_map(&ms, S0, B, H))
+        !make_bf16_row_map(&mv, v, B, T, H) || !make_state_map(&ms, S0, B, H))
         return cudaErrorInvalidValue;
     tcf::Params prm;
     prm.g = g;
@@ -673,7 +665,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_pdl(tcf::verify_fwd_kernel, dim3(H, B), dim3(tcf::NT), smem, st, mq, mk, mv, mo, mu, ms, prm);
+    return launch_pdl(tcf::verify_fwd_kernel, dim3(H, B), dim3(tcf::NT), smem, st, mq, mk, mv, ms, prm);
 }
 
 }  // namespace canopy
