@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one verify
 # launch of the default workload, from an ncu capture of the current kernel;
 # set to None whenever the kernel changes, until it is captured again.
-VERIFY_DRAM_TRAFFIC = 29_551_872 + 83_712
+VERIFY_DRAM_TRAFFIC = 29_560_320 + 105_728
 
 
 def verify_bytes(B, T, H, d, in_bytes=2, o_bytes=4):
