@@ -7,10 +7,14 @@
 //     y_i[c] = act(bias[c] + sum_j w[c][j] X(i, K-1-j)[c]),
 // X(i, m) the input m steps up i's root path, or the committed state once
 // the path has passed the root.  Memory bound: one CTA per (stream, block of
-// CB channels) stages the stream's whole block of x (T rows of CB channels)
-// and its parents in shared memory in one round of coalesced loads, then
-// eight node lanes of 32 threads (four channels each) read every tap from
-// shared memory and write y coalesced.
+// 128 channels) stages the stream's whole block of x (T rows of 128
+// channels) and its parents in shared memory in one round of coalesced
+// loads.  With C a multiple of 8, one thread per node builds the node's
+// table of K tap sources (a node index, or a state slot once the path has
+// passed the root), and node lanes of 16 threads (eight channels each, 16-
+// or 32-byte accesses) read every tap from shared memory and write y
+// coalesced; otherwise node lanes of 32 threads take four channels each and
+// walk the parent chain themselves.
 #include "common.cuh"
 
 namespace canopy {
@@ -131,6 +135,134 @@ __global__ void __launch_bounds__(NT) tree_conv_kernel(const T_* __restrict__ x,
     }
 }
 
+// Eight consecutive channels (16 bytes of bf16, 32 of fp32).
+__device__ inline void load8c(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(wd[e] << 16);
+        v[2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+    }
+}
+__device__ inline void load8c(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p), c = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+}
+__device__ inline void copy8c(__nv_bfloat16* d, const __nv_bfloat16* s) {
+    *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(s);
+}
+__device__ inline void copy8c(float* d, const float* s) {
+    *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(s);
+    *reinterpret_cast<uint4*>(d + 4) = *reinterpret_cast<const uint4*>(s + 4);
+}
+__device__ inline void store8c(float* p, const float (&v)[8]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ inline void store8c(__nv_bfloat16* p, const float (&v)[8]) {
+    uint32_t wd[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        wd[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+// n consecutive floats (n a multiple of 4, p 16-byte aligned) into v.
+template <int N>
+__device__ inline void load_floats(const float* p, float (&v)[N]) {
+    static_assert(N % 4 == 0, "whole float4s");
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p) + q);
+        v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+    }
+}
+
+constexpr int CT8 = CB / 8;   // channel threads of the eight-channel kernel
+constexpr int NL8 = NT / CT8; // its node lanes (two per warp)
+
+__host__ __device__ constexpr size_t tap_offset(int T, int es) { return size_t(T) * CB * es; }
+__host__ __device__ constexpr size_t par_offset(int T, int es, int K) {
+    return (tap_offset(T, es) + size_t(T) * K * 2 + 15) & ~size_t(15);
+}
+__host__ __device__ constexpr size_t conv8_smem(int T, int es, int K) { return par_offset(T, es, K) + size_t(T) * 4; }
+
+// C a multiple of 8.  Thread i < T first lists node i's K tap sources,
+// newest first: tap m is the node m steps up the root path, or, once the
+// path (n nodes) has been passed, state slot K-2-(m-n), stored as -1 - slot.
+template <typename T_, int K>
+__global__ void __launch_bounds__(NT, (K <= 4) ? 3 : 2) tree_conv8_kernel(const T_* __restrict__ x, const float* __restrict__ state,
+                                                        const float* __restrict__ w, const float* __restrict__ bias,
+                                                        const int32_t* __restrict__ parent, int T, int C, int silu,
+                                                        T_* __restrict__ y, int32_t* err) {
+    extern __shared__ __align__(16) uint8_t conv_smem_raw[];
+    T_* sX = reinterpret_cast<T_*>(conv_smem_raw);                                               // [T][CB]
+    int16_t* sTap = reinterpret_cast<int16_t*>(conv_smem_raw + tap_offset(T, sizeof(T_)));       // [T][K]
+    int* sPar = reinterpret_cast<int*>(conv_smem_raw + par_offset(T, sizeof(T_), K));            // [T]
+    const int b = blockIdx.y, cb0 = blockIdx.x * CB;
+    const int ct = threadIdx.x % CT8, nl = threadIdx.x / CT8;  // channel thread, node lane
+    const int c = cb0 + 8 * ct;                                // first of this thread's eight channels
+    const bool live = c < C;                                   // all eight or none (C % 8 == 0)
+    if (live)
+        for (int r = nl; r < T; r += NL8) copy8c(sX + size_t(r) * CB + 8 * ct, x + (size_t(b) * T + r) * C + c);
+    load_parents(parent, b, T, sPar, err, blockIdx.x == 0);
+    // this thread's weights (w[c .. c+7][0 .. K-1], contiguous and 16-byte
+    // aligned since c is a multiple of 8) and bias; the committed state is
+    // read only by the few nodes within K - 1 steps of the root
+    float wf[8 * K], bv[8];
+    if (live) {
+        load_floats(w + size_t(c) * K, wf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bv[e] = bias ? bias[c + e] : 0.f;  // bias is only 4-byte aligned
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        const int i = threadIdx.x;
+        int node = i, n = 0;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+            int tap;
+            if (node >= 0) {
+                tap = node;
+                node = sPar[node];
+                ++n;
+            } else {
+                tap = -1 - (K - 2 - (m - n));
+            }
+            sTap[i * K + m] = int16_t(tap);
+        }
+    }
+    __syncthreads();
+    if (!live) return;
+    for (int i = nl; i < T; i += NL8) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = bv[e];
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+            const int t = sTap[i * K + m];
+            float v[8];
+            if (t >= 0) {
+                load8c(sX + size_t(t) * CB + 8 * ct, v);
+            } else {
+                const float* sp = state + (size_t(b) * C + c) * (K - 1) + (-1 - t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __ldg(sp + e * (K - 1));
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wf[e * K + (K - 1 - m)], v[e], acc[e]);
+        }
+        if (silu) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = __fdividef(acc[e], 1.f + __expf(-acc[e]));
+        }
+        store8c(y + (size_t(b) * T + i) * C + c, acc);
+    }
+}
+
 template <typename T_, int K>
 __global__ void __launch_bounds__(NT) conv_commit_kernel(const int32_t* __restrict__ accepted, const T_* __restrict__ x,
                                                          const int32_t* __restrict__ parent, const float* state,
@@ -184,6 +316,19 @@ template <typename T_, int K>
 static cudaError_t tree_conv_typed(dim3 grid, const void* x, const float* state, const float* w, const float* bias,
                                    const int32_t* parent, int T, int C, int silu, void* y, int32_t* err,
                                    cudaStream_t st) {
+    if (C % 8 == 0) {
+        static bool attr8 = false;
+        if (!attr8) {
+            const cudaError_t e = cudaFuncSetAttribute(conv::tree_conv8_kernel<T_, K>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       int(conv::conv8_smem(kMaxT, sizeof(T_), K)));
+            if (e != cudaSuccess) return e;
+            attr8 = true;
+        }
+        conv::tree_conv8_kernel<T_, K><<<grid, conv::NT, conv::conv8_smem(T, sizeof(T_), K), st>>>(
+            static_cast<const T_*>(x), state, w, bias, parent, T, C, silu, static_cast<T_*>(y), err);
+        return cudaGetLastError();
+    }
     static bool attr = false;
     if (!attr) {
         const cudaError_t e = cudaFuncSetAttribute(conv::tree_conv_kernel<T_, K>,

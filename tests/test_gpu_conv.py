@@ -54,6 +54,24 @@ def test_tree_conv_matches_oracle(lib, T, fam, K, bf16, act):
         assert rel_err(yn, ref) <= 1e-5
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("T,fam,K", [(5, "chain", 4), (64, "random", 3), (200, "skewed", 8)])
+def test_tree_conv_channels_not_a_multiple_of_8(lib, T, fam, K, bf16):
+    """C = 100 (a multiple of 4, not of 8) takes the four-channel kernel;
+    C = 104 the eight-channel one with a partial last block."""
+    for C in (100, 104):
+        parents, x, state, w, bias = _case(T, fam, 2, C, K, bf16, seed=C)
+        ref = oracle.tree_conv_batch(parents, x, state, w, bias, "silu")
+        xd = _dev(x, torch.bfloat16 if bf16 else torch.float32)
+        y = lib.tree_conv(xd, _dev(state), _dev(w), _dev(parents, torch.int32), bias=_dev(bias), act="silu")
+        yn = y.float().cpu().numpy().astype(np.float64)
+        if bf16:
+            excess = np.maximum(np.abs(yn - ref) - 2.0 ** -8 * np.abs(ref), 0.0)
+            assert excess.max() / np.sqrt((ref ** 2).mean()) <= 1e-5
+        else:
+            assert rel_err(yn, ref) <= 1e-5
+
+
 def test_tree_conv_model_width_without_bias(lib):
     """The convolution width of the pages' layer shape: q, k (16 heads) and v
     (32 heads) of 128 channels each, C = 8,192, no bias, SiLU."""
