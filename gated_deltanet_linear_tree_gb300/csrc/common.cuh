@@ -220,18 +220,6 @@ __device__ inline void bulk_load(void* dst, const void* src, uint32_t bytes, uin
                  : "memory");
 }
 
-// Tiled bulk store shared -> global (4-d tensor map); boxes clipped at the
-// tensor's bounds.  Completion is tracked by bulk groups.
-__device__ inline void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3) {
-    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
-}
-__device__ inline void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk store has finished reading shared memory.
-__device__ inline void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
 // ---- tcgen05 ---------------------------------------------------------------
 
 __device__ inline void tmem_alloc(uint32_t* slot, uint32_t ncols) {
