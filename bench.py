@@ -286,8 +286,10 @@ def run_canopy(args, world, rank, local):
     vb = verify_bytes(B, T, H, d)
     cb = commit_bytes(B, T, H, d)
     achieved = vb / (v_us * 1e-6) / 1e9
-    tc_path = T <= 64
-    launches_per_step = (1 if tc_path else 4) + 1
+    # one fused launch for forward substitution or the Neumann series up to
+    # 64 nodes; otherwise tree prep, the Gram and the solve (two for split)
+    tc_path = T <= 64 and args.solve in ("fwdsub", "neumann")
+    launches_per_step = (1 if tc_path else (4 if args.solve == "split" else 3)) + 1
 
     e2e = run_e2e(canopy, sets, T, args, world)
     line = {
@@ -305,9 +307,10 @@ def run_canopy(args, world, rank, local):
         "timing": f"one CUDA graph of {G} steps (verify + commit, sets rotating) replayed {reps} times "
                   f"(+ a graph of the {rem} remaining steps) between two events; per-kernel durations from graphs of {G} launches of one kernel, "
                   f"{args.kernel_reps} replays each (p10/p50/p90 over replays)",
-        "roofline": {"bound": "hbm", "kernel": "verify (tensor-core fused)" if tc_path else "verify (fp32 SIMT)",
+        "roofline": {"bound": "hbm", "kernel": "verify (tensor-core fused)" if tc_path else
+                     "verify (tensor-core Gram, CUDA-core solve)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": VERIFY_DRAM_TRAFFIC if tc_path else None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
+                     "traffic": VERIFY_DRAM_TRAFFIC if (tc_path and args.solve == "fwdsub") else None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
         "roofline_commit": {"bound": "hbm", "achieved": cb / (c_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
                             "frac": cb / (c_us * 1e-6) / 1e9 / peak, "algorithmic_bytes": cb},
         "gpu_launches": launches_per_step * K,
@@ -692,7 +695,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["canopy", "reference"], default="canopy")
-    ap.add_argument("--solve", choices=["fwdsub", "neumann"], default="fwdsub")
+    ap.add_argument("--solve", choices=["fwdsub", "neumann", "squaring", "split"], default="fwdsub")
     ap.add_argument("--sets", type=int, default=8)
     ap.add_argument("--graph-steps", type=int, default=200, help="steps per captured graph")
     ap.add_argument("--kernel-reps", type=int, default=5, help="replays of the one-kernel graphs")
