@@ -23,6 +23,8 @@ decisions"):
   neumann   U = sum_{m=0..d} (-G)^m R, as Z <- -G Z, U <- U + Z for d rounds
   squaring  U = (I - G)(I + G^2)(I + G^4)... R with ceil(log2(d+1)) factors
   level     per depth level L in order: U_L = R_L - G_{L,:} U
+  split     the split design: W = (I + G)^-1 formed once (row i: W_i = e_i -
+            G_i W, rows in order), then U = W R
 """
 
 from __future__ import annotations
@@ -140,6 +142,15 @@ def solve_level(G, R, parent):
     return U
 
 
+def solve_split(G, R, parent=None):
+    T = G.shape[0]
+    W = np.zeros_like(G)
+    for i in range(T):
+        W[i] = -(G[i, :i] @ W[:i])
+        W[i, i] += 1.0
+    return W @ R
+
+
 SOLVERS = {
     "dense": solve_dense,
     "fwdsub": solve_fwdsub,
@@ -147,6 +158,7 @@ SOLVERS = {
     "neumann": solve_neumann,
     "squaring": solve_squaring,
     "level": solve_level,
+    "split": solve_split,
 }
 
 
