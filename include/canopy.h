@@ -96,8 +96,12 @@ typedef enum {
  * heads.  It holds the pseudo-values U fp32 [B][T][HV][dv], the cumulative
  * log gates l fp32 [B][T][HV] (l_i = sum of log g over path(i)), node depths int32
  * [B][T], the strict-ancestor bitmask uint32 [B][T][ceil(T/32)], the DFS
- * pre-order int32 [B][T], the device error word, and the scratch of the fp32
- * path.  Returns 0 for unsupported sizes. */
+ * pre-order int32 [B][T], the device error word, and the scratch of the
+ * paths beyond one fused launch (the fp32 path, trees of more than 64 nodes
+ * and the Neumann, squaring and split solves): G and C as [B][HV][T][T]
+ * fp32, gamma X_Q and R as [B][T][HV][dv] fp32.  The squaring and split
+ * solves overwrite G and C with G^(2^m), or with (I + G)^-1 and C (I + G)^-1.
+ * Returns 0 for unsupported sizes. */
 size_t canopy_workspace_bytes(int B, int T, int HV, int dk, int dv);
 
 /* Zero the workspace (including the error word); call once after allocating
