@@ -36,6 +36,20 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(canopy.SIGNATURES) == names
 
 
+def header_enum(prefix):
+    """name -> value of every `CANOPY_<prefix>_<NAME> = <int>` enumerator."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {m.group(1).lower(): int(m.group(2))
+            for m in re.finditer(r"\bCANOPY_%s_([A-Z0-9]+)\s*=\s*(\d+)" % prefix, text)}
+
+
+def test_binding_enums_match_the_header():
+    """The binding's solve and activation names carry the header's values."""
+    from gated_deltanet_linear_tree_gb300 import canopy
+    assert canopy.SOLVE == header_enum("SOLVE")
+    assert canopy.ACT == header_enum("ACT")
+
+
 def test_workspace_sizes(lib):
     n = lib.canopy_workspace_bytes(16, 64, 16, 128, 128)
     # U + l + depth + mask + order + scratch, each region 256-byte aligned
