@@ -2,7 +2,7 @@
 
 Each mutation is a plausible slip (a causal triangle for the ancestor mask, a
 dropped beta, a dropped own gate, a transposed state, a flipped sign, the
-naive ratio).  The mutated function is built here, on the CPU, from the
+naive ratio, a solver one round or one factor short, a transposed inverse).  The mutated function is built here, on the CPU, from the
 oracle's own pieces; the check is the one the pins use.
 """
 
@@ -94,3 +94,74 @@ def test_flipped_sign_fails_brute_force_pin():
 def test_naive_ratio_is_not_finite():
     g, mask = naive_ratio_gamma(trees.chain(64), np.full(64, 0.05, np.float32), True)
     assert not np.isfinite(g[mask]).all()
+
+
+def _solver_err(solve):
+    """max |U - U_dense| of a (mutated) solver on a 40-node tree whose nodes
+    share one key (k_i.k_j = 1), so that every term of the series is large
+    enough to see (the identical-keys pin's inputs)."""
+    rng = np.random.default_rng(4)
+    p = trees.uniform_random(40, rng)
+    T, dk = 40, 8
+    k1 = rng.standard_normal(dk)
+    k = np.tile(k1 / np.linalg.norm(k1), (T, 1))
+    q = rng.standard_normal((T, dk))
+    v = rng.standard_normal((T, 6))
+    a = rng.uniform(0.8, 1.0, T)
+    b = rng.uniform(0.4, 0.6, T)
+    S0 = 0.1 * rng.standard_normal((6, dk))
+    G, C, l, P = oracle.build_G_C(p, q, k, a, b)
+    R = b[:, None] * (v - P[:, None] * (k @ S0.T))
+    assert int(trees.node_depths(p).max()) >= 4
+    return np.abs(solve(G, R, p) - SOLVERS["dense"](G, R, p)).max()
+
+
+def test_every_solver_unmutated_passes():
+    for name, fn in SOLVERS.items():
+        assert _solver_err(fn) <= 1e-12, name
+
+
+def test_neumann_one_round_short_fails():
+    def short(G, R, p):
+        d = int(trees.node_depths(p).max())
+        Z, U = R.copy(), R.copy()
+        for _ in range(d - 1):
+            Z = -(G @ Z)
+            U = U + Z
+        return U
+    assert _solver_err(short) > 1e-6
+
+
+def test_squaring_one_factor_short_fails():
+    def short(G, R, p):
+        d = int(trees.node_depths(p).max())
+        nfac = int(np.ceil(np.log2(d + 1))) - 1
+        U, Gp = R - G @ R, G
+        for _ in range(1, nfac):
+            Gp = Gp @ Gp
+            U = U + Gp @ U
+        return U
+    assert _solver_err(short) > 1e-6
+
+
+def test_squaring_with_a_plus_first_factor_fails():
+    def plus(G, R, p):
+        d = int(trees.node_depths(p).max())
+        nfac = int(np.ceil(np.log2(d + 1)))
+        U, Gp = R + G @ R, G
+        for _ in range(1, nfac):
+            Gp = Gp @ Gp
+            U = U + Gp @ U
+        return U
+    assert _solver_err(plus) > 1e-3
+
+
+def test_split_with_transposed_inverse_fails():
+    def transposed(G, R, p):
+        T = G.shape[0]
+        W = np.zeros_like(G)
+        for i in range(T):
+            W[i] = -(G[i, :i] @ W[:i])
+            W[i, i] += 1.0
+        return W.T @ R
+    assert _solver_err(transposed) > 1e-3
