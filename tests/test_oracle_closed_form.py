@@ -80,7 +80,9 @@ def test_every_solver_on_identical_keys():
     last term of the series is large: every solver within 1e-12 of the
     replay, while that last term alone is above 1e-9 (1,000 times the bound)."""
     rng = np.random.default_rng(7)
-    cases = [trees.chain(13), trees.topk(40, 2), trees.uniform_random(40, rng), trees.skewed(24, rng)]
+    cases = [trees.chain(13), trees.topk(40, 2), trees.uniform_random(40, rng), trees.skewed(24, rng),
+             # beyond one 64-node block (the blocked solver's off-diagonal products)
+             trees.topk(100, 4), trees.uniform_random(150, rng), trees.topk(200, 2)]
     for idx, p in enumerate(cases):
         q, k, v, a, b, S0 = _identical_keys(p, idx)
         o, _ = oracle.replay(p, q[:, None], k[:, None], v[:, None], a[:, None], b[:, None], S0[None])
