@@ -59,3 +59,20 @@ def test_two_gloo_ranks():
         res = dict(out)
     assert res[0][0] == res[1][0] == 1.5 + (world - 1)
     assert res[1][1] == ""
+
+
+def test_algorithmic_bytes_match_the_stated_figures():
+    """The roofline's numerator: the per-call algorithmic bytes of the
+    batched verify (B=16, T=64, H=16, d=128, bf16 q/k/v). With bf16 o the
+    formula B·H·(4·dk·dv + T·(2·dk·2 + dv·2 + 8 + 2·dv + 4·dv + 4)) + 4·B·T
+    gives 42,143,744 B; the bench also counts the depth and mask words it
+    writes (B·T·4 + B·T·⌈T/32⌉·4 = 12,288 B). The headline's fp32 o adds
+    4 MiB; the commit moves S0 once each way."""
+    sys.path.insert(0, ROOT)
+    import bench
+    B, T, H, d = 16, 64, 16, 128
+    stated = B * H * (4 * d * d + T * (2 * d * 2 + d * 2 + 8 + 2 * d + 4 * d + 4)) + 4 * B * T
+    assert stated == 42_143_744
+    assert bench.verify_bytes(B, T, H, d, o_bytes=2) == stated + 12_288
+    assert bench.verify_bytes(B, T, H, d) == stated + 12_288 + B * T * H * d * 2 == 46_350_336
+    assert bench.commit_bytes(B, T, H, d) == 33_554_432
