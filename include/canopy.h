@@ -66,7 +66,12 @@ typedef enum { CANOPY_F32 = 0, CANOPY_BF16 = 1 } canopy_dtype;
  * decisions", solve strategies behind one interface, and "The tree closed
  * form", nilpotency and squaring).  FWDSUB takes every size and dtype; the
  * other three take bf16 q/k/v with dk = dv = 128 only (else
- * CANOPY_ERR_UNSUPPORTED) and never take the path-replay dispatch below. */
+ * CANOPY_ERR_UNSUPPORTED) and never take the path-replay dispatch below.
+ * The two series forms (NEUMANN, SQUARING) are accurate while the terms
+ * (-G)^m R stay small: on deep paths whose keys are nearly aligned the terms
+ * grow before they cancel and fp32 loses them (a 64-node chain of identical
+ * keys gives errors of order 1); FWDSUB and SPLIT solve by substitution and
+ * keep ~1e-6 at any depth. */
 typedef enum {
     CANOPY_SOLVE_FWDSUB = 0,   /* blocked forward substitution, 64-node blocks            */
     CANOPY_SOLVE_NEUMANN = 1,  /* finite Neumann series, d rounds (Bole's solve)          */
