@@ -97,3 +97,26 @@ def test_every_solver_on_identical_keys():
         for name, fn in SOLVERS.items():
             err = np.abs(base + C @ fn(G, R, p) - o[:, 0]).max()
             assert err <= 1e-12, (idx, name, err)
+
+
+def test_series_forms_lose_fp32_accuracy_on_aligned_deep_paths():
+    """The numerical range of the series forms (the solvers run in float32):
+    on a 64-node chain of identical keys the terms (-G)^m R reach ~1e7
+    before they cancel, so the Neumann series and the squaring form lose
+    the result while substitution and the split design keep ~1e-6; on a
+    shallow tree all four agree."""
+    def errs(p):
+        q, k, v, a, b, S0 = _identical_keys(p, 1)
+        o, _ = oracle.replay(p, q[:, None], k[:, None], v[:, None], a[:, None], b[:, None], S0[None])
+        G, C, l, P = build_G_C(p, q, k, a, b)
+        R = b[:, None] * (v - P[:, None] * (k @ S0.T))
+        base = P[:, None] * (q @ S0.T)
+        rms = np.sqrt((o[:, 0] ** 2).mean())
+        f32 = [x.astype(np.float32) for x in (G, R, C, base)]
+        return {s: float(np.abs(f32[3] + f32[2] @ SOLVERS[s](f32[0], f32[1], p) - o[:, 0]).max() / rms)
+                for s in ("fwdsub", "neumann", "squaring", "split")}
+    deep = errs(trees.chain(64))
+    assert deep["fwdsub"] < 1e-5 and deep["split"] < 1e-5
+    assert deep["neumann"] > 1e-2 and deep["squaring"] > 1e-2
+    shallow = errs(trees.topk(200, 2))
+    assert max(shallow.values()) < 1e-5
