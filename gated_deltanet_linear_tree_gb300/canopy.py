@@ -25,12 +25,14 @@ VERIFY_INPUTS_READY = 0x1
 VERIFY_STATE_READY = 0x2
 COMMIT_STATE_READY = 0x1
 ACT = {"none": 0, "silu": 1}
+WS_REGION = {"err": 0, "l": 1, "depth": 2, "mask": 3, "order": 4, "u": 5}
 
 # name -> (restype, argtypes); mirrors include/canopy.h
 _P, _I, _S, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
 SIGNATURES = {
     "canopy_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_workspace_init": (_I, [_P, _S, _P]),
+    "canopy_workspace_offset": (_S, [_I, _I, _I, _I, _I, _I]),
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                                 ctypes.c_uint, _P]),
@@ -114,6 +116,27 @@ def workspace(B: int, T: int, HV: int, d: int, device="cuda") -> torch.Tensor:
     ws = torch.empty(n, dtype=torch.uint8, device=device)
     _check(load().canopy_workspace_init(_ptr(ws), n, _stream()), "canopy_workspace_init")
     return ws
+
+
+def workspace_views(ws, B: int, T: int, HV: int, d: int) -> dict:
+    """Views of the workspace regions a caller may read (canopy_ws_region):
+    l fp32 [B, T, HV], depth int32 [B, T], mask int32 [B, T, ceil(T/32)]
+    (the uint32 words' bits), order int32 [B, T], U fp32 [B, T, HV, d]."""
+    _need(ws, "workspace", torch.uint8)
+    W = (T + 31) // 32
+    shapes = {"l": ((B, T, HV), torch.float32), "depth": ((B, T), torch.int32),
+              "mask": ((B, T, W), torch.int32), "order": ((B, T), torch.int32),
+              "u": ((B, T, HV, d), torch.float32)}
+    out = {}
+    for name, (shape, dt) in shapes.items():
+        off = int(load().canopy_workspace_offset(B, T, HV, d, d, WS_REGION[name]))
+        n = 1
+        for x in shape:
+            n *= x
+        if off == ctypes.c_size_t(-1).value or off + 4 * n > ws.numel():
+            raise CanopyError(f"workspace too small or sizes unsupported for region {name}")
+        out[name] = ws[off:off + 4 * n].view(dt).view(shape)
+    return out
 
 
 def tree_prep(parent, g, ws):

@@ -75,6 +75,20 @@ size_t canopy_workspace_bytes(int B, int T, int HV, int dk, int dv) {
     return ws_layout(B, T, HV, dv).total;
 }
 
+size_t canopy_workspace_offset(int B, int T, int HV, int dk, int dv, canopy_ws_region region) {
+    if (canopy_workspace_bytes(B, T, HV, dk, dv) == 0) return ~size_t(0);
+    const WsLayout L = ws_layout(B, T, HV, dv);
+    switch (region) {
+        case CANOPY_WS_ERR: return L.err;
+        case CANOPY_WS_L: return L.l;
+        case CANOPY_WS_DEPTH: return L.depth;
+        case CANOPY_WS_MASK: return L.mask;
+        case CANOPY_WS_ORDER: return L.order;
+        case CANOPY_WS_U: return L.U;
+    }
+    return ~size_t(0);
+}
+
 canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream) {
     if (!aligned16(workspace) || bytes == 0) return CANOPY_ERR_ARG;
     return cuda_status(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));

@@ -109,6 +109,24 @@ typedef enum {
  * Returns 0 for unsupported sizes. */
 size_t canopy_workspace_bytes(int B, int T, int HV, int dk, int dv);
 
+/* Regions of the workspace that hold results a caller may read (the rest is
+ * scratch with no stable contents). */
+typedef enum {
+    CANOPY_WS_ERR = 0,    /* int32: the sticky device error word (always at offset 0)   */
+    CANOPY_WS_L = 1,      /* fp32 [B][T][HV]: l_i, natural log                           */
+    CANOPY_WS_DEPTH = 2,  /* int32 [B][T]: |A(i)|                                       */
+    CANOPY_WS_MASK = 3,   /* uint32 [B][T][ceil(T/32)]: bit j%32 of word j/32 set iff j
+                             is a strict ancestor of i                                   */
+    CANOPY_WS_ORDER = 4,  /* int32 [B][T]: DFS pre-order, children in index order
+                             (order[b][pos] = node; written by canopy_tree_prep only)    */
+    CANOPY_WS_U = 5       /* fp32 [B][T][HV][dv]: the pseudo-values U                    */
+} canopy_ws_region;
+
+/* Byte offset of a region inside a workspace of canopy_workspace_bytes(B, T,
+ * HV, dk, dv) bytes (every region starts on a 256-byte boundary); (size_t)-1
+ * for unsupported sizes or an unknown region.  Host-only, no CUDA call. */
+size_t canopy_workspace_offset(int B, int T, int HV, int dk, int dv, canopy_ws_region region);
+
 /* Zero the workspace (including the error word); call once after allocating
  * it.  Enqueued on `stream`. */
 canopy_status canopy_workspace_init(void* workspace, size_t bytes, void* stream);
@@ -239,8 +257,11 @@ canopy_status canopy_serial_replay(const void* q, const void* k, const void* v, 
  *     B=1, T=31, HV=16 at dk=dv=128; larger calls return
  *     CANOPY_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up the array's address there
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     The kept address belongs to the device's context at that time: after a
+ *     cudaDeviceReset (or any teardown of that context) do not call this
+ *     entry point again in the same process.
  *   - All calls share the one array, which keeps the last call's contents;
  *     nothing in it needs to start at zero (every snapshot is written before
  *     it is read), but calls that overlap on the GPU race with each other.

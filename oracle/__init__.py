@@ -18,14 +18,16 @@ flash-linear-attention form (S of shape dk x dv, o = S^T q).  ``chain`` is
 written in that other orientation on purpose, so the two cross-check.
 
 Modules
-  tree         ancestors, depths and masks, written here (not shared)
+  tree         ancestors, depths, masks and the DFS pre-order, written here
+               (not shared)
   replay       the definition: the recurrence run along every root path
   chain        sequential recurrence for a chain, dk x dv orientation
   brute        every node's root path run as a fresh chain
   closed_form  log-space closed form with six solvers (dense, forward
                substitution, blocked forward substitution, Neumann, squaring,
                level-synchronous), fp64, plus an fp32 twin and the naive-ratio
-               twin used by the stability pin
+               twin used by the stability pin; closed_form_heads carries
+               every head of one stream at once (the round trip's check)
   commit       the accepted node's state from the pseudo-values
   conv         the tree-aware short causal convolution and its state commit
 
@@ -42,6 +44,7 @@ from .tree import (  # noqa: F401
     depths,
     strict_ancestor_mask,
     cumulative_log_gate,
+    dfs_preorder,
 )
 from .replay import replay, replay_batch  # noqa: F401
 from .chain import chain_recurrence  # noqa: F401
@@ -49,6 +52,7 @@ from .brute import brute_force  # noqa: F401
 from .closed_form import (  # noqa: F401
     closed_form,
     closed_form_batch,
+    closed_form_heads,
     build_G_C,
     SOLVERS,
 )

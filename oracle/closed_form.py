@@ -192,3 +192,39 @@ def closed_form_batch(parent, q, k, v, alpha, beta, S0, solver: str = "fwdsub",
                 parent[b], q[b, :, h], k[b, :, h], v[b, :, h], alpha[b, :, h],
                 beta[b, :, h], S0[b, h], solver, dtype)
     return O, U, L
+
+
+def closed_form_heads(parent, q, k, v, alpha, beta, S0, scale: float = 1.0):
+    """The same closed form for one stream and all heads at once (fp64), with
+    the forward-substitution solve; the head axis is carried through every
+    step, nothing else changes.  q, k [T, H, dk] (key heads); v [T, HV, dv];
+    alpha, beta [T, HV]; S0 [HV, dv, dk]; value head j reads key head
+    j // (HV / H) and q is multiplied by ``scale``, as in ``replay``.
+    Returns (O [T, HV, dv], U [T, HV, dv], l [T, HV])."""
+    from .replay import value_heads
+    p = validate_parent(parent)
+    T = p.size
+    v = np.asarray(v, np.float64).transpose(1, 0, 2)              # [HV, T, dv]
+    HV = v.shape[0]
+    q = (value_heads(q, HV) * float(scale)).transpose(1, 0, 2)    # [HV, T, dk]
+    k = value_heads(k, HV).transpose(1, 0, 2)
+    a = np.asarray(alpha, np.float64)
+    b = np.asarray(beta, np.float64).T                            # [HV, T]
+    S0 = np.asarray(S0, np.float64)
+    Ms = strict_ancestor_mask(p)
+    Mp = Ms | np.eye(T, dtype=bool)
+    l = cumulative_log_gate(p, a)                                 # [T, HV]
+    lt = l.T
+    P = np.exp(lt)                                                # [HV, T]
+    diff = np.where(Mp[None], lt[:, :, None] - lt[:, None, :], 0.0)
+    Gam = np.where(Mp[None], np.exp(diff), 0.0)                   # [HV, T, T]
+    KT = k.transpose(0, 2, 1)
+    G = np.where(Ms[None], b[:, :, None] * Gam * (k @ KT), 0.0)
+    C = np.where(Mp[None], Gam * (q @ KT), 0.0)
+    S0T = S0.transpose(0, 2, 1)
+    R = b[:, :, None] * (v - P[:, :, None] * (k @ S0T))           # [HV, T, dv]
+    U = np.zeros_like(R)
+    for i in range(T):
+        U[:, i] = R[:, i] - (G[:, i, None, :i] @ U[:, :i])[:, 0]
+    O = P[:, :, None] * (q @ S0T) + C @ U
+    return O.transpose(1, 0, 2), U.transpose(1, 0, 2), l

@@ -58,3 +58,19 @@ def cumulative_log_gate(parent, alpha) -> np.ndarray:
     for i in range(len(parent)):
         l[i] = la[i] + (l[parent[i]] if parent[i] >= 0 else 0.0)
     return l
+
+
+def dfs_preorder(parent) -> np.ndarray:
+    """Depth-first pre-order from the root, children visited in increasing
+    index order: order[pos] = the node at position pos (canopy page,
+    "Design decisions", tree order: subtrees contiguous)."""
+    p = validate_parent(parent)
+    kids = [[] for _ in range(p.size)]
+    for i in range(1, p.size):
+        kids[p[i]].append(i)
+    out, stack = [], [0]
+    while stack:
+        n = stack.pop()
+        out.append(n)
+        stack.extend(reversed(kids[n]))       # the smallest child is visited first
+    return np.array(out, dtype=np.int64)

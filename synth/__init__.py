@@ -24,5 +24,5 @@ from .trees import (  # noqa: F401
     leaves,
     family,
 )
-from .values import make_inputs, round_bf16, stream_seed  # noqa: F401
+from .values import make_inputs, make_aligned_inputs, round_bf16, stream_seed  # noqa: F401
 from .configs import CONFIGS, config_inputs  # noqa: F401

@@ -1,0 +1,104 @@
+"""Cases whose deep terms matter: every node of a stream has the same key.
+
+With random unit keys in 128 dimensions k_i.k_j is about 0.09, so the terms
+(-G)^m R of the series a solve sums fall below 1e-3 of the result by m = 2-3,
+and a solve that dropped an ancestor beyond the second on a path, or a
+Neumann series one round short, would still pass a 1e-2 bound.  With one key
+per (stream, head) (synth.make_aligned_inputs: beta in [0.4, 0.6], gates in
+[0.8, 1]) G's entries stay near 0.5 along every path, so those mistakes move
+the output by 1e-4 to O(1) of its rms.
+
+Each case names the tree and the solves it is run through on the GPU.  The
+series forms (Neumann, squaring) are only run where their terms stay small
+enough for fp32 (depth <= 12: on a 64-node chain of aligned keys the terms
+reach ~1e7 before they cancel); substitution and the split design take every
+depth.  ``BOUND`` holds, per (case, solve), ten times the error the GPU
+measured on these inputs (GB300, max |o - o_ref| / rms(o_ref) against the
+fp64 oracle), rounded up to two significant digits; each must stay at or
+below the 1e-2 bf16 tolerance too.  tests/test_deep_cases_sensitivity.py
+checks, on the CPU, that the planted mistakes above exceed these bounds.
+"""
+
+import numpy as np
+
+import synth
+from synth import trees
+
+B, H, D = 2, 4, 128
+
+
+def _random(T, seed, max_depth=None):
+    rng = np.random.default_rng(seed)
+    while True:
+        p = trees.uniform_random(T, rng)
+        if max_depth is None or trees.tree_depth(p) <= max_depth:
+            return p
+
+
+# name -> (parent array builder, solves)
+CASES = {
+    # one 64-node block: the fused tensor-core kernels
+    "chain13": (lambda: trees.chain(13), ("fwdsub", "neumann", "squaring")),
+    "top2_40": (lambda: trees.topk(40, 2), ("fwdsub", "neumann", "squaring")),
+    "top4_64": (lambda: trees.topk(64, 4), ("fwdsub", "neumann", "squaring")),
+    "random64": (lambda: _random(64, 1, 10), ("fwdsub", "neumann", "split")),
+    "chain64": (lambda: trees.chain(64), ("fwdsub", "split")),
+    "skewed64": (lambda: trees.skewed(64, np.random.default_rng(2)), ("fwdsub", "split")),
+    # beyond one block: blocked / level substitution and the variants
+    "chain100": (lambda: trees.chain(100), ("fwdsub", "split")),
+    "top2_200": (lambda: trees.topk(200, 2), ("fwdsub", "neumann", "squaring", "split")),
+    "random150": (lambda: _random(150, 3, 12), ("fwdsub", "neumann", "squaring", "split")),
+    "top4_256": (lambda: trees.topk(256, 4), ("fwdsub", "neumann", "squaring")),
+    "skewed200": (lambda: trees.skewed(200, np.random.default_rng(4)), ("fwdsub", "split")),
+    "chain256": (lambda: trees.chain(256), ("fwdsub", "split")),
+}
+
+# (case, solve) -> bound on max |o - o_ref| / rms(o_ref): ten times the error measured
+# on GB300 (fp32 o), rounded up to two significant digits
+BOUND = {
+    ("chain13", "fwdsub"): 0.00057,  # measured 5.69e-05
+    ("chain13", "neumann"): 0.00012,  # measured 1.15e-05
+    ("chain13", "squaring"): 0.00024,  # measured 2.31e-05
+    ("top2_40", "fwdsub"): 0.00071,  # measured 7.1e-05
+    ("top2_40", "neumann"): 0.00011,  # measured 1.1e-05
+    ("top2_40", "squaring"): 0.00018,  # measured 1.78e-05
+    ("top4_64", "fwdsub"): 0.0013,  # measured 0.00013
+    ("top4_64", "neumann"): 0.00013,  # measured 1.27e-05
+    ("top4_64", "squaring"): 0.00024,  # measured 2.36e-05
+    ("random64", "fwdsub"): 0.00077,  # measured 7.61e-05
+    ("random64", "neumann"): 0.00014,  # measured 1.34e-05
+    ("random64", "split"): 0.00021,  # measured 2.03e-05
+    ("chain64", "fwdsub"): 0.00098,  # measured 9.75e-05
+    ("chain64", "split"): 0.00027,  # measured 2.63e-05
+    ("skewed64", "fwdsub"): 0.001,  # measured 9.96e-05
+    ("skewed64", "split"): 0.00031,  # measured 3.07e-05
+    ("chain100", "fwdsub"): 0.00032,  # measured 3.12e-05
+    ("chain100", "split"): 0.00032,  # measured 3.12e-05
+    ("top2_200", "fwdsub"): 0.00025,  # measured 2.48e-05
+    ("top2_200", "neumann"): 0.00025,  # measured 2.48e-05
+    ("top2_200", "squaring"): 0.00025,  # measured 2.48e-05
+    ("top2_200", "split"): 0.00025,  # measured 2.49e-05
+    ("random150", "fwdsub"): 0.00025,  # measured 2.45e-05
+    ("random150", "neumann"): 0.00025,  # measured 2.45e-05
+    ("random150", "squaring"): 0.00025,  # measured 2.45e-05
+    ("random150", "split"): 0.00025,  # measured 2.45e-05
+    ("top4_256", "fwdsub"): 0.00022,  # measured 2.12e-05
+    ("top4_256", "neumann"): 0.00022,  # measured 2.12e-05
+    ("top4_256", "squaring"): 0.00022,  # measured 2.12e-05
+    ("skewed200", "fwdsub"): 0.00032,  # measured 3.14e-05
+    ("skewed200", "split"): 0.00032,  # measured 3.14e-05
+    ("chain256", "fwdsub"): 0.00032,  # measured 3.17e-05
+    ("chain256", "split"): 0.00032,  # measured 3.17e-05
+}
+
+
+def inputs(name):
+    """The seeded inputs of a case (identical parents in both streams)."""
+    build, _ = CASES[name]
+    p = build()
+    seed = sum(map(ord, name))
+    return synth.make_aligned_inputs([p] * B, H, D, D, True, case=77, rnd=seed)
+
+
+def params():
+    return [(name, solve) for name, (_, solves) in CASES.items() for solve in solves]

@@ -43,3 +43,13 @@ def run_verify(canopy, dev, solve="fwdsub", o_dtype=torch.float32, ws=None, scal
                       solve=solve, o_dtype=o_dtype, scale=scale)
     err = canopy.read_device_error(ws)
     return o, ws, err
+
+
+def page_metrics(x, ref):
+    """The canopy page's own error measures ("Hard constraints", oracle
+    parity): the largest absolute difference, and the relative Frobenius
+    norm ||x - ref||_F / ||ref||_F over the whole tensor."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    d = x - ref
+    return float(np.abs(d).max()), float(np.sqrt((d ** 2).sum() / (ref ** 2).sum()))

@@ -9,7 +9,7 @@ import torch
 import oracle
 import synth
 from synth import trees
-from tests.gpu_helpers import TOL_BF16, TOL_F32, oracle_outputs, rel_err, run_verify, to_device
+from tests.gpu_helpers import TOL_BF16, TOL_F32, oracle_outputs, page_metrics, rel_err, run_verify, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -130,12 +130,15 @@ def test_commit_on_sanitised_tree(lib, T):
     assert rel_err(S_new.cpu().numpy(), ref) <= TOL_BF16
 
 
-def _round_trip(lib, B, T, H, rounds, bf16, check_streams):
+def _round_trip(lib, B, T, H, rounds, bf16, replay_streams):
     """Verify a fresh tree, accept a random root-to-leaf path, commit it into
-    S0 in fp32; the oracle carries its own fp64 state from the same S0."""
+    S0 in fp32; the oracle carries its own fp64 state from the same S0.
+    Every stream's o is checked every round against the oracle's closed form
+    (carried over all heads at once), and the streams replay_streams(r)
+    against the replay itself.  Returns the per-round errors."""
     S_dev = None
     S_orc = None
-    worst_o = worst_s = 0.0
+    curve = []
     for r in range(rounds):
         inp = synth.config_inputs(4, rnd=r, B=B, T=T, H=H, bf16=bf16)
         if r == 0:
@@ -151,10 +154,13 @@ def _round_trip(lib, B, T, H, rounds, bf16, check_streams):
         lib.commit(torch.from_numpy(acc).cuda(), S_dev, dev["k"], dev["parent"], ws, out=S_dev)
         assert lib.read_device_error(ws) == 0
         on = o.cpu().numpy()
-        for b in check_streams(r):
+        o_cf = np.stack([oracle.closed_form_heads(inp["parent"][b], inp["q"][b], inp["k"][b], inp["v"][b],
+                                                  inp["g"][b], inp["beta"][b], S_orc[b])[0] for b in range(B)])
+        e_o = rel_err(on, o_cf)
+        for b in replay_streams(r):
             o_ref, _ = oracle.replay(inp["parent"][b], inp["q"][b], inp["k"][b], inp["v"][b], inp["g"][b],
                                      inp["beta"][b], S_orc[b], keep_states=False)
-            worst_o = max(worst_o, rel_err(on[b], o_ref))
+            e_o = max(e_o, rel_err(on[b], o_ref))
         # the oracle's own state: replay only the accepted path
         for b in range(B):
             path = oracle.root_path(inp["parent"][b], int(acc[b]))
@@ -162,22 +168,37 @@ def _round_trip(lib, B, T, H, rounds, bf16, check_streams):
             _, S_path = oracle.replay(chain, inp["q"][b][path], inp["k"][b][path], inp["v"][b][path],
                                       inp["g"][b][path], inp["beta"][b][path], S_orc[b], keep_states=True)
             S_orc[b] = S_path[-1]
-        worst_s = max(worst_s, rel_err(S_dev.cpu().numpy(), S_orc))
-    return worst_o, worst_s
+        Sd = S_dev.cpu().numpy()
+        curve.append((e_o, rel_err(Sd, S_orc), *page_metrics(on, o_cf), *page_metrics(Sd, S_orc)))
+    return np.array(curve)
+
+
+def _print_curve(tag, curve):
+    """The error growth curve (canopy page, "M5": record it): per round, the
+    o and state errors as max/rms, then the page's max-abs and relative
+    Frobenius for o and for the state."""
+    print(f"{tag} round o_err S_err o_max_abs o_rel_fro S_max_abs S_rel_fro")
+    for r, row in enumerate(curve):
+        print(f"{tag} {r} " + " ".join(f"{x:.3e}" for x in row))
 
 
 def test_round_trip_100_rounds(lib):
-    """Batched round trip: B=16, H=16, T=128, 100 rounds; the state checked
-    every round for every stream, o checked on one rotating stream per round."""
-    wo, ws_ = _round_trip(lib, 16, 128, 16, 100, True, lambda r: [r % 16])
-    print("100 rounds: worst o err", wo, "worst state err", ws_)
-    assert wo <= TOL_BF16 and ws_ <= TOL_BF16
+    """Batched round trip: B=16, H=16, T=128, 100 rounds; o and the state
+    checked every round for every stream (o against the closed form on all
+    streams and against the replay on one rotating stream)."""
+    curve = _round_trip(lib, 16, 128, 16, 100, True, lambda r: [r % 16])
+    _print_curve("RT100", curve)
+    assert curve[:, 0].max() <= TOL_BF16 and curve[:, 1].max() <= TOL_BF16
+    assert curve[:, 3].max() <= TOL_BF16 and curve[:, 5].max() <= TOL_BF16   # bf16: relative Frobenius
 
 
 def test_round_trip_fp32_20_rounds(lib):
-    wo, ws_ = _round_trip(lib, 4, 64, 4, 20, False, lambda r: range(4))
-    print("fp32 20 rounds: worst o err", wo, "worst state err", ws_)
-    assert wo <= TOL_F32 and ws_ <= TOL_F32
+    curve = _round_trip(lib, 4, 64, 4, 20, False, lambda r: range(4))
+    _print_curve("RT32", curve)
+    assert curve[:, 0].max() <= TOL_F32 and curve[:, 1].max() <= TOL_F32
+    # the page's fp32 measures: max-abs <= 1e-4 and relative Frobenius <= 1e-5
+    assert curve[:, 2].max() <= 1e-4 and curve[:, 4].max() <= 1e-4
+    assert curve[:, 3].max() <= 1e-5 and curve[:, 5].max() <= 1e-5
 
 
 def test_overlapped_verify_commit_steps(lib):

@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 from synth import trees
-from tests.gpu_helpers import TOL_BF16, TOL_F32, oracle_outputs, rel_err, run_verify, to_device
+from tests.gpu_helpers import TOL_BF16, TOL_F32, oracle_outputs, page_metrics, rel_err, run_verify, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,13 @@ def test_case2_batched_both_tiers(lib):
     print("case2 errors: bf16 tensor-core", eb, "fp32", ea)
     assert eb <= TOL_BF16
     assert ea <= TOL_F32
+    # the page's own measures ("Hard constraints", oracle parity): bf16 relative
+    # Frobenius <= 1e-2; fp32 max-abs <= 1e-4 and relative Frobenius <= 1e-5
+    mb, fb = page_metrics(o.cpu().numpy(), o_ref)
+    ma, fa = page_metrics(o32.cpu().numpy(), o_ref)
+    print(f"case2 page metrics: bf16 max_abs {mb:.3e} rel_fro {fb:.3e}; fp32 max_abs {ma:.3e} rel_fro {fa:.3e}")
+    assert fb <= 1e-2
+    assert ma <= 1e-4 and fa <= 1e-5
 
 
 TC_T = [1, 2, 3, 8, 15, 16, 17, 31, 33, 48, 63, 64]
@@ -95,7 +102,11 @@ def test_shapes_fp32(lib, fam, T):
     o_ref, _ = oracle_outputs(inp)
     o, _, err = run_verify(lib, to_device(inp, bf16=False))
     assert err == 0
-    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_F32
+    on = o.cpu().numpy()
+    assert rel_err(on, o_ref) <= TOL_F32
+    ma, fa = page_metrics(on, o_ref)
+    print(f"FP32PAGE {fam} {T} max_abs {ma:.3e} rel_fro {fa:.3e}")
+    assert ma <= 1e-4 and fa <= 1e-5
 
 
 def test_small_gates_chain_stays_finite(lib):

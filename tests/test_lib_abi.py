@@ -48,6 +48,24 @@ def test_binding_enums_match_the_header():
     from gated_deltanet_linear_tree_gb300 import canopy
     assert canopy.SOLVE == header_enum("SOLVE")
     assert canopy.ACT == header_enum("ACT")
+    assert canopy.WS_REGION == header_enum("WS")
+
+
+def test_workspace_offsets(lib):
+    """Regions start on 256-byte boundaries, in the documented order, inside
+    the workspace; unsupported sizes and regions answer (size_t)-1."""
+    from gated_deltanet_linear_tree_gb300 import canopy
+    bad = ctypes.c_size_t(-1).value
+    for B, T, HV, d in ((16, 64, 16, 128), (3, 200, 4, 128), (1, 8, 2, 32)):
+        total = lib.canopy_workspace_bytes(B, T, HV, d, d)
+        offs = [lib.canopy_workspace_offset(B, T, HV, d, d, r) for r in range(6)]
+        assert offs[0] == 0
+        assert all(o % 256 == 0 for o in offs)
+        assert offs[1] >= 4 and offs[2] >= offs[1] + B * T * HV * 4 and offs[3] >= offs[2] + B * T * 4
+        assert offs[4] >= offs[3] + B * T * ((T + 31) // 32) * 4 and offs[5] >= offs[4] + B * T * 4
+        assert offs[5] + B * T * HV * d * 4 <= total
+    assert lib.canopy_workspace_offset(16, 257, 16, 128, 128, 1) == bad
+    assert lib.canopy_workspace_offset(16, 64, 16, 128, 128, 6) == bad
 
 
 def test_workspace_sizes(lib):

@@ -215,3 +215,57 @@ def test_q_scale_scales_the_output_only():
     o2, S2 = oracle.replay(p, q, k, v, a, b, S0, scale=1.0 / np.sqrt(dk))
     assert np.abs(o2 - o1 / np.sqrt(dk)).max() <= 1e-13
     assert np.array_equal(S1, S2)
+
+
+@pytest.mark.parametrize("fam,T", [("random", 1), ("random", 37), ("chain", 70), ("skewed", 90),
+                                   ("top4", 128)])
+def test_closed_form_heads_matches_replay(fam, T):
+    """The head-vectorised closed form (the round trip's per-stream check)
+    equals the replay, the definition, on every head, with grouped value
+    heads and a q scale (canopy page, "The tree closed form"; the head layout
+    of "Qwen3.5-9B shapes")."""
+    rng = np.random.default_rng(T)
+    p = trees.family(fam, T, rng)
+    q, k, _, _, _, _ = _inputs(rng, T, 2, 16, 12)
+    _, _, v, a, b, S0 = _inputs(rng, T, 4, 16, 12)
+    o, _ = oracle.replay(p, q, k, v, a, b, S0, keep_states=False, scale=0.3)
+    O, U, l = oracle.closed_form_heads(p, q, k, v, a, b, S0, scale=0.3)
+    assert np.abs(O - o).max() <= 1e-10 * max(1.0, np.abs(o).max())
+    # U and l are the per-head closed form's
+    for h in range(4):
+        O1, U1, l1 = oracle.closed_form(p, 0.3 * q[:, h // 2], k[:, h // 2], v[:, h], a[:, h], b[:, h], S0[h])
+        assert np.abs(U[:, h] - U1).max() <= 1e-10 * max(1.0, np.abs(U1).max())
+        assert np.abs(l[:, h] - l1).max() <= 1e-12
+
+
+def _preorder_by_definition(parent):
+    """Pre-order by recursion on the definition: a node, then each child's
+    subtree in increasing child index."""
+    T = len(parent)
+    out = []
+
+    def visit(n):
+        out.append(n)
+        for c in range(n + 1, T):
+            if parent[c] == n:
+                visit(c)
+    visit(0)
+    return out
+
+
+@pytest.mark.parametrize("fam,T", [("chain", 12), ("top3", 40), ("random", 64), ("skewed", 50)])
+def test_dfs_preorder(fam, T):
+    """The oracle's DFS pre-order equals the recursive definition, puts every
+    parent before its children and keeps every subtree contiguous."""
+    p = trees.family(fam, T, np.random.default_rng(T))
+    order = oracle.dfs_preorder(p)
+    assert list(order) == _preorder_by_definition(p)
+    pos = np.empty(T, int)
+    pos[order] = np.arange(T)
+    depth = oracle.depths(p)
+    for i in range(1, T):
+        assert pos[p[i]] < pos[i]
+    for n in range(T):   # the subtree of n occupies pos[n] .. pos[n] + size - 1
+        sub = [i for i in range(T) if n in oracle.root_path(p, i)]
+        assert sorted(pos[sub]) == list(range(pos[n], pos[n] + len(sub)))
+    assert depth[order[0]] == 0

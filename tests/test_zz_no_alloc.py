@@ -17,7 +17,7 @@ import torch
 
 import synth
 from synth import trees
-from tests.gpu_helpers import TOL_F32, rel_err, to_device
+from tests.gpu_helpers import TOL_F32, oracle_outputs, rel_err, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -29,17 +29,42 @@ def _case(seed, T, fam):
 
 
 def test_static_serial_matches_regular_two_calls(lib):
-    for seed, T, fam in ((1, 16, "top4"), (2, 31, "random")):
+    """Two calls in a row, different trees: each matches the regular replay
+    and the fp64 oracle; the second call also runs without an err word (the
+    library then keeps the bits in a spare word of its own array)."""
+    for seed, T, fam, with_err in ((1, 16, "top4", True), (2, 31, "random", False)):
         inp = _case(seed, T, fam)
         dev = to_device(inp, True)
-        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda") if with_err else None
         o_static = lib.serial_replay_static(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"],
                                             dev["parent"], err=err)
         ws = lib.workspace(1, T, 16, 128)
         o_ref = lib.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws)
         torch.cuda.synchronize()
-        assert int(err.item()) == 0
+        if with_err:
+            assert int(err.item()) == 0
         assert rel_err(o_static.cpu().numpy(), o_ref.cpu().numpy()) <= TOL_F32
+        o_orc, _ = oracle_outputs(inp)
+        assert rel_err(o_static.cpu().numpy(), o_orc) <= TOL_F32
+
+
+def test_static_serial_reports_a_bad_tree(lib):
+    """A parent outside [0, i) is read as 0 (nothing is read out of bounds)
+    and reported: CANOPY_DEVERR_TREE is OR-ed into the caller's zeroed err,
+    and the output is the oracle's for the sanitised tree."""
+    inp = _case(3, 20, "random")
+    good = inp["parent"].copy()
+    inp["parent"][0, 12] = 40
+    dev = to_device(inp, True)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = lib.serial_replay_static(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"],
+                                 err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x1
+    fixed = dict(inp, parent=good)
+    fixed["parent"][0, 12] = 0
+    o_orc, _ = oracle_outputs(fixed)
+    assert rel_err(o.cpu().numpy(), o_orc) <= TOL_F32
 
 
 def test_static_serial_rejects_sizes_beyond_its_array(lib):
