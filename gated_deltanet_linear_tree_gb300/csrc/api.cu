@@ -16,9 +16,12 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
                                  const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
                                  int o_bf16, float scale, const Ws& ws, int inputs_ready, int state_ready,
                                  cudaStream_t st);
+cudaError_t launch_verify_tc_big(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
+                                 int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale,
-                               const Ws& ws, int gram_done, cudaStream_t st);
+                               const Ws& ws, cudaStream_t st);
 cudaError_t launch_gram_tc(const void* q, const void* k, const void* v, const float* beta, const float* S0, int T,
                            int B, int H, int HK, const Ws& ws, cudaStream_t st);
 cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
@@ -137,6 +140,9 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws,
                                                 (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
                                                 (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
+    // bf16 inputs beyond one 64-node block: one tensor-core launch, blocks in order
+    if (in_bf16 && dk == 128 && solve == CANOPY_SOLVE_FWDSUB)
+        return cuda_status(launch_verify_tc_big(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
     cudaError_t e = launch_tree_prep(parent, g, T, B, HV, ws, 0, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     if (solve != CANOPY_SOLVE_FWDSUB) {
@@ -145,14 +151,8 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         if (e != cudaSuccess) return cuda_status(e);
         return cuda_status(launch_solve_variant(int(solve), T, B, HV, o, o_bf16, scale, ws, st));
     }
-    // bf16 inputs beyond one 64-node block: the Gram products on tcgen05
-    const bool gram_tc = in_bf16 && dk == 128 && T > 64;
-    if (gram_tc) {
-        e = launch_gram_tc(q, k, v, beta, S0, T, B, HV, H, ws, st);
-        if (e != cudaSuccess) return cuda_status(e);
-    }
-    return cuda_status(
-        launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, HV, H, dk, o, o_bf16, scale, ws, gram_tc, st));
+    // fp32 inputs, or dk = dv = 32: CUDA cores
+    return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, HV, H, dk, o, o_bf16, scale, ws, st));
 }
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,

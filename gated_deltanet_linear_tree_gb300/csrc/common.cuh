@@ -211,6 +211,28 @@ __device__ inline void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* 
         : "memory");
 }
 
+// Tiled bulk store shared -> global through a tensor map (bulk-group
+// completion: commit with bulk_commit(), then bulk_wait_read<N>() before the
+// shared source is rewritten and bulk_wait<0>() before leaving).  Elements
+// outside the tensor are not written.
+__device__ inline void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+__device__ inline void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most N committed bulk groups of this thread still read their shared source.
+template <int N>
+__device__ inline void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// At most N committed bulk groups of this thread are still incomplete.
+template <int N>
+__device__ inline void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Untiled bulk copy global -> shared, completing on `bar` (both addresses
 // 16-byte aligned, bytes a multiple of 16).
 __device__ inline void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -343,10 +365,10 @@ __device__ inline uint32_t to_tf32(float x) {
 // segment with its jump target's and doubles the jump, so ceil(log2 T)
 // rounds cover every root path.  NW = 64-bit mask words (T <= 64 NW).
 
-template <int NW>
+template <int NW, typename S = float>
 struct JumpState {
     uint64_t m[NW];
-    float s;
+    S s;
     int len;
     int ptr;
 };
@@ -354,9 +376,10 @@ struct JumpState {
 // sPtr/sLen/sS/sM: shared arrays of Tcap entries (sM: Tcap*NW words).  On
 // entry sPtr[i] holds the sanitised parent and sS[i] the per-node log gate
 // (node i < T); on exit sM holds path(i) (self included), sS the cumulative
-// log gate and sLen |path(i)|.  Requires blockDim.x >= T.
-template <int NW>
-__device__ inline void jump_paths(int T, int* sPtr, int* sLen, float* sS, uint64_t* sM) {
+// log gate (summed in S: float, or double where deep paths need it) and
+// sLen |path(i)|.  Requires blockDim.x >= T.
+template <int NW, typename S = float>
+__device__ inline void jump_paths(int T, int* sPtr, int* sLen, S* sS, uint64_t* sM) {
     const int i = threadIdx.x;
     if (i < T) {
         for (int w = 0; w < NW; ++w) sM[i * NW + w] = (w == (i >> 6)) ? (1ull << (i & 63)) : 0ull;
@@ -365,7 +388,7 @@ __device__ inline void jump_paths(int T, int* sPtr, int* sLen, float* sS, uint64
     __syncthreads();
     for (int round = 0; round < 9; ++round) {
         int more = 0;
-        JumpState<NW> st;
+        JumpState<NW, S> st;
         if (i < T) {
             int p = sPtr[i];
             for (int w = 0; w < NW; ++w) st.m[w] = sM[i * NW + w];

@@ -1,6 +1,7 @@
-// Gram products of the tree verify for 64 < T <= 256 on tcgen05 tensor
-// cores (bf16 q/k/v, fp32 S0, fp32 accumulation in tensor memory): the
-// inputs of the level-by-level substitution in verify_simt.cu.
+// Gram products of the tree verify on tcgen05 tensor cores (bf16 q/k/v,
+// fp32 S0, fp32 accumulation in tensor memory), written to the workspace as
+// the inputs of the solve variants in solve_variants.cu (the Neumann series
+// beyond one 64-node block, the squaring form and the split design).
 //
 // canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed form"
 // (Bole's Theorem 1), in the (dv, dk) orientation:

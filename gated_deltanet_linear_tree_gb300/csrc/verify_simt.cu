@@ -1,5 +1,5 @@
-// Closed-form tree verify in fp32 on CUDA cores (the fp32 path, and every
-// size the tensor-core kernel does not take).
+// Closed-form tree verify in fp32 on CUDA cores: the fp32 path (and the
+// dk = dv = 32 heads), which the tensor-core kernels do not take.
 //
 // canopy page (projects.dotslasha.me/p/canopy.md), "The tree closed form".
 // Three launches after tree prep:
@@ -371,233 +371,18 @@ __global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict_
     level_solve<OutT, DV>(o, T, H, ws, scale);
 }
 
-// Blocked forward substitution over 64-node diagonal blocks (canopy page,
-// "Design decisions": 64-node diagonal blocks, off-diagonal updates as block
-// products), for the G and C the tensor-core Gram kernel leaves: every tile
-// on or below the diagonal written in full, zero off the paths.  For row
-// block r:
-//   R'_r = R_r - sum_{s<r} G_rs U_s,   W_rr = (I + G_rr)^-1,   U_r = W_rr R'_r,
-//   O_r  = gamma X_Q,r + sum_{s<=r} C_rs U_s.
-// W_rr has the in-block ancestor pattern; its row i follows from W (I + G) =
-// I along i's in-block path, w_ik = [i = k] - sum_{e in path(i), e > k}
-// w_ie G_ek, so the rows are independent and the depth of a block, not of the
-// tree, sets the sequential part.  One CTA (512 threads) per (stream, head):
-// thread (rg, cg) owns value columns 4 cg .. 4 cg + 3 of the block's rows
-// 4 rg .. 4 rg + 3; U of the solved blocks stays in shared memory.  Trees
-// shallower than BLOCK_MIN_DEPTH take the level-by-level substitution
-// instead (fewer levels than the blocks cost, and it skips the zeros).
-constexpr int BLK_NT = 512;
-constexpr int BN = 64;     // nodes per block
-constexpr int GS = 68;     // row stride of the staged 64 x 64 tiles (16-byte rows)
-constexpr int BLOCK_MIN_DEPTH = 32;
-
-// U is kept for whole blocks (rows past T are zero).
-__host__ __device__ constexpr size_t block_smem(int T, int DV) {
-    return size_t((T + BN - 1) / BN * BN) * DV * 4 + size_t(3) * BN * GS * 4 + size_t(BN) * DV * 4 +
-           size_t(BN) * BN;
-}
-
-// 4 x 4 register tile: acc[r][c] -= or += sum_k A[4 rg + r][k] B[k][4 cg + c]
-// over k = 0..63, A in a [BN][GS] tile, B in rows of DV floats (b = &B[0][4 cg]).
-template <int DV, bool SUB>
-__device__ __forceinline__ void tile_mac(float (&acc)[4][4], const float* a, const float* b) {
-#pragma unroll 2
-    for (int k = 0; k < BN; k += 4) {
-        float4 u[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) u[kk] = *reinterpret_cast<const float4*>(b + (k + kk) * DV);
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float4 w = *reinterpret_cast<const float4*>(a + r * GS + k);
-            const float x = (w.x * u[0].x + w.y * u[1].x) + (w.z * u[2].x + w.w * u[3].x);
-            const float y = (w.x * u[0].y + w.y * u[1].y) + (w.z * u[2].y + w.w * u[3].y);
-            const float z = (w.x * u[0].z + w.y * u[1].z) + (w.z * u[2].z + w.w * u[3].z);
-            const float q = (w.x * u[0].w + w.y * u[1].w) + (w.z * u[2].w + w.w * u[3].w);
-            if (SUB) {
-                acc[r][0] -= x; acc[r][1] -= y; acc[r][2] -= z; acc[r][3] -= q;
-            } else {
-                acc[r][0] += x; acc[r][1] += y; acc[r][2] += z; acc[r][3] += q;
-            }
-        }
-    }
-}
-
-template <typename OutT, int DV>
-__global__ void __launch_bounds__(BLK_NT, 1) solve_block_kernel(OutT* __restrict__ o, int T, int H, Ws ws,
-                                                                float scale) {
-    static_assert(DV == 128 && BLK_NT == 512 && SOLVE_NT == BLK_NT,
-                  "thread tile: 16 row groups x 32 column groups of 4 x 4");
-    __shared__ int sDepth;
-    if (threadIdx.x == 0) sDepth = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < T; i += BLK_NT) atomicMax(&sDepth, ws.depth[size_t(blockIdx.y) * T + i]);
-    __syncthreads();
-    if (sDepth < BLOCK_MIN_DEPTH) {
-        level_solve<OutT, DV>(o, T, H, ws, scale);
-        return;
-    }
-    extern __shared__ float smem[];
-    const int nb = (T + BN - 1) / BN;
-    float* sU = smem;                  // [nb * BN][DV]
-    float* sG = sU + size_t(nb) * BN * DV;   // [BN][GS] G tile
-    float* sC = sG + BN * GS;          // [BN][GS] C tile
-    float* sW = sC + BN * GS;          // [BN][GS] W_rr
-    float* sRp = sW + BN * GS;         // [BN][DV] R'_r
-    uint8_t* sPl = reinterpret_cast<uint8_t*>(sRp + BN * DV);  // [BN][BN] in-block paths, root side first
-    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-    const int cg = t & 31, rg = t >> 5;  // columns 4 cg .. 4 cg + 3, block rows 4 rg .. 4 rg + 3
-    const size_t bh = size_t(b) * H + h;
-    const float* gsb = ws.gs + bh * T * T;
-    const float* csb = ws.cs + bh * T * T;
-
-    for (int r = 0; r < nb; ++r) {
-        const int n0 = BN * r;
-        float accR[4][4], accO[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = n0 + 4 * rg + q;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-            if (i < T) {
-                const size_t ni = (size_t(b) * T + i) * H + h;
-                x = *reinterpret_cast<const float4*>(ws.rr + ni * DV + 4 * cg);
-                y = *reinterpret_cast<const float4*>(ws.xq + ni * DV + 4 * cg);
-            }
-            accR[q][0] = x.x; accR[q][1] = x.y; accR[q][2] = x.z; accR[q][3] = x.w;
-            accO[q][0] = y.x; accO[q][1] = y.y; accO[q][2] = y.z; accO[q][3] = y.w;
-        }
-        // tiles s = 0..r of block row r; the off-diagonal ones update R' and O
-        for (int s = 0; s <= r; ++s) {
-            __syncthreads();  // the tiles of the previous step are no longer read
-            for (int e = t; e < BN * BN; e += BLK_NT) {
-                const int rho = e / BN, j = e % BN, i = n0 + rho, jj = BN * s + j;
-                const bool in = i < T && jj < T;
-                sG[rho * GS + j] = in ? gsb[size_t(i) * T + jj] : 0.f;
-                sC[rho * GS + j] = in ? csb[size_t(i) * T + jj] : 0.f;
-            }
-            if (s == r && t < BN) {
-                // in-block path of node n0 + t (ancestors in block r, then the node)
-                const int rho = t, i = n0 + rho;
-                uint64_t bits = 0;
-                if (i < T) {
-                    const uint32_t* mrow = ws.mask + (size_t(b) * T + i) * ws.W;
-                    const uint32_t w0 = mrow[2 * r], w1 = (2 * r + 1 < ws.W) ? mrow[2 * r + 1] : 0u;
-                    bits = (uint64_t(w1) << 32 | w0) | (1ull << rho);
-                }
-                int d = 0;
-                for (; bits; bits &= bits - 1) sPl[rho * BN + d++] = uint8_t(__ffsll(static_cast<long long>(bits)) - 1);
-                for (int z = d; z < BN; ++z) sPl[rho * BN + z] = 0xFF;
-            }
-            __syncthreads();
-            if (s == r) break;
-            const float* us = sU + size_t(BN) * s * DV + 4 * cg;
-            tile_mac<DV, true>(accR, sG + 4 * rg * GS, us);
-            tile_mac<DV, false>(accO, sC + 4 * rg * GS, us);
-        }
-        // W_rr rows (one thread per row), left-looking along the in-block path
-        if (t < BN) {
-            const int rho = t;
-            const uint8_t* pl = sPl + rho * BN;
-            float* wr = sW + rho * GS;
-            for (int k = 0; k < BN; ++k) wr[k] = 0.f;
-            int n = 0;
-            while (n < BN && pl[n] != 0xFF) ++n;
-            for (int d = n - 1; d >= 0; --d) {
-                const int k = pl[d];
-                float a0 = (d == n - 1) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                int e = d + 1;
-                for (; e + 3 < n; e += 4) {
-                    const int e0 = pl[e], e1 = pl[e + 1], e2 = pl[e + 2], e3 = pl[e + 3];
-                    a0 -= wr[e0] * sG[e0 * GS + k];
-                    a1 -= wr[e1] * sG[e1 * GS + k];
-                    a2 -= wr[e2] * sG[e2 * GS + k];
-                    a3 -= wr[e3] * sG[e3 * GS + k];
-                }
-                for (; e < n; ++e) {
-                    const int e0 = pl[e];
-                    a0 -= wr[e0] * sG[e0 * GS + k];
-                }
-                wr[k] = (a0 + a1) + (a2 + a3);
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(sRp + (4 * rg + q) * DV + 4 * cg) =
-                make_float4(accR[q][0], accR[q][1], accR[q][2], accR[q][3]);
-        __syncthreads();
-        // U_r = W_rr R'_r (rows past T: zero W rows, zero R')
-        float uo[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) uo[q][0] = uo[q][1] = uo[q][2] = uo[q][3] = 0.f;
-        tile_mac<DV, false>(uo, sW + 4 * rg * GS, sRp + 4 * cg);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = n0 + 4 * rg + q;
-            const float4 u4 = make_float4(uo[q][0], uo[q][1], uo[q][2], uo[q][3]);
-            *reinterpret_cast<float4*>(sU + size_t(i) * DV + 4 * cg) = u4;
-            if (i < T) *reinterpret_cast<float4*>(ws.U + ((size_t(b) * T + i) * H + h) * DV + 4 * cg) = u4;
-        }
-        __syncthreads();
-        // O_r += C_rr U_r
-        tile_mac<DV, false>(accO, sC + 4 * rg * GS, sU + size_t(n0) * DV + 4 * cg);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = n0 + 4 * rg + q;
-            if (i < T) {
-                OutT* op = o + ((size_t(b) * T + i) * H + h) * DV + 4 * cg;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) store_out(op + cc, scale * accO[q][cc]);
-            }
-        }
-    }
-}
-
 }  // namespace simt
 
 template <typename InT, int DK, int DV>
 static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v, const float* beta,
                                      const float* S0, int T, int B, int H, int HK, void* o, int o_bf16, float scale,
-                                     const Ws& ws, int gram_done, cudaStream_t st) {
-    cudaError_t e = cudaSuccess;
-    if (!gram_done) {
-        dim3 g1((T + simt::ROWS - 1) / simt::ROWS, H, B);
-        simt::gram_kernel<InT, DK, DV><<<g1, 256, 0, st>>>(static_cast<const InT*>(q), static_cast<const InT*>(k),
-                                                          static_cast<const InT*>(v), beta, S0, T, H, HK, ws);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+                                     const Ws& ws, cudaStream_t st) {
+    dim3 g1((T + simt::ROWS - 1) / simt::ROWS, H, B);
+    simt::gram_kernel<InT, DK, DV><<<g1, 256, 0, st>>>(static_cast<const InT*>(q), static_cast<const InT*>(k),
+                                                      static_cast<const InT*>(v), beta, S0, T, H, HK, ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     dim3 g2(H, B);
-    if (gram_done) {
-        // full tiles from the tensor-core Gram (dk = dv = 128): blocked substitution
-        if constexpr (DV != 128) {
-            return cudaErrorInvalidValue;
-        } else {
-            // either substitution may run (the CTA picks by its tree's depth)
-            const size_t smem = std::max(simt::block_smem(T, DV), simt::solve_smem(T, DV));
-            const size_t smem_max = std::max(simt::block_smem(kMaxT, DV), simt::solve_smem(kMaxT, DV));
-            if (o_bf16) {
-                static bool attr = false;
-                if (!attr) {
-                    e = cudaFuncSetAttribute(simt::solve_block_kernel<__nv_bfloat16, DV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max));
-                    if (e != cudaSuccess) return e;
-                    attr = true;
-                }
-                simt::solve_block_kernel<__nv_bfloat16, DV><<<g2, simt::BLK_NT, smem, st>>>(
-                    static_cast<__nv_bfloat16*>(o), T, H, ws, scale);
-            } else {
-                static bool attr = false;
-                if (!attr) {
-                    e = cudaFuncSetAttribute(simt::solve_block_kernel<float, DV>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max));
-                    if (e != cudaSuccess) return e;
-                    attr = true;
-                }
-                simt::solve_block_kernel<float, DV><<<g2, simt::BLK_NT, smem, st>>>(static_cast<float*>(o), T, H, ws,
-                                                                                    scale);
-            }
-            return cudaGetLastError();
-        }
-    }
     const size_t smem = simt::solve_smem(T, DV);
     const size_t smem_max = simt::solve_smem(kMaxT, DV);
     if (o_bf16) {
@@ -626,10 +411,10 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
 
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
                                const float* S0, int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale,
-                               const Ws& ws, int gram_done, cudaStream_t st) {
+                               const Ws& ws, cudaStream_t st) {
     using bf = __nv_bfloat16;
 #define CANOPY_SIMT(IT, D) \
-    return launch_simt_typed<IT, D, D>(q, k, v, beta, S0, T, B, H, HK, o, o_bf16, scale, ws, gram_done, st)
+    return launch_simt_typed<IT, D, D>(q, k, v, beta, S0, T, B, H, HK, o, o_bf16, scale, ws, st)
     if (d == 128) {
         if (in_bf16) CANOPY_SIMT(bf, 128);
         CANOPY_SIMT(float, 128);

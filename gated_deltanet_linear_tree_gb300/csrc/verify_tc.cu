@@ -662,6 +662,22 @@ bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Node rows of o or U ([B][T][H][128], fp32 or bf16) for tiled bulk stores:
+// boxes of 32 node rows x 128 columns of one (stream, head), no swizzle
+// (a [32][128] row-major staging tile).
+bool make_row_store_map(CUtensorMap* m, void* base, int bf16, int B, int T, int H) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t es = bf16 ? 2 : 4;
+    const cuuint64_t dims[4] = {128, cuuint64_t(H), cuuint64_t(T), cuuint64_t(B)};
+    const cuuint64_t strides[3] = {128 * es, cuuint64_t(H) * 128 * es, cuuint64_t(T) * H * 128 * es};
+    const cuuint32_t box[4] = {128, 1, 32, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // S0 [B][H][128][128] fp32 -> boxes of 32 columns x 128 rows with the
 // 128-byte swizzle (one (stream, head) state is four boxes).
 bool make_state_map(CUtensorMap* m, const float* base, int B, int H) {
