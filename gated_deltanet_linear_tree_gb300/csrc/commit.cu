@@ -4,19 +4,28 @@
 // (last line) and "What the commit kernel stores", in the (dv, dk)
 // orientation:  S_new = gamma_a S0 + sum_{j in path(a)} exp(l_a - l_j) u_j k_j^T,
 // all in fp32, from the U and l the verify call left in the workspace and
-// that call's k and parent.  Memory bound: every element of S0 is read once
-// (one bulk copy per tile) and S_new written once with 16-byte coalesced
-// stores; the path's k rows and weighted u entries are staged in shared
-// memory 32 nodes at a time.
+// that call's k and parent.
+//
+// Memory bound: every element of S0 is read once and S_new written once.
+// One CTA (256 threads) rebuilds TPC 32-row tiles of a (stream, value head)
+// state (the whole state at dv = 128), so the path walk and the path's k rows
+// are fetched once per state.  At its start the CTA requests all its S0 tiles
+// by bulk copy (all in flight at once); each tile is updated and stored as
+// soon as it lands, so the stores of the first tiles overlap the loads of the
+// last.  The path's k rows and weighted u rows are staged in shared memory 32
+// nodes at a time.  (Measured on GB300, verify + commit steps at B = 16,
+// T = 64: whole states per CTA 18.4 us a step, half states 19.0, 32-row tiles
+// 19.4.)
 #include "common.cuh"
 
 namespace canopy {
 
 namespace cm {
 
-constexpr int NT = 128;    // threads per CTA
-constexpr int ROWS = 32;   // value rows per CTA
+constexpr int NT = 256;    // threads per CTA
+constexpr int ROWS = 32;   // value rows per tile (one bulk copy)
 constexpr int CH = 32;     // path nodes staged per pass
+constexpr int TPC = 4;    // 32-row tiles per CTA (the whole state at dv = 128)
 
 __device__ inline float4 k4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ inline float4 k4(const __nv_bfloat16* p) {
@@ -25,52 +34,78 @@ __device__ inline float4 k4(const __nv_bfloat16* p) {
                        __uint_as_float(w.y & 0xFFFF0000u));
 }
 
-// One CTA rebuilds ROWS value rows of one (stream, head) state.  Its S0 tile
-// is fetched by one bulk copy into shared memory at the start.  path(a) is
-// walked up the stream's parent array (an input, so with state_ready it is
-// read, and the path's k rows staged, while the preceding verify finishes);
-// after that kernel has completed, one round of loads brings l and the u
-// entries of the path, weighted by exp(l_a - l_j), and the path's rank-one
-// terms are accumulated into the tile, which is stored in place of (or
-// beside) S0.
+template <typename InT, int DK, int DV>
+struct CommitSmem {
+    static constexpr int NTILE = (DV / ROWS < TPC) ? DV / ROWS : TPC;
+    static constexpr uint32_t TILE = ROWS * DK * 4;
+    float s[NTILE * ROWS * DK];    // S0, then S_new, tile by tile
+    InT k[CH][DK];                 // k rows of the current path chunk
+    float wu[CH][DV];              // exp(l_a - l_j) u_j for the chunk's nodes, every value row
+    int par[kMaxT];                // the stream's parents
+    int path[kMaxT];               // path(a), a first
+    uint64_t bar[TPC];
+    int n, bad;
+};
+
+// Stage path nodes c0 .. c0 + cn - 1: their k rows, and (after the verify has
+// completed) their weighted u rows.
+template <typename InT, int DK, int DV>
+__device__ __forceinline__ void stage_k(CommitSmem<InT, DK, DV>& S, const InT* __restrict__ k, int b, int T, int HK,
+                                        int hk, int c0, int cn) {
+    constexpr int KV = 16 / sizeof(InT);  // k elements per 16-byte load
+    for (int e = threadIdx.x; e < cn * (DK / KV); e += NT) {
+        const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = S.path[c0 + r];
+        *reinterpret_cast<uint4*>(&S.k[r][c]) =
+            *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
+    }
+}
+template <typename InT, int DK, int DV>
+__device__ __forceinline__ void stage_wu(CommitSmem<InT, DK, DV>& S, const Ws& ws, int b, int T, int H, int h,
+                                         float la, int c0, int cn) {
+    for (int e = threadIdx.x; e < cn * (DV / 4); e += NT) {
+        const int r = e / (DV / 4), c = (e % (DV / 4)) * 4, j = S.path[c0 + r];
+        const size_t nh = (size_t(b) * T + j) * H + h;
+        const float w = expf(la - ws.l[nh]);
+        const float4 u = *reinterpret_cast<const float4*>(ws.U + nh * DV + c);
+        *reinterpret_cast<float4*>(&S.wu[r][c]) = make_float4(w * u.x, w * u.y, w * u.z, w * u.w);
+    }
+}
+
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted,
                                                     const int32_t* __restrict__ parent, const float* S0,
                                                     float* S_new, const InT* __restrict__ k, int T, int H, int HK,
                                                     Ws ws, int state_ready) {
-    constexpr int C4 = DK / 4;             // float4 per state row (threads per row)
-    constexpr int F4 = ROWS * C4 / NT;     // float4 per thread = rows per thread
-    constexpr int KV = 16 / sizeof(InT);   // k elements per 16-byte load
-    constexpr uint32_t TILE = ROWS * DK * 4;
-    static_assert(F4 >= 2 && F4 % 2 == 0 && (ROWS * C4) % NT == 0 && NT % C4 == 0, "tile shape");
-    __shared__ __align__(128) float sS[ROWS * DK];
-    __shared__ __align__(16) InT sK[CH][DK];
-    __shared__ __align__(16) float sWU[CH][ROWS];
-    __shared__ int sPar[kMaxT];        // the stream's parents
-    __shared__ int sPath[kMaxT];       // path(a), a first
-    __shared__ __align__(8) uint64_t sBar;
-    __shared__ int sN, sBad;
-    const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
-    const int v0 = rt * ROWS;
+    using Sm = CommitSmem<InT, DK, DV>;
+    constexpr int NTILE = Sm::NTILE;
+    constexpr int C4 = DK / 4;             // float4 per state row
+    constexpr int RPT = ROWS * C4 / NT;    // rows of a tile per thread
+    static_assert(NTILE <= TPC && NT % C4 == 0 && (ROWS * C4) % NT == 0 && RPT >= 1, "tile shape");
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Sm& S = *reinterpret_cast<Sm*>(smem_raw);
+    const int h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
     const int hk = h / (H / HK);  // the key head this value head reads
-    // this thread: rows r0 .. r0 + F4 - 1 of the tile, float4 column c4
-    const int c4 = t % C4, r0 = (t / C4) * F4;
-    const size_t sbase = ((size_t(b) * H + h) * DV + v0) * DK;
+    // this thread: float4 column c4 of rows r0 .. r0 + RPT - 1 of every tile
+    const int c4 = t % C4, r0 = (t / C4) * RPT;
+    const int vbase = blockIdx.x * NTILE * ROWS;  // first value row of this CTA
+    const size_t sbase = ((size_t(b) * H + h) * DV + vbase) * DK;
 
-    // Programmatic dependent launch: with state_ready, the S0 tile, the
+    // Programmatic dependent launch: with state_ready, the S0 tiles, the
     // accepted node, the parents and the path's k rows are read while the
     // preceding kernel finishes; the workspace and S_new only after it has
     // completed.
     if (!state_ready) pdl_wait();
     pdl_trigger();
     if (t == 0) {
-        mbar_init(&sBar, 1);
+        for (int i = 0; i < NTILE; ++i) mbar_init(&S.bar[i], 1);
         fence_mbar_init();
-        mbar_expect_tx(&sBar, TILE);
-        bulk_load(sS, S0 + sbase, TILE, &sBar);
+        for (int i = 0; i < NTILE; ++i) {
+            mbar_expect_tx(&S.bar[i], Sm::TILE);
+            bulk_load(S.s + i * ROWS * DK, S0 + sbase + size_t(i) * ROWS * DK, Sm::TILE, &S.bar[i]);
+        }
     }
     if (t < 32) {
-        for (int j = t; j < T; j += 32) sPar[j] = parent[size_t(b) * T + j];
+        for (int j = t; j < T; j += 32) S.par[j] = parent[size_t(b) * T + j];
         int a = accepted[b];
         __syncwarp();
         if (t == 0) {
@@ -81,78 +116,64 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
             // reads as 0), so the walk ends within a + 1 steps
             int n = 0;
             for (int j = a; j >= 0;) {
-                sPath[n++] = j;
-                const int pj = sPar[j];
+                S.path[n++] = j;
+                const int pj = S.par[j];
                 j = (j == 0) ? -1 : ((pj >= 0 && pj < j) ? pj : 0);
             }
-            sN = n;
-            sBad = bad;
+            S.n = n;
+            S.bad = bad;
         }
     }
     __syncthreads();
-    const int n = sN;
-    // k rows of the first chunk of the path (an input)
-    {
-        const int cn = min(CH, n);
-        for (int e = t; e < cn * (DK / KV); e += NT) {
-            const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[r];
-            *reinterpret_cast<uint4*>(&sK[r][c]) =
-                *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
-        }
-    }
+    const int n = S.n;
+    const int nch = (n + CH - 1) / CH;
+    stage_k(S, k, b, T, HK, hk, 0, min(CH, n));
     if (state_ready) pdl_wait();
-    if (sBad && t == 0 && h == 0 && rt == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
-    const float la = (n > 0) ? ws.l[(size_t(b) * T + sPath[0]) * H + h] : 0.f;
+    if (S.bad && t == 0 && h == 0 && blockIdx.x == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
+    const float la = (n > 0) ? ws.l[(size_t(b) * T + S.path[0]) * H + h] : 0.f;
+    const float gamma_a = (n > 0) ? expf(la) : 1.f;
+    stage_wu(S, ws, b, T, H, h, la, 0, min(CH, n));
+    __syncthreads();
 
-    float4 acc[F4];
-    bool have_tile = false;
-    for (int c0 = 0; c0 == 0 || c0 < n; c0 += CH) {
-        const int cn = max(0, min(CH, n - c0));
-        if (c0) {
-            __syncthreads();
-            for (int e = t; e < cn * (DK / KV); e += NT) {
-                const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = sPath[c0 + r];
-                *reinterpret_cast<uint4*>(&sK[r][c]) =
-                    *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
-            }
-        }
-        for (int e = t; e < cn * ROWS; e += NT) {
-            const int r = e / ROWS, c = e % ROWS, j = sPath[c0 + r];
-            const size_t nh = (size_t(b) * T + j) * H + h;
-            sWU[r][c] = expf(la - ws.l[nh]) * ws.U[nh * DV + v0 + c];
-        }
-        if (!have_tile) {
-            if (!mbar_wait(&sBar, 0) && t == 0) raise_err(ws.err, CANOPY_DEVERR_TIMEOUT);
-            const float gamma_a = (n > 0) ? expf(la) : 1.f;
+    bool timeout = false;
+#pragma unroll 1
+    for (int tile = 0; tile < NTILE; ++tile) {
+        const int v0 = tile * ROWS;  // relative to vbase
+        if (!mbar_wait(&S.bar[tile], 0)) timeout = true;
+        const float* st = S.s + tile * ROWS * DK;
+        float4 acc[RPT];
 #pragma unroll
-            for (int u = 0; u < F4; ++u) {
-                const float4 s = *reinterpret_cast<const float4*>(&sS[((r0 + u) * C4 + c4) * 4]);
-                acc[u] = make_float4(gamma_a * s.x, gamma_a * s.y, gamma_a * s.z, gamma_a * s.w);
-            }
-            have_tile = true;
+        for (int u = 0; u < RPT; ++u) {
+            const float4 s = *reinterpret_cast<const float4*>(st + ((r0 + u) * C4 + c4) * 4);
+            acc[u] = make_float4(gamma_a * s.x, gamma_a * s.y, gamma_a * s.z, gamma_a * s.w);
         }
-        __syncthreads();
-        for (int r = 0; r < cn; ++r) {
-            const float4 kk = k4(&sK[r][c4 * 4]);
-            float wu[F4];
-#pragma unroll
-            for (int u2 = 0; u2 < F4; u2 += 2) {
-                const float2 w2 = *reinterpret_cast<const float2*>(&sWU[r][r0 + u2]);
-                wu[u2] = w2.x;
-                wu[u2 + 1] = w2.y;
+#pragma unroll 1
+        for (int ch = 0; ch < nch; ++ch) {
+            const int cn = min(CH, n - ch * CH);
+            if (nch > 1 && (ch > 0 || tile > 0)) {
+                // deep paths: the chunk's k and u rows are staged again
+                __syncthreads();
+                stage_k(S, k, b, T, HK, hk, ch * CH, cn);
+                stage_wu(S, ws, b, T, H, h, la, ch * CH, cn);
+                __syncthreads();
             }
+            for (int r = 0; r < cn; ++r) {
+                const float4 kk = k4(&S.k[r][c4 * 4]);
 #pragma unroll
-            for (int u = 0; u < F4; ++u) {
-                acc[u].x += wu[u] * kk.x;
-                acc[u].y += wu[u] * kk.y;
-                acc[u].z += wu[u] * kk.z;
-                acc[u].w += wu[u] * kk.w;
+                for (int u = 0; u < RPT; ++u) {
+                    const float w = S.wu[r][vbase + v0 + r0 + u];
+                    acc[u].x += w * kk.x;
+                    acc[u].y += w * kk.y;
+                    acc[u].z += w * kk.z;
+                    acc[u].w += w * kk.w;
+                }
             }
         }
+#pragma unroll
+        for (int u = 0; u < RPT; ++u)
+            *reinterpret_cast<float4*>(S_new + sbase + size_t((v0 + r0 + u) * C4 + c4) * 4) = acc[u];
     }
-#pragma unroll
-    for (int u = 0; u < F4; ++u)
-        *reinterpret_cast<float4*>(S_new + sbase + size_t((r0 + u) * C4 + c4) * 4) = acc[u];
+    if (timeout && t == 0) raise_err(ws.err, CANOPY_DEVERR_TIMEOUT);
 }
 
 }  // namespace cm
@@ -161,8 +182,17 @@ template <typename InT, int D>
 static cudaError_t launch_commit_typed(const int32_t* accepted, const int32_t* parent, const float* S0,
                                        float* S_new, const void* k, int T, int B, int H, int HK, const Ws& ws,
                                        int state_ready, cudaStream_t st) {
-    dim3 grid(D / cm::ROWS, H, B);
-    return launch_pdl(cm::commit_kernel<InT, D, D>, grid, dim3(cm::NT), 0, st, accepted, parent, S0, S_new,
+    const size_t smem = sizeof(cm::CommitSmem<InT, D, D>);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(cm::commit_kernel<InT, D, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int nt = (D / cm::ROWS < cm::TPC) ? D / cm::ROWS : cm::TPC;
+    return launch_pdl(cm::commit_kernel<InT, D, D>, dim3(D / cm::ROWS / nt, H, B), dim3(cm::NT), smem, st, accepted,
+                      parent, S0, S_new,
                       static_cast<const InT*>(k), T, H, HK, ws, state_ready);
 }
 

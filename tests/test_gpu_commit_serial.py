@@ -79,6 +79,21 @@ def test_serial_tiny_case(lib):
     assert rel_err(o.cpu().numpy(), o_ref) <= TOL_F32
 
 
+def test_tiny_case_commit_every_node(lib):
+    """The tiny fp32 case (dk = dv = 32): the state committed at every node
+    equals the oracle's state of that node."""
+    inp = synth.config_inputs(0)
+    _, S_ref = oracle_outputs(inp, keep_states=True)
+    dev = to_device(inp, False)
+    o, ws, err = run_verify(lib, dev)
+    assert err == 0
+    T = inp["parent"].shape[1]
+    for a in range(T):
+        S_new = lib.commit(torch.tensor([a], dtype=torch.int32, device="cuda"), dev["S0"], dev["k"], dev["parent"], ws)
+        assert lib.read_device_error(ws) == 0
+        assert rel_err(S_new.cpu().numpy(), S_ref[:, a]) <= TOL_F32
+
+
 @pytest.mark.parametrize("T", [16, 64, 128])
 def test_device_error_flags(lib, T):
     """Bad trees and gates are reported through the error word, never by a
