@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libcanopy.so")
 OK, ERR_ARG, ERR_TREE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
 SOLVE = {"fwdsub": 0, "neumann": 1, "squaring": 2, "split": 3}
-DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT, DEVERR_LENGTH = 0x1, 0x2, 0x4, 0x8, 0x10
 VERIFY_INPUTS_READY = 0x1
 VERIFY_STATE_READY = 0x2
 COMMIT_STATE_READY = 0x1
@@ -34,9 +34,9 @@ SIGNATURES = {
     "canopy_workspace_init": (_I, [_P, _S, _P]),
     "canopy_workspace_offset": (_S, [_I, _I, _I, _I, _I, _I]),
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
-    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P,
-                                ctypes.c_uint, _P]),
-    "canopy_commit": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
+    "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I,
+                                _P, ctypes.c_uint, _P]),
+    "canopy_commit": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
                                   _P]),
@@ -166,35 +166,44 @@ def _heads(q, k, v, g, beta, S0, parent):
     return B, T, H, HV, dk, dv
 
 
+def _lengths(lengths, B):
+    if lengths is None:
+        return None
+    _need(lengths, "lengths", torch.int32, (B,))
+    return _ptr(lengths)
+
+
 def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None,
-           inputs_ready: bool = False, state_ready: bool = False, scale: float = 1.0):
+           inputs_ready: bool = False, state_ready: bool = False, scale: float = 1.0, lengths=None):
     """o [B, T, HV, dv] for every node of every stream's tree; q and k carry
     H key heads, v, g, beta and S0 HV value heads (a multiple of H), and
     scale multiplies q.  solve: "fwdsub" (every size and dtype), or
     "neumann", "squaring", "split" (bf16 q/k/v, dk = dv = 128).  inputs_ready: q, k, v, g, beta and parent are not
     written by the kernel launched just before this call on the current
     stream (CANOPY_VERIFY_INPUTS_READY); state_ready (with inputs_ready): nor
-    is S0 (CANOPY_VERIFY_STATE_READY)."""
+    is S0 (CANOPY_VERIFY_STATE_READY).  lengths: int32 [B] CUDA tensor of
+    per-stream tree sizes (ragged batches), or None for T everywhere; rows of
+    o past a stream's length are left as they were."""
     B, T, H, HV, dk, dv = _heads(q, k, v, g, beta, S0, parent)
     _need(ws, "workspace", torch.uint8)
     if out is None:
         out = torch.empty((B, T, HV, dv), dtype=o_dtype, device=q.device)
     _need(out, "o", None, (B, T, HV, dv))
     st = load().canopy_tree_verify(_ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(g), _ptr(beta), _ptr(S0),
-                                   _ptr(parent), T, B, H, HV, dk, dv, float(scale), SOLVE[solve], _ptr(out),
-                                   _dt(out),
+                                   _ptr(parent), _lengths(lengths, B), T, B, H, HV, dk, dv, float(scale),
+                                   SOLVE[solve], _ptr(out), _dt(out),
                                    _ptr(ws), (VERIFY_INPUTS_READY if inputs_ready else 0)
                                    | (VERIFY_STATE_READY if state_ready else 0), _stream())
     _check(st, "canopy_tree_verify")
     return out
 
 
-def commit(accepted, S0, k, parent, ws, out=None, state_ready: bool = False):
+def commit(accepted, S0, k, parent, ws, out=None, state_ready: bool = False, lengths=None):
     """S_new [B, HV, dv, dk] for the accepted node of every stream, from the
     preceding verify call's k (H key heads), parent and workspace.
     state_ready: S0, accepted, k and parent are not written by the kernel
     launched just before this call on the current stream
-    (CANOPY_COMMIT_STATE_READY)."""
+    (CANOPY_COMMIT_STATE_READY).  lengths: the verify call's, or None."""
     _need(S0, "S0", torch.float32)
     _need(parent, "parent", torch.int32)
     _need(k, "k")
@@ -209,9 +218,9 @@ def commit(accepted, S0, k, parent, ws, out=None, state_ready: bool = False):
     if out is None:
         out = torch.empty_like(S0)
     _need(out, "S_new", torch.float32, S0.shape)
-    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _ptr(parent), _dt(k), T, B, H, HV, dk,
-                              dv,
-                              _ptr(ws), COMMIT_STATE_READY if state_ready else 0, _stream())
+    st = load().canopy_commit(_ptr(accepted), _ptr(S0), _ptr(out), _ptr(k), _ptr(parent), _lengths(lengths, B),
+                              _dt(k), T, B, H, HV, dk, dv, _ptr(ws), COMMIT_STATE_READY if state_ready else 0,
+                              _stream())
     _check(st, "canopy_commit")
     return out
 

@@ -7,32 +7,33 @@
 namespace canopy {
 // Launchers take H = value heads (the units: v, g, beta, S0, o, workspace)
 // and HK = key heads (q, k); value head h reads key head h / (H / HK).
-cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
-                             int with_order, cudaStream_t st);
+cudaError_t launch_tree_prep(const int32_t* parent, const int32_t* lengths, const float* g, int T, int B, int H,
+                             const Ws& ws, int with_order, cudaStream_t st);
 cudaError_t launch_verify_neumann(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                   const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
                                   int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
-                                 int o_bf16, float scale, const Ws& ws, int inputs_ready, int state_ready,
-                                 cudaStream_t st);
+                                 const float* S0, const int32_t* parent, const int32_t* lengths, int T, int B, int H,
+                                 int HK, void* o, int o_bf16, float scale, const Ws& ws, int inputs_ready,
+                                 int state_ready, cudaStream_t st);
 cudaError_t launch_verify_tc_big(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
-                                 int o_bf16, float scale, const Ws& ws, cudaStream_t st);
+                                 const float* S0, const int32_t* parent, const int32_t* lengths, int T, int B, int H,
+                                 int HK, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
-                               const float* S0, int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale,
-                               const Ws& ws, cudaStream_t st);
+                               const float* S0, const int32_t* lengths, int T, int B, int H, int HK, int d, void* o,
+                               int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 cudaError_t launch_gram_tc(const void* q, const void* k, const void* v, const float* beta, const float* S0, int T,
                            int B, int H, int HK, const Ws& ws, cudaStream_t st);
-cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
-                          const void* k, int in_bf16, int T, int B, int H, int HK, int d, const Ws& ws,
+cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const int32_t* lengths, const float* S0,
+                          float* S_new, const void* k, int in_bf16, int T, int B, int H, int HK, int d, const Ws& ws,
                           int state_ready, cudaStream_t st);
 cudaError_t launch_serial(const void* q, const void* k, const void* v, int in_bf16, const float* g,
                           const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
                           int d, void* o, int o_bf16, float scale, float* snap, int32_t* err, cudaStream_t st);
 cudaError_t launch_path_replay(const void* q, const void* k, const void* v, int in_bf16, const float* g,
-                               const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
-                               int d, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
+                               const float* beta, const float* S0, const int32_t* parent, const int32_t* lengths,
+                               int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale, const Ws& ws,
+                               cudaStream_t st);
 cudaError_t launch_solve_variant(int variant, int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws,
                                  cudaStream_t st);
 cudaError_t launch_tree_conv(const void* x, int bf16, const float* state, const float* w, const float* bias,
@@ -107,15 +108,16 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g, int T, int
     if (!aligned16(parent) || !aligned16(g) || !aligned16(workspace)) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, HV)) return CANOPY_ERR_UNSUPPORTED;
     Ws ws = ws_bind(workspace, B, T, HV, 32);  // tree-prep regions do not depend on dv
-    return cuda_status(launch_tree_prep(parent, g, T, B, HV, ws, 1, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_tree_prep(parent, nullptr, g, T, B, HV, ws, 1, static_cast<cudaStream_t>(stream)));
 }
 
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
-                                 const float* g, const float* beta, const float* S0, const int32_t* parent, int T,
-                                 int B, int H, int HV, int dk, int dv, float scale, canopy_solve solve, void* o,
-                                 canopy_dtype o_dtype, void* workspace, unsigned flags, void* stream) {
+                                 const float* g, const float* beta, const float* S0, const int32_t* parent,
+                                 const int32_t* lengths, int T, int B, int H, int HV, int dk, int dv, float scale,
+                                 canopy_solve solve, void* o, canopy_dtype o_dtype, void* workspace, unsigned flags,
+                                 void* stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
-        !aligned16(parent) || !aligned16(o) || !aligned16(workspace))
+        !aligned16(parent) || !aligned16(o) || !aligned16(workspace) || (lengths && !aligned16(lengths)))
         return CANOPY_ERR_ARG;
     if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
         (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN && solve != CANOPY_SOLVE_SQUARING &&
@@ -130,20 +132,23 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     const bool tc = in_bf16 && dk == 128 && T <= 64;
     // the solve variants run on the tensor-core Gram's tiles (bf16, d = 128)
     if (solve != CANOPY_SOLVE_FWDSUB && !(in_bf16 && dk == 128)) return CANOPY_ERR_UNSUPPORTED;
+    if (solve != CANOPY_SOLVE_FWDSUB && lengths) return CANOPY_ERR_UNSUPPORTED;  // uniform T only
     if (solve == CANOPY_SOLVE_FWDSUB && path_replay_wins(T, B, HV))
-        return cuda_status(launch_path_replay(q, k, v, in_bf16, g, beta, S0, parent, T, B, HV, H, dk, o, o_bf16,
-                                              scale, ws, st));
+        return cuda_status(launch_path_replay(q, k, v, in_bf16, g, beta, S0, parent, lengths, T, B, HV, H, dk, o,
+                                              o_bf16, scale, ws, st));
     if (tc && solve == CANOPY_SOLVE_NEUMANN)
         return cuda_status(
             launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
     if (tc && solve == CANOPY_SOLVE_FWDSUB)
-        return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws,
+        return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, lengths, T, B, HV, H, o, o_bf16, scale,
+                                                ws,
                                                 (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
                                                 (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
     // bf16 inputs beyond one 64-node block: one tensor-core launch, blocks in order
     if (in_bf16 && dk == 128 && solve == CANOPY_SOLVE_FWDSUB)
-        return cuda_status(launch_verify_tc_big(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
-    cudaError_t e = launch_tree_prep(parent, g, T, B, HV, ws, 0, st);
+        return cuda_status(
+            launch_verify_tc_big(q, k, v, g, beta, S0, parent, lengths, T, B, HV, H, o, o_bf16, scale, ws, st));
+    cudaError_t e = launch_tree_prep(parent, lengths, g, T, B, HV, ws, 0, st);
     if (e != cudaSuccess) return CANOPY_ERR_CUDA;
     if (solve != CANOPY_SOLVE_FWDSUB) {
         // Neumann beyond 64 nodes, squaring and split: Gram tiles, then the solve
@@ -152,21 +157,23 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
         return cuda_status(launch_solve_variant(int(solve), T, B, HV, o, o_bf16, scale, ws, st));
     }
     // fp32 inputs, or dk = dv = 32: CUDA cores
-    return cuda_status(launch_verify_simt(q, k, v, in_bf16, beta, S0, T, B, HV, H, dk, o, o_bf16, scale, ws, st));
+    return cuda_status(
+        launch_verify_simt(q, k, v, in_bf16, beta, S0, lengths, T, B, HV, H, dk, o, o_bf16, scale, ws, st));
 }
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,
-                            const int32_t* parent, canopy_dtype in_dtype, int T, int B, int H, int HV, int dk,
-                            int dv, const void* workspace, unsigned flags, void* stream) {
+                            const int32_t* parent, const int32_t* lengths, canopy_dtype in_dtype, int T, int B,
+                            int H, int HV, int dk, int dv, const void* workspace, unsigned flags, void* stream) {
     if (!aligned16(accepted) || !aligned16(S0) || !aligned16(S_new) || !aligned16(k) || !aligned16(parent) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (lengths && !aligned16(lengths)))
         return CANOPY_ERR_ARG;
     if (in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) return CANOPY_ERR_ARG;
     if (flags & ~CANOPY_COMMIT_STATE_READY) return CANOPY_ERR_ARG;
     if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
     if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
     Ws ws = ws_bind(const_cast<void*>(workspace), B, T, HV, dv);
-    return cuda_status(launch_commit(accepted, parent, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, HV, H, dk, ws,
+    return cuda_status(launch_commit(accepted, parent, lengths, S0, S_new, k, in_dtype == CANOPY_BF16, T, B, HV, H,
+                                     dk, ws,
                                      (flags & CANOPY_COMMIT_STATE_READY) != 0, static_cast<cudaStream_t>(stream)));
 }
 

@@ -73,7 +73,8 @@ __device__ __forceinline__ void stage_wu(CommitSmem<InT, DK, DV>& S, const Ws& w
 
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ accepted,
-                                                    const int32_t* __restrict__ parent, const float* S0,
+                                                    const int32_t* __restrict__ parent,
+                                                    const int32_t* __restrict__ lengths, const float* S0,
                                                     float* S_new, const InT* __restrict__ k, int T, int H, int HK,
                                                     Ws ws, int state_ready) {
     using Sm = CommitSmem<InT, DK, DV>;
@@ -105,12 +106,16 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
         }
     }
     if (t < 32) {
-        for (int j = t; j < T; j += 32) S.par[j] = parent[size_t(b) * T + j];
+        // the stream's nodes: lengths[b] of the T-strided arrays (all T without lengths)
+        int lbad = 0;
+        const int Tb = stream_len(lengths, b, T, &lbad);
+        for (int j = t; j < Tb; j += 32) S.par[j] = parent[size_t(b) * T + j];
         int a = accepted[b];
         __syncwarp();
         if (t == 0) {
-            const int bad = (a < -1 || a >= T) ? 1 : 0;
+            int bad = (a < -1 || a >= Tb) ? CANOPY_DEVERR_ACCEPTED : 0;
             if (bad) a = -1;
+            bad |= lbad;
             // path(a) from a up to the root, parents sanitised as the verify
             // sanitises them (node 0 is the root; a parent outside [0, j)
             // reads as 0), so the walk ends within a + 1 steps
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     const int nch = (n + CH - 1) / CH;
     stage_k(S, k, b, T, HK, hk, 0, min(CH, n));
     if (state_ready) pdl_wait();
-    if (S.bad && t == 0 && h == 0 && blockIdx.x == 0) raise_err(ws.err, CANOPY_DEVERR_ACCEPTED);
+    if (S.bad && t == 0 && h == 0 && blockIdx.x == 0) raise_err(ws.err, S.bad);
     const float la = (n > 0) ? ws.l[(size_t(b) * T + S.path[0]) * H + h] : 0.f;
     const float gamma_a = (n > 0) ? expf(la) : 1.f;
     stage_wu(S, ws, b, T, H, h, la, 0, min(CH, n));
@@ -179,9 +184,9 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
 }  // namespace cm
 
 template <typename InT, int D>
-static cudaError_t launch_commit_typed(const int32_t* accepted, const int32_t* parent, const float* S0,
-                                       float* S_new, const void* k, int T, int B, int H, int HK, const Ws& ws,
-                                       int state_ready, cudaStream_t st) {
+static cudaError_t launch_commit_typed(const int32_t* accepted, const int32_t* parent, const int32_t* lengths,
+                                       const float* S0, float* S_new, const void* k, int T, int B, int H, int HK,
+                                       const Ws& ws, int state_ready, cudaStream_t st) {
     const size_t smem = sizeof(cm::CommitSmem<InT, D, D>);
     static bool attr = false;
     if (!attr) {
@@ -192,21 +197,22 @@ static cudaError_t launch_commit_typed(const int32_t* accepted, const int32_t* p
     }
     const int nt = (D / cm::ROWS < cm::TPC) ? D / cm::ROWS : cm::TPC;
     return launch_pdl(cm::commit_kernel<InT, D, D>, dim3(D / cm::ROWS / nt, H, B), dim3(cm::NT), smem, st, accepted,
-                      parent, S0, S_new,
-                      static_cast<const InT*>(k), T, H, HK, ws, state_ready);
+                      parent, lengths, S0, S_new, static_cast<const InT*>(k), T, H, HK, ws, state_ready);
 }
 
-cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const float* S0, float* S_new,
-                          const void* k, int in_bf16, int T, int B, int H, int HK, int d, const Ws& ws,
+cudaError_t launch_commit(const int32_t* accepted, const int32_t* parent, const int32_t* lengths, const float* S0,
+                          float* S_new, const void* k, int in_bf16, int T, int B, int H, int HK, int d, const Ws& ws,
                           int state_ready, cudaStream_t st) {
     using bf = __nv_bfloat16;
-    const int sr = state_ready;
+#define CANOPY_COMMIT(IT, D) \
+    return launch_commit_typed<IT, D>(accepted, parent, lengths, S0, S_new, k, T, B, H, HK, ws, state_ready, st)
     if (d == 128) {
-        if (in_bf16) return launch_commit_typed<bf, 128>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
-        return launch_commit_typed<float, 128>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
+        if (in_bf16) CANOPY_COMMIT(bf, 128);
+        CANOPY_COMMIT(float, 128);
     }
-    if (in_bf16) return launch_commit_typed<bf, 32>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
-    return launch_commit_typed<float, 32>(accepted, parent, S0, S_new, k, T, B, H, HK, ws, sr, st);
+    if (in_bf16) CANOPY_COMMIT(bf, 32);
+    CANOPY_COMMIT(float, 32);
+#undef CANOPY_COMMIT
 }
 
 }  // namespace canopy

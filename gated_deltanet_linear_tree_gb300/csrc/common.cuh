@@ -107,6 +107,19 @@ __device__ inline bool gate_ok(float a, float b) {
 
 __device__ inline void raise_err(int32_t* err, int bits) { atomicOr(err, bits); }
 
+// Nodes of stream b in a ragged batch: lengths[b], or T without lengths.  A
+// value outside [0, T] is read as the nearest bound and sets
+// CANOPY_DEVERR_LENGTH in *bad.
+__device__ inline int stream_len(const int32_t* lengths, int b, int T, int* bad) {
+    if (!lengths) return T;
+    const int n = lengths[b];
+    if (n < 0 || n > T) {
+        *bad |= CANOPY_DEVERR_LENGTH;
+        return n < 0 ? 0 : T;
+    }
+    return n;
+}
+
 // ---------------------------------------------------------------------------
 // Bounded waits use the global nanosecond timer.
 

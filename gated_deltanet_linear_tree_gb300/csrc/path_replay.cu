@@ -28,8 +28,9 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
                                                           const InT* __restrict__ v, const float* __restrict__ g,
                                                           const float* __restrict__ beta,
                                                           const float* __restrict__ S0,
-                                                          const int32_t* __restrict__ parent, OutT* __restrict__ o,
-                                                          int T, int H, int ratio, float scale, Ws ws) {
+                                                          const int32_t* __restrict__ parent,
+                                                          const int32_t* __restrict__ lengths, OutT* __restrict__ o,
+                                                          int Ts, int H, int ratio, float scale, Ws ws) {
     constexpr int C4 = DK / 32;  // float4 chunks per lane
     __shared__ int sPar[MAXT];
     __shared__ float sA[MAXT], sB[MAXT];
@@ -38,15 +39,17 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
     const int vr = rt * ROWS + row;
     const int hk = (ratio == 1) ? h : h / ratio;  // the key head this value head reads
 
+    // Ts is the stride of every [B][T] array, T this stream's node count
     int bad = 0;
+    const int T = stream_len(lengths, b, Ts, &bad);
     if (t < T) {
         const int i = t;
-        int p = parent[size_t(b) * T + i];
+        int p = parent[size_t(b) * Ts + i];
         if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) {
             bad |= CANOPY_DEVERR_TREE;
             p = (i == 0) ? -1 : 0;
         }
-        float a = g[(size_t(b) * T + i) * H + h], be = beta[(size_t(b) * T + i) * H + h];
+        float a = g[(size_t(b) * Ts + i) * H + h], be = beta[(size_t(b) * Ts + i) * H + h];
         if (!gate_ok(a, be)) {
             bad |= CANOPY_DEVERR_GATE;
             a = 1.f;
@@ -71,10 +74,10 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
                 ++d;
             }
         }
-        ws.l[(size_t(b) * T + i) * H + h] = l;
+        ws.l[(size_t(b) * Ts + i) * H + h] = l;
         if (h == 0) {
-            ws.depth[size_t(b) * T + i] = d;
-            ws.mask[(size_t(b) * T + i) * ws.W] = m;  // T <= 8: one word
+            ws.depth[size_t(b) * Ts + i] = d;
+            ws.mask[(size_t(b) * Ts + i) * ws.W] = m;  // T <= 8: one word
         }
     }
 
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
         float coef = 0.f;
         for (int e = n - 1; e >= 0; --e) {
             const int j = path[e];
-            const size_t krow = (size_t(b) * T + j) * (H / ratio) + hk;
+            const size_t krow = (size_t(b) * Ts + j) * (H / ratio) + hk;
             float4 kk[C4];
 #pragma unroll
             for (int c = 0; c < C4; ++c) kk[c] = load4(k + krow * DK + (c * 8 + gl) * 4);
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
             sk += __shfl_xor_sync(0xffffffffu, sk, 2);
             sk += __shfl_xor_sync(0xffffffffu, sk, 1);
             const float a = sA[j], be = sB[j];
-            const float vv = to_f(v[((size_t(b) * T + j) * H + h) * DV + vr]);
+            const float vv = to_f(v[((size_t(b) * Ts + j) * H + h) * DV + vr]);
             coef = be * (vv - a * sk);
 #pragma unroll
             for (int c = 0; c < C4; ++c) {
@@ -114,8 +117,8 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
                 s[c].w = a * s[c].w + coef * kk[c].w;
             }
         }
-        const size_t nrow = (size_t(b) * T + i) * H + h;
-        const size_t qrow = (size_t(b) * T + i) * (H / ratio) + hk;
+        const size_t nrow = (size_t(b) * Ts + i) * H + h;
+        const size_t qrow = (size_t(b) * Ts + i) * (H / ratio) + hk;
         float4 qq[C4];
 #pragma unroll
         for (int c = 0; c < C4; ++c) qq[c] = load4(q + qrow * DK + (c * 8 + gl) * 4);
@@ -136,23 +139,24 @@ __global__ void __launch_bounds__(128) path_replay_kernel(const InT* __restrict_
 
 template <typename InT, typename OutT, int D>
 static cudaError_t launch_pr_typed(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                   const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
-                                   float scale, const Ws& ws, cudaStream_t st) {
+                                   const float* S0, const int32_t* parent, const int32_t* lengths, int T, int B, int H,
+                                   int HK, void* o, float scale, const Ws& ws, cudaStream_t st) {
     dim3 grid(D / pr::ROWS, H, B);
     pr::path_replay_kernel<InT, OutT, D, D><<<grid, 128, 0, st>>>(
         static_cast<const InT*>(q), static_cast<const InT*>(k), static_cast<const InT*>(v), g, beta, S0, parent,
-        static_cast<OutT*>(o), T, H, H / HK, scale, ws);
+        lengths, static_cast<OutT*>(o), T, H, H / HK, scale, ws);
     return cudaGetLastError();
 }
 
 int path_replay_max_t() { return pr::MAXT; }
 
 cudaError_t launch_path_replay(const void* q, const void* k, const void* v, int in_bf16, const float* g,
-                               const float* beta, const float* S0, const int32_t* parent, int T, int B, int H, int HK,
-                               int d, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st) {
+                               const float* beta, const float* S0, const int32_t* parent, const int32_t* lengths,
+                               int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale, const Ws& ws,
+                               cudaStream_t st) {
     if (T > pr::MAXT) return cudaErrorInvalidValue;
 #define CANOPY_PR(IT, OT, D) \
-    return launch_pr_typed<IT, OT, D>(q, k, v, g, beta, S0, parent, T, B, H, HK, o, scale, ws, st)
+    return launch_pr_typed<IT, OT, D>(q, k, v, g, beta, S0, parent, lengths, T, B, H, HK, o, scale, ws, st)
     using bf = __nv_bfloat16;
     if (d == 128) {
         if (in_bf16) {

@@ -14,7 +14,8 @@ namespace prep {
 constexpr int HC = 4;  // heads per CTA
 
 __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restrict__ parent,
-                                                        const float* __restrict__ g, int T, int H, Ws ws,
+                                                        const int32_t* __restrict__ lengths,
+                                                        const float* __restrict__ g, int Ts, int H, Ws ws,
                                                         int with_order) {
     __shared__ int sPtr[kMaxT];
     __shared__ int sLen[kMaxT];
@@ -29,9 +30,14 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
     const int b = blockIdx.x, i = threadIdx.x;
     const int hc = blockIdx.y;            // this CTA's HC heads
     const bool lead = hc == 0;            // writes the per-stream outputs
+    // Ts is the stride of every [B][T] array, T this stream's node count
+    // (nodes past it are neither read nor written)
+    int lbad = 0;
+    const int T = stream_len(lengths, b, Ts, &lbad);
+    if (lbad && lead && i == 0) raise_err(ws.err, lbad);
     int bad = 0;
     if (i < T) {
-        int par = parent[size_t(b) * T + i];
+        int par = parent[size_t(b) * Ts + i];
         const bool ok = (i == 0) ? (par == -1) : (par >= 0 && par < i);
         if (!ok) {
             bad |= CANOPY_DEVERR_TREE;
@@ -47,11 +53,11 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
 
     // depth and strict-ancestor mask
     if (lead && i < T) {
-        ws.depth[size_t(b) * T + i] = sLen[i] - 1;
+        ws.depth[size_t(b) * Ts + i] = sLen[i] - 1;
         for (int w = 0; w < ws.W; ++w) {
             uint64_t word = sM[i * 4 + (w >> 1)];
             if ((w >> 1) == (i >> 6)) word &= ~(1ull << (i & 63));
-            ws.mask[(size_t(b) * T + i) * ws.W + w] = uint32_t(word >> (32 * (w & 1)));
+            ws.mask[(size_t(b) * Ts + i) * ws.W + w] = uint32_t(word >> (32 * (w & 1)));
         }
     }
 
@@ -63,7 +69,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
         __syncthreads();
         for (int e = i; e < T * hn; e += blockDim.x) {
             const int n = e / hn, hh = e % hn;
-            float a = g[(size_t(b) * T + n) * H + h0 + hh];
+            float a = g[(size_t(b) * Ts + n) * H + h0 + hh];
             if (!(a > 0.f) || !isfinite(a)) {
                 badg = CANOPY_DEVERR_GATE;
                 a = 1.f;
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
         }
         for (int e = i; e < T * hn; e += blockDim.x) {
             const int n = e / hn, hh = e % hn;
-            ws.l[(size_t(b) * T + n) * H + h0 + hh] = float(sLg[n * HC + hh]);
+            ws.l[(size_t(b) * Ts + n) * H + h0 + hh] = float(sLg[n * HC + hh]);
         }
     }
     if (badg) raise_err(ws.err, badg);
@@ -117,14 +123,15 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(const int32_t* __restric
         }
     }
     __syncthreads();
-    if (i < T) ws.order[size_t(b) * T + sPos[i]] = i;
+    if (i < T) ws.order[size_t(b) * Ts + sPos[i]] = i;
 }
 
 }  // namespace prep
 
-cudaError_t launch_tree_prep(const int32_t* parent, const float* g, int T, int B, int H, const Ws& ws,
-                             int with_order, cudaStream_t st) {
-    prep::tree_prep_kernel<<<dim3(B, (H + prep::HC - 1) / prep::HC), 256, 0, st>>>(parent, g, T, H, ws, with_order);
+cudaError_t launch_tree_prep(const int32_t* parent, const int32_t* lengths, const float* g, int T, int B, int H,
+                             const Ws& ws, int with_order, cudaStream_t st) {
+    const dim3 grid(B, (H + prep::HC - 1) / prep::HC);
+    prep::tree_prep_kernel<<<grid, 256, 0, st>>>(parent, lengths, g, T, H, ws, with_order);
     return cudaGetLastError();
 }
 

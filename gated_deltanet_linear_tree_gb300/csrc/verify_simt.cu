@@ -41,7 +41,8 @@ __device__ inline void load8(const float* p, float (&x)[8]) {
 template <typename InT, int DK, int DV>
 __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, const InT* __restrict__ k,
                                                    const InT* __restrict__ v, const float* __restrict__ beta,
-                                                   const float* __restrict__ S0, int T, int H, int HK, Ws ws) {
+                                                   const float* __restrict__ S0, const int32_t* __restrict__ lengths,
+                                                   int Ts, int H, int HK, Ws ws) {
     constexpr int GROUPS = 256 / DV;          // row groups for the S0 products
     constexpr int RPG = ROWS / GROUPS;        // rows per group
     __shared__ float sq[ROWS][DK];
@@ -49,6 +50,8 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
     __shared__ float sS0[DV][33];
     __shared__ int sPathList[8][kMaxT];
     const int i0 = blockIdx.x * ROWS, h = blockIdx.y, b = blockIdx.z;
+    int lbad = 0;  // (reported by tree prep)
+    const int T = stream_len(lengths, b, Ts, &lbad);  // this stream's nodes; Ts is the stride
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const size_t rowstride = size_t(HK) * DK;   // q and k rows: key heads
     const int hk = h / (H / HK);                // the key head this value head reads
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
         const int r = e / DK, d = e % DK, i = i0 + r;
         float xq = 0.f, xk = 0.f;
         if (i < T) {
-            const size_t off = (size_t(b) * T + i) * rowstride + size_t(hk) * DK + d;
+            const size_t off = (size_t(b) * Ts + i) * rowstride + size_t(hk) * DK + d;
             xq = to_f(q[off]);
             xk = to_f(k[off]);
         }
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
     for (int r = 0; r < RPG; ++r) {
         const int i = i0 + grp * RPG + r;
         if (i < T) {
-            const size_t n = (size_t(b) * T + i) * H + h;
+            const size_t n = (size_t(b) * Ts + i) * H + h;
             const float gam = expf(ws.l[n]);
             const float be = beta[n];
             const float vv = to_f(v[n * DV + vcol]);
@@ -108,9 +111,9 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
     for (int r = warp; r < ROWS; r += 8) {
         const int i = i0 + r;
         if (i >= T) break;
-        const size_t ni = (size_t(b) * T + i) * H + h;
+        const size_t ni = (size_t(b) * Ts + i) * H + h;
         const float li = ws.l[ni], bi = beta[ni];
-        const uint32_t* mrow = ws.mask + (size_t(b) * T + i) * ws.W;
+        const uint32_t* mrow = ws.mask + (size_t(b) * Ts + i) * ws.W;
         uint32_t word = (lane < ws.W) ? mrow[lane] : 0u;
         if (lane == (i >> 5)) word |= 1u << (i & 31);  // path(i) = A(i) + {i}
         const int cntw = __popc(word);
@@ -124,11 +127,11 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
         off -= cntw;
         for (uint32_t bits = word; bits; bits &= bits - 1) plist[off++] = 32 * lane + __ffs(bits) - 1;
         __syncwarp();
-        float* Grow = ws.gs + ((size_t(b) * H + h) * T + i) * T;
-        float* Crow = ws.cs + ((size_t(b) * H + h) * T + i) * T;
+        float* Grow = ws.gs + ((size_t(b) * H + h) * Ts + i) * Ts;
+        float* Crow = ws.cs + ((size_t(b) * H + h) * Ts + i) * Ts;
         for (int p = lane; p < n; p += 32) {
             const int j = plist[p];
-            const InT* kj = k + (size_t(b) * T + j) * rowstride + size_t(hk) * DK;
+            const InT* kj = k + (size_t(b) * Ts + j) * rowstride + size_t(hk) * DK;
             float kk0 = 0.f, kk1 = 0.f, qk0 = 0.f, qk1 = 0.f;
 #pragma unroll 2
             for (int d = 0; d < DK; d += 8) {
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const InT* __restrict__ q, co
                     qk1 += sq[r][d + e + 1] * x[e + 1];
                 }
             }
-            const float gam = expf(li - ws.l[(size_t(b) * T + j) * H + h]);
+            const float gam = expf(li - ws.l[(size_t(b) * Ts + j) * H + h]);
             Grow[j] = (j == i) ? 0.f : bi * gam * (kk0 + kk1);
             Crow[j] = gam * (qk0 + qk1);
         }
@@ -170,11 +173,12 @@ __host__ __device__ constexpr size_t solve_smem(int T, int DV) {
 // into a list and stages (j, G_ij, C_ij); then the chunk's nodes are solved
 // level by level, each group taking nodes of the level.
 template <typename OutT, int DV>
-__device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, const Ws& ws, float scale) {
+__device__ __forceinline__ void level_solve(OutT* __restrict__ o, const int32_t* __restrict__ lengths, int Ts, int H,
+                                            const Ws& ws, float scale) {
     constexpr int NG = SOLVE_NT / DV;
     extern __shared__ float smem[];
     float* sU = smem;                                       // [T][DV]
-    int* sOrder = reinterpret_cast<int*>(sU + size_t(T) * DV);  // [kMaxT] nodes by depth
+    int* sOrder = reinterpret_cast<int*>(sU + size_t(Ts) * DV);  // [kMaxT] nodes by depth
     int* sOff = sOrder + kMaxT;                             // [kMaxT + 1] level offsets
     int* sCnt = sOff + kMaxT + 1;                           // [kMaxT] nodes per level, then fill counters
     int* sNode = sCnt + kMaxT;                              // [CHN]
@@ -191,13 +195,15 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
     const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
     const int lane = t & 31, warp = t >> 5;
     const size_t bh = size_t(b) * H + h;
+    int lbad = 0;  // (reported by tree prep)
+    const int T = stream_len(lengths, b, Ts, &lbad);  // this stream's nodes; Ts is the stride
 
     for (int d = t; d < kMaxT; d += SOLVE_NT) sCnt[d] = 0;
     if (t == 0) sMaxD = 0;
     __syncthreads();
     int myd = 0;
     if (t < T) {
-        myd = ws.depth[size_t(b) * T + t];
+        myd = ws.depth[size_t(b) * Ts + t];
         myd = min(max(myd, 0), kMaxT - 1);
         atomicAdd(&sCnt[myd], 1);
         atomicMax(&sMaxD, myd);
@@ -218,8 +224,8 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
     __syncthreads();
 
     const int c = t % DV, grp = t / DV;
-    const float* gsb = ws.gs + bh * T * T;
-    const float* csb = ws.cs + bh * T * T;
+    const float* gsb = ws.gs + bh * Ts * Ts;
+    const float* csb = ws.cs + bh * Ts * Ts;
     // Chunks of CHN nodes in level order, across level boundaries: a chunk's
     // ancestor lists and coefficients are staged in one round (they depend
     // on nothing solved yet), then its nodes are solved level by level.
@@ -229,7 +235,7 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
         // stage the chunk's ancestor lists and coefficients (one warp per node)
         if (warp < cn) {
             const int e = warp, i = sOrder[c0 + e];
-            const uint32_t word = (lane < ws.W) ? ws.mask[(size_t(b) * T + i) * ws.W + lane] : 0u;
+            const uint32_t word = (lane < ws.W) ? ws.mask[(size_t(b) * Ts + i) * ws.W + lane] : 0u;
             const int cntw = __popc(word);
             int off = cntw;
 #pragma unroll
@@ -242,8 +248,8 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
             int* jrow = sJ + e * PSTRIDE;
             for (uint32_t bits = word; bits; bits &= bits - 1) jrow[off++] = 32 * lane + __ffs(bits) - 1;
             __syncwarp();
-            const float* grow = gsb + size_t(i) * T;
-            const float* crow = csb + size_t(i) * T;
+            const float* grow = gsb + size_t(i) * Ts;
+            const float* crow = csb + size_t(i) * Ts;
             // all of a lane's loads in flight at once (paths up to 256 long)
             for (int p0 = lane; p0 < n; p0 += 32 * 8) {
                 int jj[8];
@@ -268,7 +274,7 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
                 sCii[e] = crow[i];
             }
             // the node's R and gamma X_Q rows
-            const size_t ni = (size_t(b) * T + i) * H + h;
+            const size_t ni = (size_t(b) * Ts + i) * H + h;
             for (int cc = lane * 4; cc < DV; cc += 128) {
                 *reinterpret_cast<float4*>(sRr + e * DV + cc) = *reinterpret_cast<const float4*>(ws.rr + ni * DV + cc);
                 *reinterpret_cast<float4*>(sXq + e * DV + cc) = *reinterpret_cast<const float4*>(ws.xq + ni * DV + cc);
@@ -323,7 +329,7 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
                         out += pq.y;
                     }
                     const int i = sNode[e];
-                    const size_t ni = (size_t(b) * T + i) * H + h;
+                    const size_t ni = (size_t(b) * Ts + i) * H + h;
                     acc += sRr[e * DV + c];
                     out += sXq[e * DV + c] + sCii[e] * acc;
                     sU[i * DV + c] = acc;
@@ -333,7 +339,7 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
             } else {
                 for (int e = s0 + grp; e < s1; e += NG) {
                     const int i = sNode[e], n = sLen[e];
-                    const size_t ni = (size_t(b) * T + i) * H + h;
+                    const size_t ni = (size_t(b) * Ts + i) * H + h;
                     const int* jrow = sJ + e * PSTRIDE;
                     const float* gr = sG + e * PSTRIDE;
                     const float* cr = sC + e * PSTRIDE;
@@ -366,20 +372,22 @@ __device__ __forceinline__ void level_solve(OutT* __restrict__ o, int T, int H, 
 }
 
 template <typename OutT, int DV>
-__global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict__ o, int T, int H, Ws ws,
+__global__ void __launch_bounds__(SOLVE_NT) solve_level_kernel(OutT* __restrict__ o,
+                                                               const int32_t* __restrict__ lengths, int T, int H, Ws ws,
                                                                float scale) {
-    level_solve<OutT, DV>(o, T, H, ws, scale);
+    level_solve<OutT, DV>(o, lengths, T, H, ws, scale);
 }
 
 }  // namespace simt
 
 template <typename InT, int DK, int DV>
 static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v, const float* beta,
-                                     const float* S0, int T, int B, int H, int HK, void* o, int o_bf16, float scale,
-                                     const Ws& ws, cudaStream_t st) {
+                                     const float* S0, const int32_t* lengths, int T, int B, int H, int HK, void* o,
+                                     int o_bf16, float scale, const Ws& ws, cudaStream_t st) {
     dim3 g1((T + simt::ROWS - 1) / simt::ROWS, H, B);
     simt::gram_kernel<InT, DK, DV><<<g1, 256, 0, st>>>(static_cast<const InT*>(q), static_cast<const InT*>(k),
-                                                      static_cast<const InT*>(v), beta, S0, T, H, HK, ws);
+                                                      static_cast<const InT*>(v), beta, S0, lengths, T, H, HK,
+                                                      ws);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g2(H, B);
@@ -394,7 +402,7 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
             attr = true;
         }
         simt::solve_level_kernel<__nv_bfloat16, DV><<<g2, simt::SOLVE_NT, smem, st>>>(
-            static_cast<__nv_bfloat16*>(o), T, H, ws, scale);
+            static_cast<__nv_bfloat16*>(o), lengths, T, H, ws, scale);
     } else {
         static bool attr = false;
         if (!attr) {
@@ -403,18 +411,19 @@ static cudaError_t launch_simt_typed(const void* q, const void* k, const void* v
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        simt::solve_level_kernel<float, DV><<<g2, simt::SOLVE_NT, smem, st>>>(static_cast<float*>(o), T, H, ws,
+        simt::solve_level_kernel<float, DV><<<g2, simt::SOLVE_NT, smem, st>>>(static_cast<float*>(o), lengths, T, H,
+                                                                              ws,
                                                                               scale);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_verify_simt(const void* q, const void* k, const void* v, int in_bf16, const float* beta,
-                               const float* S0, int T, int B, int H, int HK, int d, void* o, int o_bf16, float scale,
-                               const Ws& ws, cudaStream_t st) {
+                               const float* S0, const int32_t* lengths, int T, int B, int H, int HK, int d, void* o,
+                               int o_bf16, float scale, const Ws& ws, cudaStream_t st) {
     using bf = __nv_bfloat16;
 #define CANOPY_SIMT(IT, D) \
-    return launch_simt_typed<IT, D, D>(q, k, v, beta, S0, T, B, H, HK, o, o_bf16, scale, ws, st)
+    return launch_simt_typed<IT, D, D>(q, k, v, beta, S0, lengths, T, B, H, HK, o, o_bf16, scale, ws, st)
     if (d == 128) {
         if (in_bf16) CANOPY_SIMT(bf, 128);
         CANOPY_SIMT(float, 128);

@@ -113,6 +113,9 @@ struct Params {
     const float* g;
     const float* beta;
     const int32_t* parent;
+    const int32_t* lengths;  // per-stream node counts, or null (T everywhere)
+    void* o;                 // written directly (not by bulk store) where a
+    float* U;                //   stream ends inside a 32-node tile
     float* l;
     int32_t* depth;
     uint32_t* mask;
@@ -204,8 +207,10 @@ __global__ void __launch_bounds__(NT, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;   // TMEM lane quadrant of this warp
     const int h = blockIdx.x, b = blockIdx.y;
-    const int T = p.T, H = p.H;
-    const int nb = (T + TP - 1) / TP;
+    const int Ts = p.T, H = p.H;  // Ts: the stride of every [B][T] array
+    int lbad = 0;
+    const int T = stream_len(p.lengths, b, Ts, &lbad);  // this stream's nodes
+    const int nb = (T + TP - 1) / TP;                   // its 64-node blocks
     const int hk = h / p.ratio;
 
     // Nothing global is touched before the preceding kernel of the stream has
@@ -219,10 +224,12 @@ __global__ void __launch_bounds__(NT, 1)
         *sFlag = 0;
         // block 0's Q/K and V tiles and S0 boxes 0 and 1 are requested first,
         // so that they travel while the tree is prepared
-        load_qk_tile(sm, &tmQ, &tmK, &bars[BAR_QK], 0, hk, b);
-        mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
-        tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
-        tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
+        if (nb > 0) {
+            load_qk_tile(sm, &tmQ, &tmK, &bars[BAR_QK], 0, hk, b);
+            mbar_expect_tx(&bars[BAR_V], 2 * L::V_TILE);
+            tma_load_4d(sm + L::VT, &tmV, &bars[BAR_V], 0, h, 0, b);
+            tma_load_4d(sm + L::VT + L::V_TILE, &tmV, &bars[BAR_V], 64, h, 0, b);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_expect_tx(&bars[BAR_S0 + i], L::S0_BOX);
             tma_load_4d(sm + L::RX + i * L::S0_BOX, &tmS, &bars[BAR_S0 + i], 32 * i, 0, h, b);
@@ -235,15 +242,15 @@ __global__ void __launch_bounds__(NT, 1)
     }
     // Parents and gates, one thread per node; padded nodes (past T) have no
     // path, beta 0 and gamma 1.
-    int bad = 0;
+    int bad = (tid == 0) ? lbad : 0;
     if (tid < kMaxT) {
         const int i = tid;
         int par = -1;
         float ga = 1.f, gb = 0.f;
         if (i < T) {
-            par = p.parent[size_t(b) * T + i];
-            ga = p.g[(size_t(b) * T + i) * H + h];
-            gb = p.beta[(size_t(b) * T + i) * H + h];
+            par = p.parent[size_t(b) * Ts + i];
+            ga = p.g[(size_t(b) * Ts + i) * H + h];
+            gb = p.beta[(size_t(b) * Ts + i) * H + h];
             if (!((i == 0) ? (par == -1) : (par >= 0 && par < i))) {
                 bad |= CANOPY_DEVERR_TREE;
                 par = (i == 0) ? -1 : 0;
@@ -282,13 +289,13 @@ __global__ void __launch_bounds__(NT, 1)
     // tree outputs for the commit: l (natural log), depth, strict-ancestor mask
     if (bad) raise_err(p.err, bad);
     if (tid < T) {
-        p.l[(size_t(b) * T + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
+        p.l[(size_t(b) * Ts + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
         if (h == 0) {
-            p.depth[size_t(b) * T + tid] = sLen[tid] - 1;
+            p.depth[size_t(b) * Ts + tid] = sLen[tid] - 1;
             for (int w = 0; w < p.W; ++w) {
                 uint32_t word = uint32_t(sMask[tid * 4 + (w >> 1)] >> (32 * (w & 1)));
                 if (w == (tid >> 5)) word &= ~(1u << (tid & 31));
-                p.mask[(size_t(b) * T + tid) * p.W + w] = word;
+                p.mask[(size_t(b) * Ts + tid) * p.W + w] = word;
             }
         }
     }
@@ -629,7 +636,8 @@ __global__ void __launch_bounds__(NT, 1)
                     const float vv = __bfloat162float(
                         *reinterpret_cast<const __nv_bfloat16*>(vt + el * 128 + ((cb ^ (el & 7)) << 4) + cw));
                     xq[e] = __float_as_uint(p.scale * gm * __uint_as_float(xq[e]));
-                    xk[e] = __float_as_uint(be * (vv - gm * __uint_as_float(xk[e])));
+                    // nodes past the stream's length are exactly zero (their rows may hold anything)
+                    xk[e] = (i < T) ? __float_as_uint(be * (vv - gm * __uint_as_float(xk[e]))) : 0u;
                 }
                 tmem_st16(lane_base + TD + hb * 32, *reinterpret_cast<uint32_t(*)[16]>(xq));
                 tmem_st16(lane_base + TD + hb * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(xq + 16));
@@ -705,6 +713,18 @@ __global__ void __launch_bounds__(NT, 1)
             wait_or_flag(&bars[BAR_W], pr, sFlag);
             tc_fence_after();
             const bool keep_u = r + 1 < nb;
+            // a tile goes by bulk store if it lies inside the stream (or the
+            // stream runs to T, where the tensor's bound clips it); a tile the
+            // stream ends inside is written from registers, row by row
+            const size_t rstride = size_t(H) * DV;
+            const size_t obase = (size_t(b) * Ts * H + h) * DV + c;
+            bool bulk[2];
+            int rows[2];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                rows[half] = min(32, T - (n0 + 32 * half));
+                bulk[half] = rows[half] == 32 || (T == Ts && rows[half] > 0);
+            }
             if (tid == 128) bulk_wait_read<0>();  // the previous block's stores have read the staging tiles
             group_sync(2, 128);
 #pragma unroll 1
@@ -713,9 +733,16 @@ __global__ void __launch_bounds__(NT, 1)
                 tmem_ld16(lane_base + TD + 64 + half * 32, *reinterpret_cast<uint32_t(*)[16]>(y));
                 tmem_ld16(lane_base + TD + 64 + half * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(y + 16));
                 tmem_wait_ld();
-                float* st = reinterpret_cast<float*>(sm + L::ST + half * L::ST_BUF) + c;
+                if (bulk[half]) {
+                    float* st = reinterpret_cast<float*>(sm + L::ST + half * L::ST_BUF) + c;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) st[e * DV] = __uint_as_float(y[e]);
+                    for (int e = 0; e < 32; ++e) st[e * DV] = __uint_as_float(y[e]);
+                } else {
+                    float* up = p.U + obase + size_t(n0 + 32 * half) * rstride;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (e < rows[half]) up[e * rstride] = __uint_as_float(y[e]);
+                }
                 if (keep_u) {
                     uint32_t wh[16], wl[16];
 #pragma unroll
@@ -737,8 +764,8 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_before();
             group_sync(2, 128);  // D has been read and the U tiles are staged
             if (tid == 128) {
-                tma_store_4d(&tmU, sm + L::ST, 0, h, n0, b);
-                tma_store_4d(&tmU, sm + L::ST + L::ST_BUF, 0, h, n0 + 32, b);
+                if (bulk[0]) tma_store_4d(&tmU, sm + L::ST, 0, h, n0, b);
+                if (bulk[1]) tma_store_4d(&tmU, sm + L::ST + L::ST_BUF, 0, h, n0 + 32, b);
                 bulk_commit();
                 if (r + 1 < nb) {
                     // the next block's X = S0 [Q; K]^T
@@ -760,7 +787,20 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint8_t* stg = sm + L::ST + half * L::ST_BUF;
-                if (p.o_bf16) {
+                if (!bulk[half]) {
+                    const size_t orow = obase + size_t(n0 + 32 * half) * rstride;
+                    if (p.o_bf16) {
+                        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.o) + orow;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e < rows[half]) op[e * rstride] = __float2bfloat16_rn(__uint_as_float(yo[half][e]));
+                    } else {
+                        float* op = static_cast<float*>(p.o) + orow;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e < rows[half]) op[e * rstride] = __uint_as_float(yo[half][e]);
+                    }
+                } else if (p.o_bf16) {
                     __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg) + c;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) st[e * DV] = __float2bfloat16_rn(__uint_as_float(yo[half][e]));
@@ -773,8 +813,8 @@ __global__ void __launch_bounds__(NT, 1)
             fence_proxy_async_smem();
             group_sync(2, 128);
             if (tid == 128) {
-                tma_store_4d(&tmO, sm + L::ST, 0, h, n0, b);
-                tma_store_4d(&tmO, sm + L::ST + L::ST_BUF, 0, h, n0 + 32, b);
+                if (bulk[0]) tma_store_4d(&tmO, sm + L::ST, 0, h, n0, b);
+                if (bulk[1]) tma_store_4d(&tmO, sm + L::ST + L::ST_BUF, 0, h, n0 + 32, b);
                 bulk_commit();
             }
         }
@@ -818,8 +858,8 @@ bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 bool make_row_store_map(CUtensorMap* m, void* base, int bf16, int B, int T, int H);
 
 cudaError_t launch_verify_tc_big(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
-                                 int o_bf16, float scale, const Ws& ws, cudaStream_t st) {
+                                 const float* S0, const int32_t* parent, const int32_t* lengths, int T, int B, int H,
+                                 int HK, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st) {
     if (T <= tcb::TP || T > kMaxT) return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, ms, mo, mu;
     if (!make_bf16_row_map(&mq, q, B, T, HK) || !make_bf16_row_map(&mk, k, B, T, HK) ||
@@ -830,6 +870,9 @@ cudaError_t launch_verify_tc_big(const void* q, const void* k, const void* v, co
     prm.g = g;
     prm.beta = beta;
     prm.parent = parent;
+    prm.lengths = lengths;
+    prm.o = o;
+    prm.U = ws.U;
     prm.l = ws.l;
     prm.depth = ws.depth;
     prm.mask = ws.mask;

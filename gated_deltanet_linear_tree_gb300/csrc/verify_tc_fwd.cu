@@ -89,6 +89,7 @@ struct Params {
     const float* g;
     const float* beta;
     const int32_t* parent;
+    const int32_t* lengths;  // per-stream node counts, or null (T everywhere)
     void* o;
     float* U;
     float* l;
@@ -125,7 +126,8 @@ __device__ inline void wait_or_flag(uint64_t* bar, int* sFlag) {
 // 0..31, hb = 1: 32..63) for value column c (this thread's TMEM lane): X_K
 // from the accumulator columns, V from the shared tile, the result as bf16
 // hi + lo into the A-operand columns.
-__device__ __forceinline__ void r_pass(int hb, const uint8_t* sm, const float2* sBG, uint32_t lane_base, int c) {
+__device__ __forceinline__ void r_pass(int hb, const uint8_t* sm, const float2* sBG, uint32_t lane_base, int c,
+                                       int T) {
     const uint8_t* vt = sm + Smem::VT + (c >> 6) * Smem::V_TILE;
     const int cb = ((c & 63) >> 3), cw = (c & 7) << 1;
     uint32_t xk[32];
@@ -142,7 +144,8 @@ __device__ __forceinline__ void r_pass(int hb, const uint8_t* sm, const float2* 
             const float vv = __bfloat162float(
                 *reinterpret_cast<const __nv_bfloat16*>(vt + i * 128 + ((cb ^ (i & 7)) << 4) + cw));
             const float2 bg = sBG[i];
-            rv[s2] = bg.x * vv - bg.y * __uint_as_float(xk[2 * e + s2]);
+            // nodes past the stream's length are exactly zero (their rows may hold anything)
+            rv[s2] = (i < T) ? bg.x * vv - bg.y * __uint_as_float(xk[2 * e + s2]) : 0.f;
         }
         split2(rv[0], rv[1], wh[e], wl[e]);
     }
@@ -175,7 +178,9 @@ __global__ void __launch_bounds__(NT, 2)
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
     const bool solve = warp < 4;
     const int h = blockIdx.x, b = blockIdx.y;
-    const int T = p.T, H = p.H;
+    const int Ts = p.T, H = p.H;  // Ts: the stride of every [B][T] array
+    int lbad = 0;
+    const int T = stream_len(p.lengths, b, Ts, &lbad);  // this stream's nodes
 
     // Programmatic dependent launch: the next kernel may begin launching at
     // once.  With inputs_ready, until the preceding kernel has completed
@@ -191,9 +196,9 @@ __global__ void __launch_bounds__(NT, 2)
     int par = -1;
     float ga = 1.f, gb = 0.f;
     if (tid < TP && tid < T) {
-        par = p.parent[size_t(b) * T + tid];
-        ga = p.g[(size_t(b) * T + tid) * H + h];
-        gb = p.beta[(size_t(b) * T + tid) * H + h];
+        par = p.parent[size_t(b) * Ts + tid];
+        ga = p.g[(size_t(b) * Ts + tid) * H + h];
+        gb = p.beta[(size_t(b) * Ts + tid) * H + h];
     }
     uint8_t* sQK = sm + L::QK;
     if (tid == 0) {
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(NT, 2)
     }
     // Validate; padded nodes: no path, beta 0, gamma 1.  Error bits are kept
     // and raised with the tree outputs, after the preceding kernel is done.
-    int bad = 0;
+    int bad = (tid == 0) ? lbad : 0;
     if (tid < TP) {
         const int i = tid;
         if (i < T) {
@@ -422,12 +427,12 @@ __global__ void __launch_bounds__(NT, 2)
         if (tid < TP) pdl_wait();
         if (bad) raise_err(p.err, bad);
         if (tid < TP && tid < T) {
-            p.l[(size_t(b) * T + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
+            p.l[(size_t(b) * Ts + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
             if (h == 0) {
-                p.depth[size_t(b) * T + tid] = sLen[tid] - 1;
+                p.depth[size_t(b) * Ts + tid] = sLen[tid] - 1;
                 const uint64_t strict = sMask[tid] & ~(1ull << tid);
                 for (int w = 0; w < p.W; ++w)
-                    p.mask[(size_t(b) * T + tid) * p.W + w] = uint32_t(strict >> (32 * w));
+                    p.mask[(size_t(b) * Ts + tid) * p.W + w] = uint32_t(strict >> (32 * w));
             }
         }
 
@@ -525,8 +530,8 @@ __global__ void __launch_bounds__(NT, 2)
         wait_or_flag(&bars[BAR_PREP], sFlag);
         tc_fence_after();
         {
-            r_pass(0, sm, sBG, lane_base, c);
-            r_pass(1, sm, sBG, lane_base, c);
+            r_pass(0, sm, sBG, lane_base, c, T);
+            r_pass(1, sm, sBG, lane_base, c, T);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(NT, 2)
         const int c = quad * 32 + lane;
         const uint32_t col0 = solve ? TA + 64 : TD + 64;
         const size_t rstride = size_t(H) * DV;  // one node row of o or U
-        const size_t base = (size_t(b) * T * H + h) * DV + c;
+        const size_t base = (size_t(b) * Ts * H + h) * DV + c;
         pdl_wait();
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -632,9 +637,9 @@ bool make_bf16_row_map(CUtensorMap* m, const void* base, int B, int T, int H);
 bool make_state_map(CUtensorMap* m, const float* base, int B, int H);
 
 cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                 const float* S0, const int32_t* parent, int T, int B, int H, int HK, void* o,
-                                 int o_bf16, float scale, const Ws& ws, int inputs_ready, int state_ready,
-                                 cudaStream_t st) {
+                                 const float* S0, const int32_t* parent, const int32_t* lengths, int T, int B, int H,
+                                 int HK, void* o, int o_bf16, float scale, const Ws& ws, int inputs_ready,
+                                 int state_ready, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ms;
     if (!make_bf16_row_map(&mq, q, B, T, HK) || !make_bf16_row_map(&mk, k, B, T, HK) ||
         !make_bf16_row_map(&mv, v, B, T, H) || !make_state_map(&ms, S0, B, H))
@@ -643,6 +648,7 @@ cudaError_t launch_verify_tc_fwd(const void* q, const void* k, const void* v, co
     prm.g = g;
     prm.beta = beta;
     prm.parent = parent;
+    prm.lengths = lengths;
     prm.o = o;
     prm.U = ws.U;
     prm.l = ws.l;

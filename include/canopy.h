@@ -96,6 +96,7 @@ typedef enum {
 #define CANOPY_DEVERR_GATE     0x2  /* g <= 0, g or beta not finite                     */
 #define CANOPY_DEVERR_ACCEPTED 0x4  /* commit: accepted node not in [-1, T)             */
 #define CANOPY_DEVERR_TIMEOUT  0x8  /* an internal bounded wait gave up                 */
+#define CANOPY_DEVERR_LENGTH   0x10 /* verify/commit: lengths[b] not in [0, T]           */
 
 /* Size in bytes of the workspace one verify/commit pair needs, for HV value
  * heads.  It holds the pseudo-values U fp32 [B][T][HV][dv], the cumulative
@@ -164,12 +165,22 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
  * early too.  The workspace and o are written only after that kernel has
  * completed, whatever the flags.  CANOPY_VERIFY_STATE_READY without
  * CANOPY_VERIFY_INPUTS_READY has no effect; other bits return
- * CANOPY_ERR_ARG. */
+ * CANOPY_ERR_ARG.
+ * lengths (canopy page, "Design decisions", memory layout: the parent array
+ * plus a per-sequence length for ragged batches): device int32 [B], or NULL
+ * when every stream has T nodes.  Stream b's tree is nodes 0 .. lengths[b]-1
+ * (0 <= lengths[b] <= T; T stays the stride of every array).  The rows of
+ * q, k, v, g, beta and parent past a stream's length do not influence any
+ * result, whatever they hold, and the rows of o and of the workspace (U, l,
+ * depth, mask) past it are not written.  A length outside [0, T] sets
+ * CANOPY_DEVERR_LENGTH and is read as the nearest bound.  The solve variants
+ * (NEUMANN, SQUARING, SPLIT) take no lengths: non-NULL returns
+ * CANOPY_ERR_UNSUPPORTED. */
 canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, canopy_dtype in_dtype,
                                  const float* g, const float* beta, const float* S0,
-                                 const int32_t* parent, int T, int B, int H, int HV, int dk, int dv,
-                                 float scale, canopy_solve solve, void* o, canopy_dtype o_dtype,
-                                 void* workspace, unsigned flags, void* stream);
+                                 const int32_t* parent, const int32_t* lengths, int T, int B, int H, int HV,
+                                 int dk, int dv, float scale, canopy_solve solve, void* o,
+                                 canopy_dtype o_dtype, void* workspace, unsigned flags, void* stream);
 
 /* Commit (canopy page, "The tree closed form", last line, and "What the
  * commit kernel stores"): for every stream b with accepted node a = accepted[b],
@@ -187,11 +198,13 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
  * its k rows while that kernel finishes; the workspace and S_new are touched
  * only after it has completed.  Other bits return CANOPY_ERR_ARG.
  *   accepted device int32 [B]; S0, S_new device fp32 [B][HV][dv][dk];
- *   k device [B][T][H][dk] in in_dtype; parent device int32 [B][T]. */
+ *   k device [B][T][H][dk] in in_dtype; parent device int32 [B][T];
+ *   lengths: the verify call's (device int32 [B] or NULL); an accepted node
+ *   at or past its stream's length sets CANOPY_DEVERR_ACCEPTED and keeps S0. */
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new,
-                            const void* k, const int32_t* parent, canopy_dtype in_dtype, int T, int B,
-                            int H, int HV, int dk, int dv, const void* workspace, unsigned flags,
-                            void* stream);
+                            const void* k, const int32_t* parent, const int32_t* lengths,
+                            canopy_dtype in_dtype, int T, int B, int H, int HV, int dk, int dv,
+                            const void* workspace, unsigned flags, void* stream);
 
 /* Activation after the short convolution. */
 typedef enum { CANOPY_ACT_NONE = 0, CANOPY_ACT_SILU = 1 } canopy_activation;

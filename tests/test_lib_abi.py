@@ -85,11 +85,12 @@ def test_status_strings_and_version(lib):
     assert lib.canopy_version() >= 1
 
 
-def _verify(lib, ptrs, T=64, B=1, H=1, HV=None, d=128, in_dt=1, solve=0, o_dt=0, flags=0, scale=1.0):
+def _verify(lib, ptrs, T=64, B=1, H=1, HV=None, d=128, in_dt=1, solve=0, o_dt=0, flags=0, scale=1.0,
+            lengths=None):
     q, k, v, g, be, S0, par, o, ws = ptrs
     HV = H if HV is None else HV
-    return lib.canopy_tree_verify(q, k, v, in_dt, g, be, S0, par, T, B, H, HV, d, d, scale, solve, o, o_dt, ws,
-                                  flags, None)
+    return lib.canopy_tree_verify(q, k, v, in_dt, g, be, S0, par, lengths, T, B, H, HV, d, d, scale, solve, o,
+                                  o_dt, ws, flags, None)
 
 
 def test_host_argument_errors(lib):
@@ -116,16 +117,21 @@ def test_host_argument_errors(lib):
     assert _verify(lib, good, H=2, HV=1) == 1
     assert _verify(lib, good, scale=float("nan")) == 1
     assert _verify(lib, good, scale=float("inf")) == 1
-    assert lib.canopy_commit(None, good[1], good[2], good[3], good[5], 1, 64, 1, 1, 1, 128, 128, good[4], 0,
+    assert _verify(lib, good, lengths=ctypes.c_void_p(0x10004)) == 1   # misaligned lengths
+    for solve in (1, 2, 3):                                         # the variants take no lengths
+        assert _verify(lib, good, solve=solve, lengths=good[0]) == 3
+    assert lib.canopy_commit(None, good[1], good[2], good[3], good[5], None, 1, 64, 1, 1, 1, 128, 128, good[4], 0,
                              None) == 1
-    assert lib.canopy_commit(good[0], good[1], good[2], good[3], None, 1, 64, 1, 1, 1, 128, 128, good[4], 0,
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], None, None, 1, 64, 1, 1, 1, 128, 128, good[4], 0,
                              None) == 1
-    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], 1, 300, 1, 1, 1, 128, 128, good[4], 0,
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], None, 1, 300, 1, 1, 1, 128, 128, good[4], 0,
                              None) == 3
-    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], 1, 64, 1, 1, 1, 128, 128, good[4], 4,
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], None, 1, 64, 1, 1, 1, 128, 128, good[4], 4,
                              None) == 1
-    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], 1, 64, 1, 4, 6, 128, 128, good[4], 0,
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], None, 1, 64, 1, 4, 6, 128, 128, good[4], 0,
                              None) == 1
+    assert lib.canopy_commit(good[0], good[1], good[2], good[3], good[5], ctypes.c_void_p(0x10004), 1, 64, 1, 1, 1,
+                             128, 128, good[4], 0, None) == 1                 # misaligned lengths
     assert lib.canopy_tree_prep(good[0], good[1], 0, 1, 1, good[2], None) == 3
     # tree convolution (x, dtype, state, weight, bias, parent, T, B, C, K, act, y, err): every case is
     # refused on the host before a launch
