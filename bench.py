@@ -430,6 +430,108 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------------------
+# tables (crossover map, dispatch table, solve strategies, layer shape): each
+# output file opens with a record of the machine and closes with the clocks
+
+def _smi(query):
+    import subprocess
+    try:
+        r = subprocess.run(["nvidia-smi", f"--query-gpu={query}", "--format=csv,noheader"], capture_output=True,
+                           text=True, timeout=20)
+        return r.stdout.strip()
+    except (OSError, subprocess.SubprocessError):
+        return ""
+
+
+def env_record(kind):
+    import torch
+    return {"env": {"table": kind, "gpu": torch.cuda.get_device_name(0), "torch": torch.__version__,
+                    "cuda": torch.version.cuda, "driver": _smi("driver_version"),
+                    "clocks_before": _smi("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"),
+                    "date_utc": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime())}}
+
+
+class TableOut:
+    """JSON lines to stdout and to --sweep-out (if given), between an
+    environment record and a closing clocks record."""
+
+    def __init__(self, args, kind):
+        self.f = open(args.sweep_out, "w") if args.sweep_out else None
+        self.write(env_record(kind))
+
+    def write(self, rec):
+        line = json.dumps(rec)
+        print(line, flush=True)
+        if self.f:
+            self.f.write(line + "\n")
+
+    def close(self):
+        self.write({"env_end": {"clocks_after": _smi("clocks.sm,clocks.max.sm,power.draw,"
+                                                     "clocks_event_reasons.active")}})
+        if self.f:
+            self.f.close()
+
+
+def time_calls(calls, flush, warmup, reps):
+    """Each call timed alone after an L2 flush (a 1 GiB fill, which also keeps
+    the host ahead of the GPU), the calls interleaved; p10/p50/p90 in us."""
+    import torch
+    times = {k: [] for k in calls}
+    for it in range(warmup + reps):
+        for name, fn in calls.items():
+            flush.fill_(float(it))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            if it >= warmup:
+                times[name].append((a, b))
+    torch.cuda.synchronize()
+    out = {}
+    for name, evs in times.items():
+        us = [1e3 * a.elapsed_time(b) for a, b in evs]
+        out[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
+                     "p90": float(np.percentile(us, 90))}
+    return out
+
+
+def run_dispatch_table(args):
+    """Below the crossover: the closed form against the path replay (both
+    forced), random trees of 1..8 nodes, B in {1, 2, 4, 8, 16}, 16 key and
+    value heads, d = 128, bf16; the library's dispatch rule is checked
+    against this table (tests/test_dispatch_table.py)."""
+    import torch
+
+    import synth
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    from synth import configs, trees
+    bld.build()
+    canopy.load()
+    H, d = 16, 128
+    flush = torch.empty(1024 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    Bs = [int(x) for x in args.sweep_b.split(",")] if args.sweep_b else configs.SWEEP_B
+    Ts = [int(x) for x in args.sweep_t.split(",")] if args.sweep_t else list(range(1, 9))
+    out = TableOut(args, "dispatch: closed form vs path replay, H = HV = 16, d = 128, bf16, random trees")
+    for B in Bs:
+        for T in Ts:
+            rng = np.random.default_rng(100 * B + T)
+            inp = synth.make_inputs([trees.family("random", T, rng) for _ in range(B)], H, d, d, True, case=3, rnd=T)
+            dev = {n: torch.from_numpy(inp[n]).to("cuda", torch.bfloat16) for n in ("q", "k", "v")}
+            for n in ("g", "beta", "S0", "parent"):
+                dev[n] = torch.from_numpy(inp[n]).cuda()
+            ws = canopy.workspace(B, T, H, d)
+            o = torch.empty((B, T, H, d), dtype=torch.float32, device="cuda")
+            calls = {f: (lambda f=f: canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"],
+                                                   dev["parent"], ws, out=o, force=f))
+                     for f in ("closed_form", "path_replay")}
+            rec = {"B": B, "T": T, "H": H, "HV": H, **time_calls(calls, flush, args.sweep_warmup, args.sweep_reps)}
+            assert canopy.read_device_error(ws) == 0
+            out.write(rec)
+    out.close()
+
+
+# ---------------------------------------------------------------------------
 # crossover sweep: closed-form verify vs the serial replay kernel
 
 def run_sweep(args):
@@ -452,7 +554,7 @@ def run_sweep(args):
     Bs = [int(x) for x in args.sweep_b.split(",")] if args.sweep_b else configs.SWEEP_B
     Ts = [int(x) for x in args.sweep_t.split(",")] if args.sweep_t else configs.SWEEP_T
     fams = args.sweep_fam.split(",") if args.sweep_fam else configs.SWEEP_FAMILIES
-    out = open(args.sweep_out, "w") if args.sweep_out else None
+    out = TableOut(args, "crossover: closed-form verify vs serial replay, H = 16, d = 128, bf16")
     solves = ["fwdsub", "neumann"]
     for B in Bs:
         for T in Ts:
@@ -474,32 +576,14 @@ def run_sweep(args):
                         continue
                     calls[sv] = (lambda sv=sv: canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
                                                              dev["S0"], dev["parent"], ws, solve=sv, out=o))
-                times = {k: [] for k in calls}
-                for it in range(args.sweep_warmup + args.sweep_reps):
-                    for name, fn in calls.items():
-                        flush.fill_(float(it))
-                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        a.record()
-                        fn()
-                        b.record()
-                        if it >= args.sweep_warmup:
-                            times[name].append((a, b))
-                torch.cuda.synchronize()
+                rec = {"B": B, "T": T, "family": fam, "depth": int(max(trees.tree_depth(p) for p in parents)),
+                       **time_calls(calls, flush, args.sweep_warmup, args.sweep_reps)}
                 assert canopy.read_device_error(ws) == 0
-                rec = {"B": B, "T": T, "family": fam, "depth": int(max(trees.tree_depth(p) for p in parents))}
-                for name, evs in times.items():
-                    us = [1e3 * a.elapsed_time(b) for a, b in evs]
-                    rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
-                                 "p90": float(np.percentile(us, 90))}
                 rec["speedup_fwdsub"] = rec["serial"]["p50"] / rec["fwdsub"]["p50"]
                 if "neumann" in rec:
                     rec["speedup_neumann"] = rec["serial"]["p50"] / rec["neumann"]["p50"]
-                line = json.dumps(rec)
-                print(line, flush=True)
-                if out:
-                    out.write(line + "\n")
-    if out:
-        out.close()
+                out.write(rec)
+    out.close()
 
 
 def run_solve_table(args):
@@ -523,7 +607,7 @@ def run_solve_table(args):
     Bs = [int(x) for x in args.sweep_b.split(",")] if args.sweep_b else [1, 16]
     Ts = [int(x) for x in args.sweep_t.split(",")] if args.sweep_t else [256]
     fams = args.sweep_fam.split(",") if args.sweep_fam else ["top8", "top4", "top2", "random", "skewed", "chain"]
-    out = open(args.sweep_out, "w") if args.sweep_out else None
+    out = TableOut(args, "solve strategies and DFS vs level order, H = 16, d = 128, bf16")
     for B in Bs:
         for T in Ts:
             for fam in fams:
@@ -546,31 +630,13 @@ def run_solve_table(args):
                         calls[sv] = (lambda sv=sv: canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"],
                                                                  dev["beta"], dev["S0"], dev["parent"], ws,
                                                                  solve=sv, out=o))
-                    times = {k: [] for k in calls}
-                    for it in range(args.sweep_warmup + args.sweep_reps):
-                        for name, fn in calls.items():
-                            flush.fill_(float(it))
-                            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                            a.record()
-                            fn()
-                            b.record()
-                            if it >= args.sweep_warmup:
-                                times[name].append((a, b))
-                    torch.cuda.synchronize()
-                    assert canopy.read_device_error(ws) == 0
                     rec = {"B": B, "T": T, "family": fam, "order": order_name,
-                           "depth": int(max(trees.tree_depth(p) for p in parents))}
-                    for name, evs in times.items():
-                        us = [1e3 * a.elapsed_time(b) for a, b in evs]
-                        rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
-                                     "p90": float(np.percentile(us, 90))}
-                    line = json.dumps(rec)
-                    print(line, flush=True)
-                    if out:
-                        out.write(line + "\n")
+                           "depth": int(max(trees.tree_depth(p) for p in parents)),
+                           **time_calls(calls, flush, args.sweep_warmup, args.sweep_reps)}
+                    assert canopy.read_device_error(ws) == 0
+                    out.write(rec)
                     del ws, snap, o, dev
-    if out:
-        out.close()
+    out.close()
 
 
 def run_layer_shape(args):
@@ -592,7 +658,7 @@ def run_layer_shape(args):
     # 1 GiB: larger than L2, and long enough (about 0.15 ms) that the host has
     # queued the timed call before the GPU reaches it
     flush = torch.empty(1024 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
-    out = open(args.sweep_out, "w") if args.sweep_out else None
+    out = TableOut(args, "one GDN layer at 16 key / 32 value heads, d = 128, scale 1/sqrt(128)")
     for B, T, fam in ((1, 16, "schedule421"), (1, 64, "random"), (16, 64, "random")):
         rng = np.random.default_rng(7000 + 100 * B + T)
         parents = [configs.make_tree(fam, T, rng) for _ in range(B)]
@@ -635,34 +701,16 @@ def run_layer_shape(args):
             canopy.tree_conv(xc, cst, cw, dev["parent"], act="silu", out=yc)
 
         calls = {"verify": ver, "verify_commit": step, "serial": ser, "tree_conv": conv}
-        times = {k: [] for k in calls}
-        for it in range(args.sweep_warmup + args.sweep_reps):
-            for name, fn in calls.items():
-                flush.fill_(float(it))
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                if it >= args.sweep_warmup:
-                    times[name].append((a, b))
-        torch.cuda.synchronize()
-        assert canopy.read_device_error(ws) == 0
         rec = {"layer": "H=16 key heads, HV=32 value heads, dk=dv=128, scale 1/sqrt(128)", "B": B, "T": T,
-               "tree": fam, "depth": int(max(trees.tree_depth(p) for p in parents))}
-        for name, evs in times.items():
-            us = [1e3 * a.elapsed_time(b) for a, b in evs]
-            rec[name] = {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
-                         "p90": float(np.percentile(us, 90))}
+               "tree": fam, "depth": int(max(trees.tree_depth(p) for p in parents)),
+               **time_calls(calls, flush, args.sweep_warmup, args.sweep_reps)}
+        assert canopy.read_device_error(ws) == 0
         rec["speedup_verify"] = rec["serial"]["p50"] / rec["verify"]["p50"]
         conv_bytes = 2 * B * T * C * 2 + B * C * 3 * 4 + C * 4 * 4
         rec["tree_conv_channels"] = C
         rec["tree_conv_GBps"] = conv_bytes / (rec["tree_conv"]["p50"] * 1e3)
-        line = json.dumps(rec)
-        print(line, flush=True)
-        if out:
-            out.write(line + "\n")
-    if out:
-        out.close()
+        out.write(rec)
+    out.close()
 
 
 def run_memory(args):
@@ -709,6 +757,8 @@ def main():
                     help="one GDN layer at 16 key / 32 value heads with the 1/sqrt(dk) q scale")
     ap.add_argument("--solve-table", action="store_true",
                     help="solve strategies and DFS vs level order side by side (T = 256 by default)")
+    ap.add_argument("--dispatch-table", action="store_true",
+                    help="closed form vs path replay below the crossover (the dispatch rule's data)")
     ap.add_argument("--sweep-b", default="")
     ap.add_argument("--sweep-t", default="")
     ap.add_argument("--sweep-fam", default="")
@@ -727,6 +777,9 @@ def main():
         return
     if args.solve_table:
         run_solve_table(args)
+        return
+    if args.dispatch_table:
+        run_dispatch_table(args)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -23,6 +23,10 @@ SOLVE = {"fwdsub": 0, "neumann": 1, "squaring": 2, "split": 3}
 DEVERR_TREE, DEVERR_GATE, DEVERR_ACCEPTED, DEVERR_TIMEOUT, DEVERR_LENGTH = 0x1, 0x2, 0x4, 0x8, 0x10
 VERIFY_INPUTS_READY = 0x1
 VERIFY_STATE_READY = 0x2
+VERIFY_CLOSED_FORM = 0x4
+VERIFY_PATH_REPLAY = 0x8
+PLAN = {"none": -1, "path_replay": 0, "tc_block": 1, "tc_neumann": 2, "tc_blocked": 3, "fp32": 4, "variant": 5}
+FORCE = {None: 0, "closed_form": VERIFY_CLOSED_FORM, "path_replay": VERIFY_PATH_REPLAY}
 COMMIT_STATE_READY = 0x1
 ACT = {"none": 0, "silu": 1}
 WS_REGION = {"err": 0, "l": 1, "depth": 2, "mask": 3, "order": 4, "u": 5}
@@ -36,6 +40,7 @@ SIGNATURES = {
     "canopy_tree_prep": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "canopy_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I,
                                 _P, ctypes.c_uint, _P]),
+    "canopy_verify_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_uint, _I]),
     "canopy_commit": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint, _P]),
     "canopy_snapshot_bytes": (_S, [_I, _I, _I, _I, _I]),
     "canopy_serial_replay": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P,
@@ -174,7 +179,7 @@ def _lengths(lengths, B):
 
 
 def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torch.float32, out=None,
-           inputs_ready: bool = False, state_ready: bool = False, scale: float = 1.0, lengths=None):
+           inputs_ready: bool = False, state_ready: bool = False, scale: float = 1.0, lengths=None, force=None):
     """o [B, T, HV, dv] for every node of every stream's tree; q and k carry
     H key heads, v, g, beta and S0 HV value heads (a multiple of H), and
     scale multiplies q.  solve: "fwdsub" (every size and dtype), or
@@ -183,7 +188,9 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
     stream (CANOPY_VERIFY_INPUTS_READY); state_ready (with inputs_ready): nor
     is S0 (CANOPY_VERIFY_STATE_READY).  lengths: int32 [B] CUDA tensor of
     per-stream tree sizes (ragged batches), or None for T everywhere; rows of
-    o past a stream's length are left as they were."""
+    o past a stream's length are left as they were.  force: None (the
+    library's dispatch), "closed_form" or "path_replay" (forward substitution
+    only; the path replay takes trees of up to 8 nodes)."""
     B, T, H, HV, dk, dv = _heads(q, k, v, g, beta, S0, parent)
     _need(ws, "workspace", torch.uint8)
     if out is None:
@@ -193,9 +200,17 @@ def verify(q, k, v, g, beta, S0, parent, ws, solve: str = "fwdsub", o_dtype=torc
                                    _ptr(parent), _lengths(lengths, B), T, B, H, HV, dk, dv, float(scale),
                                    SOLVE[solve], _ptr(out), _dt(out),
                                    _ptr(ws), (VERIFY_INPUTS_READY if inputs_ready else 0)
-                                   | (VERIFY_STATE_READY if state_ready else 0), _stream())
+                                   | (VERIFY_STATE_READY if state_ready else 0) | FORCE[force], _stream())
     _check(st, "canopy_tree_verify")
     return out
+
+
+def verify_plan(T: int, B: int, H: int, HV: int, bf16: bool, d: int, solve: str = "fwdsub", force=None,
+                lengths: bool = False) -> str:
+    """Which path canopy_tree_verify takes for these sizes (a PLAN name)."""
+    code = load().canopy_verify_plan(T, B, H, HV, BF16 if bf16 else F32, d, d, SOLVE[solve], FORCE[force],
+                                     int(bool(lengths)))
+    return {v: k for k, v in PLAN.items()}[code]
 
 
 def commit(accepted, S0, k, parent, ws, out=None, state_ready: bool = False, lengths=None):

@@ -5,6 +5,7 @@
 #include "common.cuh"
 
 namespace canopy {
+int path_replay_max_t();
 // Launchers take H = value heads (the units: v, g, beta, S0, o, workspace)
 // and HK = key heads (q, k); value head h reads key head h / (H / HK).
 cudaError_t launch_tree_prep(const int32_t* parent, const int32_t* lengths, const float* g, int T, int B, int H,
@@ -54,21 +55,59 @@ bool sizes_ok(int B, int T, int H) { return B >= 1 && H >= 1 && T >= 1 && T <= k
 
 // Dispatch below the crossover (canopy page, "Design decisions": the serial
 // path below it, the closed form above): replaying each node's root path
-// from S0 beats the closed form's fixed chain of stages for single-node
-// trees, and for two- and three-node trees while there are few (stream,
-// value head) pairs to spread over the GPU.  Measured on GB300 at 16 value
-// heads (us, replay vs closed form): T = 2: 8.2 vs 12.5 at one stream, 16.2
-// vs 16.4 at sixteen; T = 3: 10.2 vs 12.3 at one stream, about 19 vs 16.4 at
-// sixteen; the cut-offs interpolate between the two.
+// from S0 beats the closed form's fixed chain of dependent stages for trees
+// of one or two nodes, and for three-node trees while there are few (stream,
+// value head) pairs to spread over the GPU.  From the GB300 dispatch table
+// (profiles/dispatch_H16_d128.jsonl: random trees, 16 value heads, replay /
+// closed form time): T = 1: 0.57-0.73; T = 2: 0.64-0.90; T = 3: 0.79-0.95
+// up to B = 8, 1.03 at B = 16; T = 4: 0.96-1.03 up to B = 4, 1.10 and more
+// beyond; T >= 5: above 1.09.  tests/test_dispatch_table.py checks the rule
+// against that table.
 bool path_replay_wins(int T, int B, int HV) {
     const size_t units = size_t(B) * HV;
-    return T == 1 || (T == 2 && units <= 128) || (T == 3 && units <= 64);
+    return T <= 2 || (T == 3 && units <= 128);
 }
 
 // key heads H, value heads HV: HV a positive multiple of H
 bool heads_ok(int H, int HV) { return H >= 1 && HV >= H && HV % H == 0; }
 
 canopy_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CANOPY_OK : CANOPY_ERR_CUDA; }
+
+constexpr unsigned kVerifyFlags =
+    CANOPY_VERIFY_INPUTS_READY | CANOPY_VERIFY_STATE_READY | CANOPY_VERIFY_CLOSED_FORM | CANOPY_VERIFY_PATH_REPLAY;
+
+// The checks of a verify call that do not look at pointers.
+canopy_status verify_args(int T, int B, int H, int HV, canopy_dtype in_dtype, canopy_dtype o_dtype, int dk, int dv,
+                          canopy_solve solve, unsigned flags, int has_lengths, float scale) {
+    if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
+        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN && solve != CANOPY_SOLVE_SQUARING &&
+         solve != CANOPY_SOLVE_SPLIT) ||
+        (flags & ~kVerifyFlags) || !std::isfinite(scale))
+        return CANOPY_ERR_ARG;
+    const unsigned force = flags & (CANOPY_VERIFY_CLOSED_FORM | CANOPY_VERIFY_PATH_REPLAY);
+    if (force == (CANOPY_VERIFY_CLOSED_FORM | CANOPY_VERIFY_PATH_REPLAY) || (force && solve != CANOPY_SOLVE_FWDSUB))
+        return CANOPY_ERR_ARG;
+    if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
+    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    const bool bf16_128 = in_dtype == CANOPY_BF16 && dk == 128;
+    // the solve variants run on the tensor-core Gram's tiles (bf16, d = 128), uniform T
+    if (solve != CANOPY_SOLVE_FWDSUB && (!bf16_128 || has_lengths)) return CANOPY_ERR_UNSUPPORTED;
+    if ((flags & CANOPY_VERIFY_PATH_REPLAY) && T > path_replay_max_t()) return CANOPY_ERR_UNSUPPORTED;
+    return CANOPY_OK;
+}
+
+// The plan of a verify call whose arguments passed verify_args.
+canopy_plan verify_plan(int T, int B, int HV, canopy_dtype in_dtype, int dk, canopy_solve solve, unsigned flags) {
+    const bool bf16_128 = in_dtype == CANOPY_BF16 && dk == 128;
+    if (solve == CANOPY_SOLVE_FWDSUB) {
+        if (flags & CANOPY_VERIFY_PATH_REPLAY) return CANOPY_PLAN_PATH_REPLAY;
+        if (!(flags & CANOPY_VERIFY_CLOSED_FORM) && path_replay_wins(T, B, HV)) return CANOPY_PLAN_PATH_REPLAY;
+        if (bf16_128) return T <= 64 ? CANOPY_PLAN_TC_BLOCK : CANOPY_PLAN_TC_BLOCKED;
+        return CANOPY_PLAN_FP32;
+    }
+    if (solve == CANOPY_SOLVE_NEUMANN && T <= 64) return CANOPY_PLAN_TC_NEUMANN;
+    return CANOPY_PLAN_VARIANT;
+}
 
 }  // namespace
 
@@ -119,46 +158,50 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(S0) ||
         !aligned16(parent) || !aligned16(o) || !aligned16(workspace) || (lengths && !aligned16(lengths)))
         return CANOPY_ERR_ARG;
-    if ((in_dtype != CANOPY_F32 && in_dtype != CANOPY_BF16) || (o_dtype != CANOPY_F32 && o_dtype != CANOPY_BF16) ||
-        (solve != CANOPY_SOLVE_FWDSUB && solve != CANOPY_SOLVE_NEUMANN && solve != CANOPY_SOLVE_SQUARING &&
-         solve != CANOPY_SOLVE_SPLIT) ||
-        (flags & ~(CANOPY_VERIFY_INPUTS_READY | CANOPY_VERIFY_STATE_READY)) || !std::isfinite(scale))
-        return CANOPY_ERR_ARG;
-    if (B <= 0 || H <= 0 || T <= 0 || !heads_ok(H, HV)) return CANOPY_ERR_ARG;
-    if (!sizes_ok(B, T, HV) || dk != dv || (dk != 128 && dk != 32)) return CANOPY_ERR_UNSUPPORTED;
+    const canopy_status as = verify_args(T, B, H, HV, in_dtype, o_dtype, dk, dv, solve, flags, lengths != nullptr,
+                                         scale);
+    if (as != CANOPY_OK) return as;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Ws ws = ws_bind(workspace, B, T, HV, dv);
     const int in_bf16 = in_dtype == CANOPY_BF16, o_bf16 = o_dtype == CANOPY_BF16;
-    const bool tc = in_bf16 && dk == 128 && T <= 64;
-    // the solve variants run on the tensor-core Gram's tiles (bf16, d = 128)
-    if (solve != CANOPY_SOLVE_FWDSUB && !(in_bf16 && dk == 128)) return CANOPY_ERR_UNSUPPORTED;
-    if (solve != CANOPY_SOLVE_FWDSUB && lengths) return CANOPY_ERR_UNSUPPORTED;  // uniform T only
-    if (solve == CANOPY_SOLVE_FWDSUB && path_replay_wins(T, B, HV))
-        return cuda_status(launch_path_replay(q, k, v, in_bf16, g, beta, S0, parent, lengths, T, B, HV, H, dk, o,
-                                              o_bf16, scale, ws, st));
-    if (tc && solve == CANOPY_SOLVE_NEUMANN)
-        return cuda_status(
-            launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
-    if (tc && solve == CANOPY_SOLVE_FWDSUB)
-        return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, lengths, T, B, HV, H, o, o_bf16, scale,
-                                                ws,
-                                                (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
-                                                (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
-    // bf16 inputs beyond one 64-node block: one tensor-core launch, blocks in order
-    if (in_bf16 && dk == 128 && solve == CANOPY_SOLVE_FWDSUB)
-        return cuda_status(
-            launch_verify_tc_big(q, k, v, g, beta, S0, parent, lengths, T, B, HV, H, o, o_bf16, scale, ws, st));
-    cudaError_t e = launch_tree_prep(parent, lengths, g, T, B, HV, ws, 0, st);
-    if (e != cudaSuccess) return CANOPY_ERR_CUDA;
-    if (solve != CANOPY_SOLVE_FWDSUB) {
-        // Neumann beyond 64 nodes, squaring and split: Gram tiles, then the solve
-        e = launch_gram_tc(q, k, v, beta, S0, T, B, HV, H, ws, st);
-        if (e != cudaSuccess) return cuda_status(e);
-        return cuda_status(launch_solve_variant(int(solve), T, B, HV, o, o_bf16, scale, ws, st));
+    switch (verify_plan(T, B, HV, in_dtype, dk, solve, flags)) {
+        case CANOPY_PLAN_PATH_REPLAY:
+            return cuda_status(launch_path_replay(q, k, v, in_bf16, g, beta, S0, parent, lengths, T, B, HV, H, dk, o,
+                                                  o_bf16, scale, ws, st));
+        case CANOPY_PLAN_TC_BLOCK:
+            return cuda_status(launch_verify_tc_fwd(q, k, v, g, beta, S0, parent, lengths, T, B, HV, H, o, o_bf16,
+                                                    scale, ws, (flags & CANOPY_VERIFY_INPUTS_READY) != 0,
+                                                    (flags & CANOPY_VERIFY_STATE_READY) != 0, st));
+        case CANOPY_PLAN_TC_NEUMANN:
+            return cuda_status(
+                launch_verify_neumann(q, k, v, g, beta, S0, parent, T, B, HV, H, o, o_bf16, scale, ws, st));
+        case CANOPY_PLAN_TC_BLOCKED:
+            return cuda_status(
+                launch_verify_tc_big(q, k, v, g, beta, S0, parent, lengths, T, B, HV, H, o, o_bf16, scale, ws, st));
+        case CANOPY_PLAN_FP32: {
+            const cudaError_t e = launch_tree_prep(parent, lengths, g, T, B, HV, ws, 0, st);
+            if (e != cudaSuccess) return CANOPY_ERR_CUDA;
+            return cuda_status(
+                launch_verify_simt(q, k, v, in_bf16, beta, S0, lengths, T, B, HV, H, dk, o, o_bf16, scale, ws, st));
+        }
+        case CANOPY_PLAN_VARIANT: {
+            // Neumann beyond 64 nodes, squaring and split: tree prep, Gram tiles, then the solve
+            cudaError_t e = launch_tree_prep(parent, nullptr, g, T, B, HV, ws, 0, st);
+            if (e != cudaSuccess) return CANOPY_ERR_CUDA;
+            e = launch_gram_tc(q, k, v, beta, S0, T, B, HV, H, ws, st);
+            if (e != cudaSuccess) return cuda_status(e);
+            return cuda_status(launch_solve_variant(int(solve), T, B, HV, o, o_bf16, scale, ws, st));
+        }
+        default:
+            return CANOPY_ERR_ARG;
     }
-    // fp32 inputs, or dk = dv = 32: CUDA cores
-    return cuda_status(
-        launch_verify_simt(q, k, v, in_bf16, beta, S0, lengths, T, B, HV, H, dk, o, o_bf16, scale, ws, st));
+}
+
+canopy_plan canopy_verify_plan(int T, int B, int H, int HV, canopy_dtype in_dtype, int dk, int dv,
+                               canopy_solve solve, unsigned flags, int has_lengths) {
+    if (verify_args(T, B, H, HV, in_dtype, CANOPY_F32, dk, dv, solve, flags, has_lengths, 1.f) != CANOPY_OK)
+        return CANOPY_PLAN_NONE;
+    return verify_plan(T, B, HV, in_dtype, dk, solve, flags);
 }
 
 canopy_status canopy_commit(const int32_t* accepted, const float* S0, float* S_new, const void* k,

@@ -86,6 +86,20 @@ typedef enum {
                                             kernel launched just before this call */
 #define CANOPY_VERIFY_STATE_READY 0x2u   /* S0 is not written by the kernel launched just
                                             before this call */
+#define CANOPY_VERIFY_CLOSED_FORM 0x4u   /* FWDSUB: never the path replay below the crossover */
+#define CANOPY_VERIFY_PATH_REPLAY 0x8u   /* FWDSUB: always the path replay (T <= 8; larger T
+                                            returns CANOPY_ERR_UNSUPPORTED) */
+
+/* How a verify call is carried out (canopy_verify_plan). */
+typedef enum {
+    CANOPY_PLAN_NONE = -1,        /* the call would be refused (an argument error)           */
+    CANOPY_PLAN_PATH_REPLAY = 0,  /* each node's root path replayed from S0 (tiny trees)     */
+    CANOPY_PLAN_TC_BLOCK = 1,     /* one tensor-core launch, one 64-node block (T <= 64)     */
+    CANOPY_PLAN_TC_NEUMANN = 2,   /* the same with the Neumann series                         */
+    CANOPY_PLAN_TC_BLOCKED = 3,   /* one tensor-core launch, 64-node blocks in order (T > 64) */
+    CANOPY_PLAN_FP32 = 4,         /* tree prep, Gram and level solve in fp32 on CUDA cores   */
+    CANOPY_PLAN_VARIANT = 5       /* tree prep, tensor-core Gram, then the solve variant     */
+} canopy_plan;
 
 /* Flags of canopy_commit. */
 #define CANOPY_COMMIT_STATE_READY 0x1u   /* S0, accepted, k and parent are not written by
@@ -149,7 +163,7 @@ canopy_status canopy_tree_prep(const int32_t* parent, const float* g,
  * in_dtype CANOPY_BF16 selects the tensor-core path (tcgen05, bf16 operands,
  * fp32 accumulation); CANOPY_F32 selects the fp32 path.  S0 is read only.
  * With solve = CANOPY_SOLVE_FWDSUB, trees below the measured crossover (one
- * node; two nodes with B * HV <= 128; three with B * HV <= 64) are verified by replaying
+ * or two nodes; three with B * HV <= 128) are verified by replaying
  * each node's root path from S0 in fp32 instead (same outputs and workspace
  * contents; canopy page, "Design decisions": serial below the crossover).
  * flags: 0, or CANOPY_VERIFY_INPUTS_READY, optionally with
@@ -181,6 +195,16 @@ canopy_status canopy_tree_verify(const void* q, const void* k, const void* v, ca
                                  const int32_t* parent, const int32_t* lengths, int T, int B, int H, int HV,
                                  int dk, int dv, float scale, canopy_solve solve, void* o,
                                  canopy_dtype o_dtype, void* workspace, unsigned flags, void* stream);
+
+/* The plan canopy_tree_verify follows for these sizes, dtype, solve and
+ * flags, with lengths given (has_lengths != 0) or not; CANOPY_PLAN_NONE where
+ * the call would return an error for them.  The dispatch below the crossover
+ * (canopy page, "Design decisions": the serial path below the crossover, the
+ * closed form above it) sends trees of one or two nodes, and three-node trees
+ * over at most 128 (stream, value head) pairs, to the path replay.
+ * Host-only, no CUDA call. */
+canopy_plan canopy_verify_plan(int T, int B, int H, int HV, canopy_dtype in_dtype, int dk, int dv,
+                               canopy_solve solve, unsigned flags, int has_lengths);
 
 /* Commit (canopy page, "The tree closed form", last line, and "What the
  * commit kernel stores"): for every stream b with accepted node a = accepted[b],

@@ -40,7 +40,7 @@ def header_enum(prefix):
     """name -> value of every `CANOPY_<prefix>_<NAME> = <int>` enumerator."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     return {m.group(1).lower(): int(m.group(2))
-            for m in re.finditer(r"\bCANOPY_%s_([A-Z0-9]+)\s*=\s*(\d+)" % prefix, text)}
+            for m in re.finditer(r"\bCANOPY_%s_([A-Z0-9_]+)\s*=\s*(-?\d+)" % prefix, text)}
 
 
 def test_binding_enums_match_the_header():
@@ -49,6 +49,33 @@ def test_binding_enums_match_the_header():
     assert canopy.SOLVE == header_enum("SOLVE")
     assert canopy.ACT == header_enum("ACT")
     assert canopy.WS_REGION == header_enum("WS")
+    assert canopy.PLAN == header_enum("PLAN")
+
+
+def test_verify_plan(lib):
+    """The dispatch the verify call follows, queried on the host: tiny trees
+    over few (stream, value head) pairs take the path replay, bf16 at d = 128
+    the tensor cores (one block up to 64 nodes, blocks in order beyond), fp32
+    or d = 32 the CUDA cores; the forcing flags and refused combinations."""
+    from gated_deltanet_linear_tree_gb300 import canopy
+    vp = canopy.verify_plan
+    assert vp(1, 16, 16, 16, True, 128) == "path_replay"
+    assert vp(1, 16, 16, 16, True, 128, force="closed_form") == "tc_block"
+    assert vp(8, 1, 16, 16, True, 128) == "tc_block"
+    assert vp(8, 1, 16, 16, True, 128, force="path_replay") == "path_replay"
+    assert vp(9, 1, 16, 16, True, 128, force="path_replay") == "none"     # the replay takes <= 8 nodes
+    assert vp(64, 16, 16, 16, True, 128) == "tc_block"
+    assert vp(65, 16, 16, 16, True, 128) == "tc_blocked"
+    assert vp(256, 16, 16, 16, True, 128, lengths=True) == "tc_blocked"
+    assert vp(64, 16, 16, 16, False, 128) == "fp32"
+    assert vp(8, 1, 2, 2, True, 32, force="closed_form") == "fp32"
+    assert vp(64, 2, 4, 4, True, 128, solve="neumann") == "tc_neumann"
+    assert vp(65, 2, 4, 4, True, 128, solve="neumann") == "variant"
+    assert vp(64, 2, 4, 4, True, 128, solve="split") == "variant"
+    assert vp(64, 2, 4, 4, True, 128, solve="split", lengths=True) == "none"
+    assert vp(64, 2, 4, 4, True, 128, solve="neumann", force="closed_form") == "none"
+    assert vp(257, 2, 4, 4, True, 128) == "none"
+    assert lib.canopy_verify_plan(8, 1, 4, 4, 1, 128, 128, 0, 0xC, 0) == -1     # both forcing flags
 
 
 def test_workspace_offsets(lib):
@@ -111,8 +138,11 @@ def test_host_argument_errors(lib):
     for solve in (1, 2, 3):                                         # variants: bf16 and d = 128 only
         assert _verify(lib, good, solve=solve, in_dt=0) == 3
         assert _verify(lib, good, solve=solve, d=32) == 3
-    assert _verify(lib, good, flags=4) == 1                         # unknown flag
-    assert _verify(lib, good, flags=8) == 1
+    assert _verify(lib, good, flags=0x10) == 1                      # unknown flag
+    assert _verify(lib, good, flags=0x20) == 1
+    assert _verify(lib, good, flags=0xC) == 1                       # closed form and path replay forced at once
+    assert _verify(lib, good, flags=0x8, solve=1) == 1              # forcing flags: forward substitution only
+    assert _verify(lib, good, flags=0x8, T=9) == 3                  # the path replay takes at most 8 nodes
     assert _verify(lib, good, H=2, HV=3) == 1                       # value heads not a multiple of key heads
     assert _verify(lib, good, H=2, HV=1) == 1
     assert _verify(lib, good, scale=float("nan")) == 1
