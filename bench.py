@@ -44,10 +44,13 @@ WORKLOAD = dict(name="batched verify B=16 T=64 H=16 dk=dv=128 random trees depth
                 case=2, B=16, T=64, H=16, d=128)
 METRIC = "µs per GDN layer tree-verify and verified nodes/s (B=16,T=64); % HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one verify
-# launch of the default workload, from an ncu capture of the current kernel;
-# set to None whenever the kernel changes, until it is captured again.
-VERIFY_DRAM_TRAFFIC = 29_560_320 + 105_728
+NOMINAL_HBM_GBS = 7900.0     # GB300 HBM3e, nominal (context beside the measured copy peak)
+# DRAM bytes of one verify launch of the default workload from an ncu capture
+# of the current kernel (dram__bytes_read.sum, dram__bytes_write.sum); set to
+# None whenever the kernel changes, until it is captured again.  The writes
+# (o and U, 16.8 MB) are still in L2 when the launch ends and reach DRAM
+# during later launches, so the capture's write figure is far below them.
+VERIFY_DRAM_TRAFFIC = {"read": 29_562_368, "write": 100_864}
 
 
 def verify_bytes(B, T, H, d, in_bytes=2, o_bytes=4):
@@ -217,7 +220,44 @@ def capture_graph(canopy, sets, T, solve, n, kind):
 
 
 def set_bytes(s):
-    return sum(t.numel() * t.element_size() for k, t in s.items() if k != "host")
+    return sum(t.numel() * t.element_size() for k, t in s.items() if k not in ("host", "src"))
+
+
+def verify_after_producer(canopy, sets, solve, n, reps):
+    """us per verify when the kernel before it is a plain HBM-bound kernel
+    that writes the verify's q, k and v (a stand-in for the projection that
+    produces them), with no overlap flags: graphs of n x (producer copies)
+    and of n x (producer copies, verify), the difference per verify.  The
+    verify can then start nothing before the copies complete."""
+    import torch
+    for s in sets:
+        if "src" not in s:
+            s["src"] = {c: s[c].clone() for c in ("q", "k", "v")}
+
+    def graph(with_verify):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                s = sets[i % len(sets)]
+                for c in ("q", "k", "v"):
+                    s[c].copy_(s["src"][c])
+                if with_verify:
+                    canopy.verify(s["q"], s["k"], s["v"], s["g"], s["beta"], s["S0"], s["parent"], s["ws"],
+                                  solve=solve, out=s["o"])
+        torch.cuda.synchronize()
+        return g
+
+    gp, gpv = graph(False), graph(True)
+    tp, tpv = [], []
+    for _ in range(reps):
+        for g, out in ((gp, tp), (gpv, tpv)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            out.append(a.elapsed_time(b))
+    return 1e3 * (statistics.median(tpv) - statistics.median(tp)) / n, 1e3 * statistics.median(tp) / n
 
 
 def run_canopy(args, world, rank, local):
@@ -274,6 +314,7 @@ def run_canopy(args, world, rank, local):
             out.append(a.elapsed_time(b) / G)
     clk = clocks.stop()
     total_ms = max_over_ranks(total_ms, world)
+    vp_us, prod_us = verify_after_producer(canopy, sets, args.solve, G, args.kernel_reps)
     errs = [canopy.read_device_error(s["ws"]) for s in sets]
     assert not any(errs), errs
 
@@ -286,10 +327,19 @@ def run_canopy(args, world, rank, local):
     vb = verify_bytes(B, T, H, d)
     cb = commit_bytes(B, T, H, d)
     achieved = vb / (v_us * 1e-6) / 1e9
-    # one fused launch for forward substitution or the Neumann series up to
-    # 64 nodes; otherwise tree prep, the Gram and the solve (two for split)
-    tc_path = T <= 64 and args.solve in ("fwdsub", "neumann")
-    launches_per_step = (1 if tc_path else (4 if args.solve == "split" else 3)) + 1
+    # forward substitution: one launch at every T (the fused kernel up to 64
+    # nodes, the blocked tensor-core kernel beyond); the Neumann series is
+    # one launch up to 64 nodes; otherwise tree prep, the Gram and the solve
+    # (two launches for split)
+    one_launch = args.solve == "fwdsub" or (T <= 64 and args.solve == "neumann")
+    launches_per_step = (1 if one_launch else (4 if args.solve == "split" else 3)) + 1
+    kernel = {("fwdsub", True): "tcf::verify_fwd_kernel (fused, tcgen05)",
+              ("fwdsub", False): "tcb::verify_big_kernel (blocked, tcgen05)",
+              ("neumann", True): "tc::verify_neumann_kernel (fused, tcgen05)"}.get(
+                  (args.solve, T <= 64), "tree prep + tensor-core Gram + CUDA-core solve variant")
+    traffic = None
+    if VERIFY_DRAM_TRAFFIC is not None and T == 64 and args.solve == "fwdsub":
+        traffic = VERIFY_DRAM_TRAFFIC["read"] + VERIFY_DRAM_TRAFFIC["write"]
 
     e2e = run_e2e(canopy, sets, T, args, world)
     line = {
@@ -307,12 +357,25 @@ def run_canopy(args, world, rank, local):
         "timing": f"one CUDA graph of {G} steps (verify + commit, sets rotating) replayed {reps} times "
                   f"(+ a graph of the {rem} remaining steps) between two events; per-kernel durations from graphs of {G} launches of one kernel, "
                   f"{args.kernel_reps} replays each (p10/p50/p90 over replays)",
-        "roofline": {"bound": "hbm", "kernel": "verify (tensor-core fused)" if tc_path else
-                     "verify (tensor-core Gram, CUDA-core solve)",
+        "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": VERIFY_DRAM_TRAFFIC if (tc_path and args.solve == "fwdsub") else None, "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs"},
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
+                     "traffic": traffic,
+                     "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch; o and U "
+                                     "are still in L2 when the launch ends, so its writes reach DRAM later"
+                                     if traffic is not None else "no capture of the current kernel",
+                     "algorithmic_bytes": vb, "peak_source": f"{peak_src} hbm_gbs",
+                     "setting": "back to back over rotating input sets, overlap flags set (the preceding "
+                                "kernel is a verify or commit of another set)"},
+        "roofline_verify_after_producer": {
+            "bound": "hbm", "us_per_launch": vp_us, "achieved": vb / (vp_us * 1e-6) / 1e9, "peak": peak,
+            "unit": "GB/s", "frac": vb / (vp_us * 1e-6) / 1e9 / peak,
+            "frac_nominal": vb / (vp_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
+            "setting": "each verify follows copy kernels that write its q, k and v (no overlap flags); "
+                       f"time of (copies + verify) minus copies alone ({prod_us:.2f} us) per launch"},
         "roofline_commit": {"bound": "hbm", "achieved": cb / (c_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
-                            "frac": cb / (c_us * 1e-6) / 1e9 / peak, "algorithmic_bytes": cb},
+                            "frac": cb / (c_us * 1e-6) / 1e9 / peak,
+                            "frac_nominal": cb / (c_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, "algorithmic_bytes": cb},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "e2e": e2e,
@@ -366,64 +429,94 @@ def run_e2e(canopy, sets, T, args, world):
             "ms_per_step": ms / K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
-def cpu_baseline(inp, seconds):
-    """The fp64 oracle as it stands, on a bounded sample of the workload:
-    whole streams of the first input set, until `seconds` have passed."""
+def _oracle_streams(args):
+    """Worker of the CPU baseline's process pool: the fp64 oracle replay of
+    whole streams (one stream per task, every head of it at once)."""
     import oracle
+    parent, q, k, v, g, beta, S0 = args
+    oracle.replay(parent, q, k, v, g, beta, S0, keep_states=False)
+    return parent.shape[0]
+
+
+def cpu_baseline(inp, seconds, repeats=3):
+    """The fp64 oracle as it stands, on a bounded sample of the workload: the
+    first input set's streams, each replayed whole (all heads at once, NumPy
+    einsum, no BLAS call), spread over a process pool of one worker per host
+    core (spawned: the workers start no CUDA context).  The sample is sized
+    so that one pass takes about seconds / repeats; the value is the median
+    of `repeats` passes."""
+    import multiprocessing as mp
     B = inp["parent"].shape[0]
     T = inp["parent"].shape[1]
-    t0 = time.perf_counter()
-    n = 0
-    b = 0
-    while True:
-        oracle.replay(inp["parent"][b % B], inp["q"][b % B], inp["k"][b % B], inp["v"][b % B], inp["g"][b % B],
-                      inp["beta"][b % B], inp["S0"][b % B], keep_states=False)
-        n += T
-        b += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "verified nodes/s", "cores": 1, "host_cores": os.cpu_count(),
-            "kind": "oracle", "sample": f"{b} whole streams (T={T}, H={inp['q'].shape[2]}, dk=dv=128) of the "
-            f"workload, fp64 NumPy replay, single-threaded"}
+    cores = os.cpu_count() or 1
+    tasks = [tuple(inp[n][b] for n in ("parent", "q", "k", "v", "g", "beta", "S0")) for b in range(B)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_streams, tasks[:cores])            # start-up and imports, untimed
+        t0 = time.perf_counter()
+        pool.map(_oracle_streams, tasks)
+        per_pass = time.perf_counter() - t0
+        mult = max(1, int(round(seconds / repeats / max(per_pass, 1e-3))))
+        rates = []
+        for _ in range(repeats):
+            t0 = time.perf_counter()
+            n = sum(pool.map(_oracle_streams, tasks * mult))
+            rates.append(n / (time.perf_counter() - t0))
+    return {"value": statistics.median(rates), "unit": "verified nodes/s", "cores": cores, "host_cores": cores,
+            "blas_threads": 0, "repeats": repeats, "kind": "oracle",
+            "sample": f"{B * mult} whole streams per pass (T={T}, H={inp['q'].shape[2]}, dk=dv={inp['q'].shape[3]}) of the "
+                      f"workload's first input set, fp64 NumPy replay, one stream per task over {cores} spawned "
+                      f"worker processes; median of {repeats} passes (einsum: no BLAS threads)"}
 
 
 # ---------------------------------------------------------------------------
 # reference arm: the fp64 oracle on the host cores
 
 def run_reference(args, world, rank):
+    """The oracle on the host cores: each step replays the first m nodes of
+    one stream per host core (a bounded sample of the workload, every head
+    at once), the streams spread over spawned worker processes; m is sized
+    so that the whole run takes about two minutes."""
     if rank != 0:
         return
-    import oracle
+    import multiprocessing as mp
+
     import synth
     wl = WORKLOAD
     inp = synth.config_inputs(wl["case"], rnd=0)
     B, T = inp["parent"].shape
-    t0 = time.perf_counter()
-    oracle.replay(inp["parent"][0][:8], inp["q"][0][:8], inp["k"][0][:8], inp["v"][0][:8], inp["g"][0][:8],
-                  inp["beta"][0][:8], inp["S0"][0], keep_states=False)
-    t_node = (time.perf_counter() - t0) / 8
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    m = int(max(1, min(T, budget / t_node)))
+    cores = os.cpu_count() or 1
+    names = ("parent", "q", "k", "v", "g", "beta", "S0")
 
-    def one(i):
-        b = i % B
-        oracle.replay(inp["parent"][b][:m], inp["q"][b][:m], inp["k"][b][:m], inp["v"][b][:m], inp["g"][b][:m],
-                      inp["beta"][b][:m], inp["S0"][b], keep_states=False)
+    def tasks(i, m):
+        out = []
+        for c in range(cores):
+            b = (i * cores + c) % B
+            out.append(tuple(inp[n][b] if n == "S0" else inp[n][b][:m] for n in names))
+        return out
 
-    for i in range(args.warmup):
-        one(i)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        one(i)
-    dt = time.perf_counter() - t0
-    value = m * args.steps / dt
-    sample = f"first {m} nodes of one stream's tree per step (H=16, dk=dv=128), fp64 NumPy replay"
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_streams, tasks(0, 8))               # start-up and imports, untimed
+        t0 = time.perf_counter()
+        pool.map(_oracle_streams, tasks(0, 8))
+        t_node = (time.perf_counter() - t0) / 8
+        budget = 120.0 / max(1, args.steps + args.warmup)
+        m = int(max(1, min(T, budget / max(t_node, 1e-6))))
+        for i in range(args.warmup):
+            pool.map(_oracle_streams, tasks(i, m))
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            pool.map(_oracle_streams, tasks(i, m))
+        dt = time.perf_counter() - t0
+    value = cores * m * args.steps / dt
+    sample = (f"first {m} nodes of {cores} streams' trees per step (one stream per spawned worker process; "
+              f"H=16, dk=dv=128), fp64 NumPy replay")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "verified nodes/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl["name"]},
-            "cpu_baseline": {"value": value, "unit": "verified nodes/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "verified nodes/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "verified nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -737,6 +830,102 @@ def run_memory(args):
         print(json.dumps(rec), flush=True)
 
 
+PROFILE_CASES = {
+    # name: (what runs, B, T, tree family)
+    "verify64": ("verify", 16, 64, "random_depth_4_20"),
+    "verify128": ("verify", 16, 128, "random"),
+    "verify256": ("verify", 16, 256, "random"),
+    "verify256_chain": ("verify", 16, 256, "chain"),
+    "neumann64": ("neumann", 16, 64, "random_depth_4_20"),
+    "commit64": ("commit", 16, 64, "random_depth_4_20"),
+    "serial64": ("serial", 4, 64, "random_depth_4_20"),
+    "path_replay3": ("path_replay", 16, 3, "random"),
+    "tree_conv64": ("tree_conv", 16, 64, "random_depth_4_20"),
+}
+
+
+def run_profile_case(args):
+    """A small, fixed case of one kernel for profilers: seeded inputs (16 key
+    and value heads, d = 128, bf16 q/k/v, fp32 S0 and o), one warm-up call,
+    then --profile-reps calls, each after a 256 MB fill that evicts L2.  The
+    tree convolution runs over the 8,192 channels of a 16-key / 32-value-head
+    layer's q, k and v (K = 4, SiLU).  Device memory stays under 1 GB."""
+    import torch
+
+    import synth
+    from gated_deltanet_linear_tree_gb300 import build as bld
+    from gated_deltanet_linear_tree_gb300 import canopy
+    from synth import configs, trees
+    bld.build()
+    canopy.load()
+    kind, B, T, fam = PROFILE_CASES[args.profile_case]
+    H, d = 16, 128
+    rng = np.random.default_rng(11)
+    parents = [configs.make_tree(fam, T, rng) for _ in range(B)]
+    inp = synth.make_inputs(parents, H, d, d, True, case=97, rnd=T)
+    dev = {n: torch.from_numpy(inp[n]).to("cuda", torch.bfloat16) for n in ("q", "k", "v")}
+    for n in ("g", "beta", "S0", "parent"):
+        dev[n] = torch.from_numpy(inp[n]).cuda()
+    dev["acc"] = torch.tensor([int(rng.choice(trees.leaves(p))) for p in parents], dtype=torch.int32,
+                              device="cuda")
+    ws = canopy.workspace(B, T, H, d)
+    o = torch.empty((B, T, H, d), dtype=torch.float32, device="cuda")
+    S_new = torch.empty_like(dev["S0"])
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+
+    def ver(solve="fwdsub", force=None):
+        canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
+                      solve=solve, out=o, force=force)
+
+    if kind == "verify":
+        fn = ver
+    elif kind == "neumann":
+        def fn():
+            ver("neumann")
+    elif kind == "path_replay":
+        def fn():
+            ver(force="path_replay")
+    elif kind == "commit":
+        ver()
+
+        def fn():
+            canopy.commit(dev["acc"], dev["S0"], dev["k"], dev["parent"], ws, out=S_new)
+    elif kind == "serial":
+        snap = torch.empty(canopy.snapshot_bytes(B, T, H, d), dtype=torch.uint8, device="cuda")
+
+        def fn():
+            canopy.serial_replay(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
+                                 snapshot=snap, out=o)
+    elif kind == "tree_conv":
+        C = 2 * 16 * d + 32 * d
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(5)
+        xc = torch.randn((B, T, C), device="cuda", generator=gen).to(torch.bfloat16)
+        cst = torch.randn((B, C, 3), device="cuda", generator=gen)
+        cw = 0.5 * torch.randn((C, 4), device="cuda", generator=gen)
+        yc = torch.empty_like(xc)
+
+        def fn():
+            canopy.tree_conv(xc, cst, cw, dev["parent"], act="silu", out=yc)
+    else:
+        raise ValueError(kind)
+    fn()
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.profile_reps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(1e3 * a.elapsed_time(b))
+    assert canopy.read_device_error(ws) == 0
+    print(json.dumps({"profile_case": args.profile_case, "kind": kind, "B": B, "T": T, "tree": fam,
+                      "depth": int(max(trees.tree_depth(p) for p in parents)),
+                      "us_per_call_after_l2_fill": times}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -765,7 +954,13 @@ def main():
     ap.add_argument("--sweep-reps", type=int, default=50)
     ap.add_argument("--sweep-warmup", type=int, default=10)
     ap.add_argument("--sweep-out", default="")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default="",
+                    help="a small fixed case of one kernel, for ncu")
+    ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.memory:
         run_memory(args)
         return

@@ -76,3 +76,15 @@ def test_algorithmic_bytes_match_the_stated_figures():
     assert bench.verify_bytes(B, T, H, d, o_bytes=2) == stated + 12_288
     assert bench.verify_bytes(B, T, H, d) == stated + 12_288 + B * T * H * d * 2 == 46_350_336
     assert bench.commit_bytes(B, T, H, d) == 33_554_432
+
+
+def test_cpu_baseline_process_pool():
+    """The CPU baseline's pool of spawned oracle workers runs, counts whole
+    streams and reports its core count and repeats."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    inp = synth.config_inputs(0)
+    r = bench.cpu_baseline(inp, seconds=0.3, repeats=2)
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["repeats"] == 2
+    assert r["cores"] == (os.cpu_count() or 1)
