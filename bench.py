@@ -850,7 +850,8 @@ PROFILE_CASES = {
 def run_profile_case(args):
     """A small, fixed case of one kernel for profilers: seeded inputs (16 key
     and value heads, d = 128, bf16 q/k/v, fp32 S0 and o), one warm-up call,
-    then --profile-reps calls, each after a 256 MB fill that evicts L2.  The
+    then --profile-reps calls, each after a 256 MB read that evicts L2 (a
+    read leaves clean lines, so the call pays no write-back of them).  The
     tree convolution runs over the 8,192 channels of a 16-key / 32-value-head
     layer's q, k and v (K = 4, SiLU).  Device memory stays under 1 GB."""
     import torch
@@ -907,16 +908,24 @@ def run_profile_case(args):
         cst = torch.randn((B, C, 3), device="cuda", generator=gen)
         cw = 0.5 * torch.randn((C, 4), device="cuda", generator=gen)
         yc = torch.empty_like(xc)
+        # eight input / output pairs (268 MB) for the back-to-back graph below
+        xs = [xc] + [torch.randn_like(xc, dtype=torch.float32).to(torch.bfloat16) for _ in range(7)]
+        ys = [torch.empty_like(xc) for _ in range(8)]
 
         def fn():
             canopy.tree_conv(xc, cst, cw, dev["parent"], act="silu", out=yc)
+
+        def rotating(i):
+            canopy.tree_conv(xs[i % 8], cst, cw, dev["parent"], act="silu", out=ys[i % 8])
     else:
         raise ValueError(kind)
     fn()
     torch.cuda.synchronize()
     times = []
+    flush.fill_(1.0)
+    torch.cuda.synchronize()
     for i in range(args.profile_reps):
-        flush.fill_(float(i))
+        flush.sum()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -924,9 +933,40 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         times.append(1e3 * a.elapsed_time(b))
     assert canopy.read_device_error(ws) == 0
-    print(json.dumps({"profile_case": args.profile_case, "kind": kind, "B": B, "T": T, "tree": fam,
-                      "depth": int(max(trees.tree_depth(p) for p in parents)),
-                      "us_per_call_after_l2_fill": times}), flush=True)
+    rec = {"profile_case": args.profile_case, "kind": kind, "B": B, "T": T, "tree": fam,
+           "depth": int(max(trees.tree_depth(p) for p in parents)), "us_per_call_after_l2_read": times}
+    if kind == "tree_conv":
+        # back to back over the eight pairs (each call's data is out of L2):
+        # one graph of 64 calls, replayed
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(64):
+                rotating(i)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            reps.append(1e3 * a.elapsed_time(b) / 64)
+        rec["us_per_call_back_to_back"] = reps
+        # the same bytes moved by a plain device copy (y = x), for scale
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            for i in range(64):
+                ys[i % 8].copy_(xs[i % 8])
+        g2.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g2.replay()
+        b.record()
+        torch.cuda.synchronize()
+        rec["us_per_plain_copy_of_x_back_to_back"] = 1e3 * a.elapsed_time(b) / 64
+    print(json.dumps(rec), flush=True)
 
 
 def main():
