@@ -840,6 +840,9 @@ PROFILE_CASES = {
     "verify256": ("verify", 16, 256, "random"),
     "verify256_chain": ("verify", 16, 256, "chain"),
     "neumann64": ("neumann", 16, 64, "random_depth_4_20"),
+    "neumann256": ("neumann", 16, 256, "random"),
+    "neumann256_top8": ("neumann", 16, 256, "top8"),
+    "split256": ("split", 16, 256, "random"),
     "commit64": ("commit", 16, 64, "random_depth_4_20"),
     "serial64": ("serial", 4, 64, "random_depth_4_20"),
     "path_replay3": ("path_replay", 16, 3, "random"),
@@ -883,9 +886,9 @@ def run_profile_case(args):
 
     if kind == "verify":
         fn = ver
-    elif kind == "neumann":
+    elif kind in ("neumann", "split"):
         def fn():
-            ver("neumann")
+            ver(kind)
     elif kind == "path_replay":
         def fn():
             ver(force="path_replay")

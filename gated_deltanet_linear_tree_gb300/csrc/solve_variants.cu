@@ -14,8 +14,9 @@
 // paths), gamma X_Q and R as [B][T][H][dv]; like the blocked substitution
 // they write U = (I + G)^-1 R to the workspace (the commit reads it) and
 //     o = scale (gamma X_Q + C U).
-// fp32 on CUDA cores, 64 x 64 tiles through shared memory.
-//   neumann_kernel  one CTA per (stream, head): Z <- -G Z for d rounds, U += Z;
+// The Neumann series beyond 64 nodes runs on tensor cores (neumann_tc.cu);
+// the two kernels here are fp32 on CUDA cores, 64 x 64 tiles through shared
+// memory:
 //   squaring_kernel one CTA per (stream, head): Z <- (I + P) Z with P = -G,
 //                   then P <- P^2 in place of G, k factors in all;
 //   invert_kernel   one CTA per (stream, head): W = (I + G)^-1 in place of G
@@ -193,44 +194,6 @@ __device__ __forceinline__ void finish(OutT* o, const float* sU, float* sA, cons
             for (int cc = 0; cc < 4; ++cc) store_out(op + cc, scale * acc[q][cc]);
         }
     }
-}
-
-// Finite Neumann series: Z_0 = R, Z_m = -G Z_{m-1}, U = sum_{m=0..d} Z_m
-// (d = the stream's tree depth; Z_{d+1} = 0).  U accumulates in registers
-// (16 entries per thread and block), Z lives in shared memory.
-template <typename OutT>
-__global__ void __launch_bounds__(NT, 1) neumann_kernel(OutT* __restrict__ o, int T, int H, Ws ws, float scale) {
-    extern __shared__ float smem[];
-    __shared__ int sDepth;
-    const int nb = (T + BN - 1) / BN;
-    float* sZ = smem;                          // [nb * BN][DV]
-    float* sA = sZ + size_t(nb) * BN * DV;     // [BN][GS]
-    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-    const int cg = t & 31, rg = t >> 5;
-    const size_t bh = size_t(b) * H + h;
-    const int d = stream_depth(ws, b, T, t, &sDepth);
-    load_panel(sZ, ws.rr, b, h, T, H, nb, t);
-    __syncthreads();
-    float u[MAXNB][4][4];
-#pragma unroll
-    for (int r = 0; r < MAXNB; ++r)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                u[r][q][cc] = (r < nb) ? sZ[size_t(BN * r + 4 * rg + q) * DV + 4 * cg + cc] : 0.f;
-    const float* G = ws.gs + bh * T * T;
-    for (int m = 1; m <= d; ++m) apply_panel<true, true>(sZ, sA, G, T, nb, t, u);
-#pragma unroll
-    for (int r = 0; r < MAXNB; ++r) {
-        if (r >= nb) continue;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(sZ + size_t(BN * r + 4 * rg + q) * DV + 4 * cg) =
-                make_float4(u[r][q][0], u[r][q][1], u[r][q][2], u[r][q][3]);
-    }
-    __syncthreads();
-    finish(o, sZ, sA, ws.cs + bh * T * T, ws, b, h, T, H, nb, scale, t);
 }
 
 // P <- P^2 in place for a [T][T] matrix with tiles on and below the
@@ -458,13 +421,6 @@ static cudaError_t launch_variant_typed(int variant, int T, int B, int H, OutT* 
                                         cudaStream_t st) {
     dim3 grid(H, B);
     cudaError_t e;
-    if (variant == 1) {
-        static bool attr = false;
-        e = set_smem_once(sv::neumann_kernel<OutT>, sv::panel_smem(kMaxT, 1), attr);
-        if (e != cudaSuccess) return e;
-        sv::neumann_kernel<OutT><<<grid, sv::NT, sv::panel_smem(T, 1), st>>>(o, T, H, ws, scale);
-        return cudaGetLastError();
-    }
     if (variant == 2) {
         static bool attr = false;
         e = set_smem_once(sv::squaring_kernel<OutT>, sv::panel_smem(kMaxT, 2), attr);
@@ -489,10 +445,14 @@ static cudaError_t launch_variant_typed(int variant, int T, int B, int H, OutT* 
     return cudaErrorInvalidValue;
 }
 
-// variant: 1 Neumann series, 2 squaring form, 3 split design (dk = dv = 128).
+cudaError_t launch_neumann_tc(int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
+
+// variant: 1 Neumann series (on tensor cores, neumann_tc.cu; T > 64), 2
+// squaring form, 3 split design (dk = dv = 128).
 cudaError_t launch_solve_variant(int variant, int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws,
                                  cudaStream_t st) {
     if (T < 1 || T > kMaxT) return cudaErrorInvalidValue;
+    if (variant == 1) return launch_neumann_tc(T, B, H, o, o_bf16, scale, ws, st);
     if (o_bf16)
         return launch_variant_typed(variant, T, B, H, static_cast<__nv_bfloat16*>(o), scale, ws, st);
     return launch_variant_typed(variant, T, B, H, static_cast<float*>(o), scale, ws, st);

@@ -54,7 +54,10 @@ CASES = {
 }
 
 # (case, solve) -> bound on max |o - o_ref| / rms(o_ref): ten times the error measured
-# on GB300 (fp32 o), rounded up to two significant digits
+# on GB300 (fp32 o), rounded up to two significant digits.  The Neumann bounds
+# beyond 64 nodes were set from the fp32 CUDA-core series; its tensor-core
+# successor (bf16 hi/lo products) measures 5-7x more and still passes them,
+# so they are kept as they are.
 BOUND = {
     ("chain13", "fwdsub"): 0.00057,  # measured 5.69e-05
     ("chain13", "neumann"): 0.00012,  # measured 1.15e-05
@@ -75,15 +78,15 @@ BOUND = {
     ("chain100", "fwdsub"): 0.00032,  # measured 3.12e-05
     ("chain100", "split"): 0.00032,  # measured 3.12e-05
     ("top2_200", "fwdsub"): 0.00025,  # measured 2.48e-05
-    ("top2_200", "neumann"): 0.00025,  # measured 2.48e-05
+    ("top2_200", "neumann"): 0.00025,  # measured 2.48e-05 by the fp32 CUDA-core series; the tensor-core series measures 1.70e-04
     ("top2_200", "squaring"): 0.00025,  # measured 2.48e-05
     ("top2_200", "split"): 0.00025,  # measured 2.49e-05
     ("random150", "fwdsub"): 0.00025,  # measured 2.45e-05
-    ("random150", "neumann"): 0.00025,  # measured 2.45e-05
+    ("random150", "neumann"): 0.00025,  # measured 2.45e-05 by the fp32 CUDA-core series; the tensor-core series measures 1.37e-04
     ("random150", "squaring"): 0.00025,  # measured 2.45e-05
     ("random150", "split"): 0.00025,  # measured 2.45e-05
     ("top4_256", "fwdsub"): 0.00022,  # measured 2.12e-05
-    ("top4_256", "neumann"): 0.00022,  # measured 2.12e-05
+    ("top4_256", "neumann"): 0.00022,  # measured 2.12e-05 by the fp32 CUDA-core series; the tensor-core series measures 1.24e-04
     ("top4_256", "squaring"): 0.00022,  # measured 2.12e-05
     ("skewed200", "fwdsub"): 0.00032,  # measured 3.14e-05
     ("skewed200", "split"): 0.00032,  # measured 3.14e-05
