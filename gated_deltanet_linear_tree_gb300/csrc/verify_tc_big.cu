@@ -103,7 +103,7 @@ struct Smem {
 
 enum {
     BAR_QK = 0, BAR_V, BAR_S0, BAR_S0B, BAR_SFREE, BAR_KS0, BAR_KS1, BAR_G, BAR_X, BAR_XT, BAR_MW, BAR_TGF,
-    BAR_CR0, BAR_CR1, BAR_W, BAR_DREAD, BAR_TREAD, BAR_CGB0, BAR_CGB1, NBAR
+    BAR_CR0, BAR_CR1, BAR_W, BAR_DREAD, BAR_TREAD, BAR_CGB0, BAR_CGB1, BAR_PREP, NBAR
 };
 static_assert(NBAR <= 32 && BAR_S0B == BAR_S0 + 1 && BAR_KS1 == BAR_KS0 + 1 && BAR_CR1 == BAR_CR0 + 1 &&
                   BAR_CGB1 == BAR_CGB0 + 1,
@@ -165,6 +165,58 @@ __device__ __forceinline__ void issue_gram(uint32_t tmem, uint32_t aQK, uint32_t
         const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
         const uint64_t db = sdesc_sw128(b_lo + (ks >> 2) * b_atom + (ks & 3) * 32);
         mma_bf16_ss(tmem + TG, da, db, idesc_bf16(128, 64), ks != 0);
+    }
+}
+
+// Path bitmasks and root-path log2 gate sums by pointer jumping (as in
+// jump_paths), run by the 128 solve threads alone, two nodes each, with
+// their named barrier; ceil(log2 T) rounds cover every root path.
+__device__ void jump_paths_solve(int T, int* sPtr, int* sLen, double* sS, uint64_t* sM) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int i = t + 128 * u;
+        if (i < T) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) sM[i * 4 + w] = (w == (i >> 6)) ? (1ull << (i & 63)) : 0ull;
+            sLen[i] = 1;
+        }
+    }
+    group_sync(1, 128);
+    int rounds = 0;
+    while ((1 << rounds) < T) ++rounds;
+    for (int round = 0; round < rounds; ++round) {
+        JumpState<4, double> st[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = t + 128 * u;
+            if (i >= T) continue;
+            const int pp = sPtr[i];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) st[u].m[w] = sM[i * 4 + w];
+            st[u].s = sS[i];
+            st[u].len = sLen[i];
+            st[u].ptr = pp;
+            if (pp >= 0) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) st[u].m[w] |= sM[pp * 4 + w];
+                st[u].s += sS[pp];
+                st[u].len += sLen[pp];
+                st[u].ptr = sPtr[pp];
+            }
+        }
+        group_sync(1, 128);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = t + 128 * u;
+            if (i >= T) continue;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) sM[i * 4 + w] = st[u].m[w];
+            sS[i] = st[u].s;
+            sLen[i] = st[u].len;
+            sPtr[i] = st[u].ptr;
+        }
+        group_sync(1, 128);
     }
 }
 
@@ -240,66 +292,76 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_relinquish();
         tc_fence_before();
     }
-    // Parents and gates, one thread per node; padded nodes (past T) have no
-    // path, beta 0 and gamma 1.
-    int bad = (tid == 0) ? lbad : 0;
-    if (tid < kMaxT) {
-        const int i = tid;
-        int par = -1;
-        float ga = 1.f, gb = 0.f;
-        if (i < T) {
-            par = p.parent[size_t(b) * Ts + i];
-            ga = p.g[(size_t(b) * Ts + i) * H + h];
-            gb = p.beta[(size_t(b) * Ts + i) * H + h];
-            if (!((i == 0) ? (par == -1) : (par >= 0 && par < i))) {
-                bad |= CANOPY_DEVERR_TREE;
-                par = (i == 0) ? -1 : 0;
-            }
-            if (!gate_ok(ga, gb)) {
-                bad |= CANOPY_DEVERR_GATE;
-                ga = 1.f;
-                gb = 0.f;
-            }
-        }
-        sPar[i] = par;
-        sLsum[i] = (i < T) ? double(log2f(ga)) : 0.0;
-        sBeta[i] = gb;
-    }
-    __syncthreads();  // barrier initialisation and the node arrays are visible
-
-    // ---- tree prep: path bitmasks and root-path log2 gate sums (fp64) by
-    // pointer jumping; every CTA of the stream does the same small work ----
-    jump_paths<4, double>(T, sPar, sLen, sLsum, sMask);
-    if (tid < kMaxT) {
-        const int i = tid;
-        if (i >= T) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) sMask[i * 4 + w] = 0ull;
-            sLen[i] = 0;
-        }
-        const float l2 = (i < T) ? float(sLsum[i]) : 0.f;
-        sL2[i] = l2;
-        sGam[i] = exp2f(l2);
-    }
-    __syncthreads();
+    __syncthreads();  // barrier initialisation and the tensor-memory address are visible
     tc_fence_after();
     const uint32_t tmem = *sTmem;
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
 
-    // tree outputs for the commit: l (natural log), depth, strict-ancestor mask
-    if (bad) raise_err(p.err, bad);
-    if (tid < T) {
-        p.l[(size_t(b) * Ts + tid) * H + h] = sL2[tid] * 0.69314718055994531f;
-        if (h == 0) {
-            p.depth[size_t(b) * Ts + tid] = sLen[tid] - 1;
-            for (int w = 0; w < p.W; ++w) {
-                uint32_t word = uint32_t(sMask[tid * 4 + (w >> 1)] >> (32 * (w & 1)));
-                if (w == (tid >> 5)) word &= ~(1u << (tid & 31));
-                p.mask[(size_t(b) * Ts + tid) * p.W + w] = word;
+    if (warp < 4) {
+        // ---- tree prep by the solve warps (their named barrier), while the
+        // state warps convert S0 and the issuer starts the first Gram
+        // product: parents and gates, two nodes per thread (padded nodes
+        // have no path, beta 0 and gamma 1), then path bitmasks and
+        // root-path log2 gate sums (fp64) by pointer jumping; every CTA of
+        // the stream does the same small work ----
+        int bad = (tid == 0) ? lbad : 0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + 128 * u;
+            int par = -1;
+            float ga = 1.f, gb = 0.f;
+            if (i < T) {
+                par = p.parent[size_t(b) * Ts + i];
+                ga = p.g[(size_t(b) * Ts + i) * H + h];
+                gb = p.beta[(size_t(b) * Ts + i) * H + h];
+                if (!((i == 0) ? (par == -1) : (par >= 0 && par < i))) {
+                    bad |= CANOPY_DEVERR_TREE;
+                    par = (i == 0) ? -1 : 0;
+                }
+                if (!gate_ok(ga, gb)) {
+                    bad |= CANOPY_DEVERR_GATE;
+                    ga = 1.f;
+                    gb = 0.f;
+                }
+            }
+            sPar[i] = par;
+            sLsum[i] = (i < T) ? double(log2f(ga)) : 0.0;
+            sBeta[i] = gb;
+        }
+        group_sync(1, 128);
+        jump_paths_solve(T, sPar, sLen, sLsum, sMask);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + 128 * u;
+            if (i >= T) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) sMask[i * 4 + w] = 0ull;
+                sLen[i] = 0;
+            }
+            const float l2 = (i < T) ? float(sLsum[i]) : 0.f;
+            sL2[i] = l2;
+            sGam[i] = exp2f(l2);
+        }
+        group_sync(1, 128);
+        // tree outputs for the commit: l (natural log), depth, strict-ancestor mask
+        if (bad) raise_err(p.err, bad);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + 128 * u;
+            if (i >= T) continue;
+            p.l[(size_t(b) * Ts + i) * H + h] = sL2[i] * 0.69314718055994531f;
+            if (h == 0) {
+                p.depth[size_t(b) * Ts + i] = sLen[i] - 1;
+                for (int w = 0; w < p.W; ++w) {
+                    uint32_t word = uint32_t(sMask[i * 4 + (w >> 1)] >> (32 * (w & 1)));
+                    if (w == (i >> 5)) word &= ~(1u << (i & 31));
+                    p.mask[(size_t(b) * Ts + i) * p.W + w] = word;
+                }
             }
         }
+        group_sync(1, 128);  // the tree-prep arrays inside the path lists are no longer read
+        if (tid == 0) mbar_arrive(&bars[BAR_PREP]);  // gamma, beta and the masks are ready
     }
-    __syncthreads();  // the tree-prep arrays inside the path lists are no longer read
 
     const uint32_t aQK = smem_u32(sm + L::QK);
     uint32_t ks_issued[2] = {0u, 0u};  // issuer: K_s copies per slot
@@ -620,6 +682,7 @@ __global__ void __launch_bounds__(NT, 1)
             __syncwarp();
             wait_or_flag(&bars[BAR_X], pr, sFlag);
             wait_or_flag(&bars[BAR_V], pr, sFlag);
+            if (r == 0) wait_or_flag(&bars[BAR_PREP], 0, sFlag);  // gamma and beta
             tc_fence_after();
 #pragma unroll 1
             for (int hb = 0; hb < 2; ++hb) {
