@@ -339,6 +339,7 @@ def run_canopy(args, world, rank, local):
         traffic = VERIFY_DRAM_TRAFFIC["read"] + VERIFY_DRAM_TRAFFIC["write"]
 
     e2e = run_e2e(canopy, sets, T, args, world)
+    e2e_copied = run_e2e(canopy, sets, T, args, world, state_on_device=False)
     line = {
         "metric": METRIC, "value": value, "unit": "verified nodes/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -372,6 +373,7 @@ def run_canopy(args, world, rank, local):
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "e2e": e2e,
+        "e2e_state_copied": e2e_copied,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sets[0]["host"], args.cpu_seconds)
@@ -389,47 +391,101 @@ def bench_config(args, world):
             "parallelism": f"replicas x{world}"}
 
 
-def run_e2e(canopy, sets, T, args, world):
+def run_e2e(canopy, sets, T, args, world, state_on_device=True):
     """Same metric through the public API with host buffers: every step copies
-    its inputs from pinned host memory and reads o and S_new back."""
+    its inputs from pinned host memory and reads its output o back.  With
+    state_on_device (decoding as it runs: the recurrent state never leaves
+    the GPU), the inputs are the round's q, k, v, g, beta, parent and accepted
+    leaf, and each step verifies against the state and commits into it in
+    place; otherwise S0 is copied in and S_new read back every step as well.
+    A step's inputs travel as one packed host-to-device copy and its results
+    as one packed device-to-host copy, each on a stream of its own, so that
+    step i + 1's inputs and step i - 1's results move while step i computes
+    (three device buffer sets in rotation; events order every reuse)."""
     import torch
     K = max(10, min(args.e2e_steps, args.steps))
-    names = ("q", "k", "v", "g", "beta", "S0", "parent", "acc")
-    hosts = []
+    names = ("q", "k", "v", "g", "beta", "parent", "acc") + (() if state_on_device else ("S0",))
+    outs = ("o",) + (() if state_on_device else ("S_new",))
+
+    def packing(fields):
+        lay, off = [], 0
+        for n, t in fields:
+            nb = t.numel() * t.element_size()
+            lay.append((n, off, nb, t.dtype, tuple(t.shape)))
+            off = (off + nb + 255) // 256 * 256
+        return lay, off
+
+    def views(buf, lay):
+        return {n: buf[o:o + nb].view(dt).view(sh) for n, o, nb, dt, sh in lay}
+
+    in_lay, in_size = packing([(n, sets[0][n]) for n in names])
+    out_lay, out_size = packing([(n, sets[0][n]) for n in outs])
+    h2d = sum(nb for _, _, nb, _, _ in in_lay)
+    d2h = sum(nb for _, _, nb, _, _ in out_lay)
+    host_in = []
     for s in sets[:2]:
-        hosts.append({n: s[n].cpu().pin_memory() for n in names})
-    dev = {n: torch.empty_like(sets[0][n]) for n in names}
-    ws = sets[0]["ws"]
-    o = torch.empty_like(sets[0]["o"])
-    S_new = torch.empty_like(sets[0]["S0"])
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    S_h = torch.empty(S_new.shape, dtype=S_new.dtype).pin_memory()
-    h2d = sum(hosts[0][n].numel() * hosts[0][n].element_size() for n in names)
-    d2h = o.numel() * o.element_size() + S_new.numel() * S_new.element_size()
-
-    def one(h):
+        hb = torch.empty(in_size, dtype=torch.uint8).pin_memory()
+        hv = views(hb, in_lay)
         for n in names:
-            dev[n].copy_(h[n], non_blocking=True)
-        canopy.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["S0"], dev["parent"], ws,
-                      solve=args.solve, out=o)
-        canopy.commit(dev["acc"], dev["S0"], dev["k"], dev["parent"], ws, out=S_new)
-        o_h.copy_(o, non_blocking=True)
-        S_h.copy_(S_new, non_blocking=True)
+            hv[n].copy_(s[n].cpu())
+        host_in.append(hb)
+    host_out = [torch.empty(out_size, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    dev_in = [torch.empty(in_size, dtype=torch.uint8, device="cuda") for _ in range(3)]
+    dev_out = [torch.empty(out_size, dtype=torch.uint8, device="cuda") for _ in range(3)]
+    din = [views(x, in_lay) for x in dev_in]
+    dout = [views(x, out_lay) for x in dev_out]
+    state = sets[0]["S0"].clone() if state_on_device else None
+    ws = sets[0]["ws"]
+    cur = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, computed, out_read = [ev() for _ in range(3)], [ev() for _ in range(3)], [ev() for _ in range(3)]
+    for e in computed + out_read:
+        e.record(cur)
 
-    for i in range(3):
-        one(hosts[i % 2])
+    def one(i):
+        j, hsel = i % 3, i % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(computed[j])          # step i - 3 has finished with these inputs
+            dev_in[j].copy_(host_in[hsel], non_blocking=True)
+            in_ready[j].record(s_in)
+        cur.wait_event(in_ready[j])
+        cur.wait_event(out_read[j])               # step i - 3's results have left
+        d, o = din[j], dout[j]
+        S0 = state if state_on_device else d["S0"]
+        S_new = state if state_on_device else o["S_new"]
+        canopy.verify(d["q"], d["k"], d["v"], d["g"], d["beta"], S0, d["parent"], ws, solve=args.solve,
+                      out=o["o"])
+        canopy.commit(d["acc"], S0, d["k"], d["parent"], ws, out=S_new)
+        computed[j].record(cur)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(computed[j])
+            host_out[hsel].copy_(dev_out[j], non_blocking=True)
+            out_read[j].record(s_out)
+
+    for i in range(6):
+        one(i)
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    a.record(cur)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
     for i in range(K):
-        one(hosts[i % 2])
-    b.record()
+        one(i)
+    cur.wait_stream(s_out)
+    b.record(cur)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), world)
-    B = dev["parent"].shape[0]
+    assert canopy.read_device_error(ws) == 0
+    B = sets[0]["parent"].shape[0]
+    what = ("q, k, v, g, beta, parent and the accepted leaf in, o out; the recurrent state stays on the GPU and "
+            "is committed in place" if state_on_device else
+            "q, k, v, g, beta, parent, the accepted leaf and S0 in, o and S_new out")
     return {"value": B * T * K * world / (ms / 1e3), "unit": "verified nodes/s", "steps": K,
-            "ms_per_step": ms / K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": ms / K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": f"per step: {what}; one packed pinned host-to-device copy and one packed device-to-host "
+                      "copy, on their own streams, overlapping the neighbouring steps' compute"}
 
 
 def _oracle_streams(args):
