@@ -48,26 +48,57 @@ struct CommitSmem {
 };
 
 // Stage path nodes c0 .. c0 + cn - 1: their k rows, and (after the verify has
-// completed) their weighted u rows.
+// completed) their weighted u rows.  Each thread issues all its loads before
+// it stores any of them, so a chunk costs one memory round trip.
 template <typename InT, int DK, int DV>
 __device__ __forceinline__ void stage_k(CommitSmem<InT, DK, DV>& S, const InT* __restrict__ k, int b, int T, int HK,
                                         int hk, int c0, int cn) {
     constexpr int KV = 16 / sizeof(InT);  // k elements per 16-byte load
-    for (int e = threadIdx.x; e < cn * (DK / KV); e += NT) {
-        const int r = e / (DK / KV), c = (e % (DK / KV)) * KV, j = S.path[c0 + r];
-        *reinterpret_cast<uint4*>(&S.k[r][c]) =
-            *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
+    constexpr int PER = DK / KV;          // 16-byte loads per k row
+    constexpr int IT = (CH * PER + NT - 1) / NT;
+    uint4 buf[IT];
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int e = threadIdx.x + i * NT;
+        if (e < cn * PER) {
+            const int r = e / PER, c = (e % PER) * KV, j = S.path[c0 + r];
+            buf[i] = *reinterpret_cast<const uint4*>(k + ((size_t(b) * T + j) * HK + hk) * DK + c);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int e = threadIdx.x + i * NT;
+        if (e < cn * PER) *reinterpret_cast<uint4*>(&S.k[e / PER][(e % PER) * KV]) = buf[i];
     }
 }
+// la = l of the accepted node; with cn > 0 it is read here, in the same round
+// trip as the chunk's l and u entries (path[0] is the accepted node).
 template <typename InT, int DK, int DV>
 __device__ __forceinline__ void stage_wu(CommitSmem<InT, DK, DV>& S, const Ws& ws, int b, int T, int H, int h,
-                                         float la, int c0, int cn) {
-    for (int e = threadIdx.x; e < cn * (DV / 4); e += NT) {
-        const int r = e / (DV / 4), c = (e % (DV / 4)) * 4, j = S.path[c0 + r];
-        const size_t nh = (size_t(b) * T + j) * H + h;
-        const float w = expf(la - ws.l[nh]);
-        const float4 u = *reinterpret_cast<const float4*>(ws.U + nh * DV + c);
-        *reinterpret_cast<float4*>(&S.wu[r][c]) = make_float4(w * u.x, w * u.y, w * u.z, w * u.w);
+                                         float& la, bool read_la, int c0, int cn) {
+    constexpr int PER = DV / 4;
+    constexpr int IT = (CH * PER + NT - 1) / NT;
+    if (read_la) la = ws.l[(size_t(b) * T + S.path[0]) * H + h];
+    float lj[IT];
+    float4 u[IT];
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int e = threadIdx.x + i * NT;
+        if (e < cn * PER) {
+            const int r = e / PER, c = (e % PER) * 4;
+            const size_t nh = (size_t(b) * T + S.path[c0 + r]) * H + h;
+            lj[i] = ws.l[nh];
+            u[i] = *reinterpret_cast<const float4*>(ws.U + nh * DV + c);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int e = threadIdx.x + i * NT;
+        if (e < cn * PER) {
+            const float w = expf(la - lj[i]);
+            *reinterpret_cast<float4*>(&S.wu[e / PER][(e % PER) * 4]) =
+                make_float4(w * u[i].x, w * u[i].y, w * u[i].z, w * u[i].w);
+        }
     }
 }
 
@@ -97,6 +128,22 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     // completed.
     if (!state_ready) pdl_wait();
     pdl_trigger();
+    // Warp 0 requests the stream's parents, its length and the accepted node
+    // before the S0 copies are issued, so that these few bytes (which the
+    // path walk, and through it every later read, waits on) are not queued
+    // behind the 64 KB of S0 per CTA.
+    constexpr int PPL = kMaxT / 32;  // parents per lane
+    int pj[PPL];
+    int a = -1, len = T;
+    if (t < 32) {
+#pragma unroll
+        for (int i = 0; i < PPL; ++i) {
+            const int j = t + 32 * i;
+            pj[i] = (j < T) ? parent[size_t(b) * T + j] : 0;
+        }
+        a = accepted[b];
+        if (lengths) len = lengths[b];
+    }
     if (t == 0) {
         for (int i = 0; i < NTILE; ++i) mbar_init(&S.bar[i], 1);
         fence_mbar_init();
@@ -108,12 +155,16 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     if (t < 32) {
         // the stream's nodes: lengths[b] of the T-strided arrays (all T without lengths)
         int lbad = 0;
-        const int Tb = stream_len(lengths, b, T, &lbad);
-        for (int j = t; j < Tb; j += 32) S.par[j] = parent[size_t(b) * T + j];
-        int a = accepted[b];
+        if (len < 0 || len > T) {
+            lbad = CANOPY_DEVERR_LENGTH;
+            len = len < 0 ? 0 : T;
+        }
+#pragma unroll
+        for (int i = 0; i < PPL; ++i)
+            if (t + 32 * i < len) S.par[t + 32 * i] = pj[i];
         __syncwarp();
         if (t == 0) {
-            int bad = (a < -1 || a >= Tb) ? CANOPY_DEVERR_ACCEPTED : 0;
+            int bad = (a < -1 || a >= len) ? CANOPY_DEVERR_ACCEPTED : 0;
             if (bad) a = -1;
             bad |= lbad;
             // path(a) from a up to the root, parents sanitised as the verify
@@ -122,8 +173,8 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
             int n = 0;
             for (int j = a; j >= 0;) {
                 S.path[n++] = j;
-                const int pj = S.par[j];
-                j = (j == 0) ? -1 : ((pj >= 0 && pj < j) ? pj : 0);
+                const int p = S.par[j];
+                j = (j == 0) ? -1 : ((p >= 0 && p < j) ? p : 0);
             }
             S.n = n;
             S.bad = bad;
@@ -135,9 +186,9 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
     stage_k(S, k, b, T, HK, hk, 0, min(CH, n));
     if (state_ready) pdl_wait();
     if (S.bad && t == 0 && h == 0 && blockIdx.x == 0) raise_err(ws.err, S.bad);
-    const float la = (n > 0) ? ws.l[(size_t(b) * T + S.path[0]) * H + h] : 0.f;
+    float la = 0.f;
+    stage_wu(S, ws, b, T, H, h, la, n > 0, 0, min(CH, n));
     const float gamma_a = (n > 0) ? expf(la) : 1.f;
-    stage_wu(S, ws, b, T, H, h, la, 0, min(CH, n));
     __syncthreads();
 
     bool timeout = false;
@@ -159,7 +210,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(const int32_t* __restrict__ 
                 // deep paths: the chunk's k and u rows are staged again
                 __syncthreads();
                 stage_k(S, k, b, T, HK, hk, ch * CH, cn);
-                stage_wu(S, ws, b, T, H, h, la, ch * CH, cn);
+                stage_wu(S, ws, b, T, H, h, la, false, ch * CH, cn);
                 __syncthreads();
             }
             for (int r = 0; r < cn; ++r) {
