@@ -188,7 +188,8 @@ __host__ __device__ constexpr size_t tap_offset(int T, int es) { return size_t(T
 __host__ __device__ constexpr size_t par_offset(int T, int es, int K) {
     return (tap_offset(T, es) + size_t(T) * K * 2 + 15) & ~size_t(15);
 }
-__host__ __device__ constexpr size_t conv8_smem(int T, int es, int K) { return par_offset(T, es, K) + size_t(T) * 4; }
+__host__ __device__ constexpr size_t st_offset(int T, int es, int K) { return (par_offset(T, es, K) + size_t(T) * 4 + 15) & ~size_t(15); }
+__host__ __device__ constexpr size_t conv8_smem(int T, int es, int K) { return st_offset(T, es, K) + size_t(K - 1) * CB * 4; }
 
 // C a multiple of 8.  Thread i < T first lists node i's K tap sources,
 // newest first: tap m is the node m steps up the root path, or, once the
@@ -202,12 +203,47 @@ __global__ void __launch_bounds__(NT, (K <= 4) ? 3 : 2) tree_conv8_kernel(const 
     T_* sX = reinterpret_cast<T_*>(conv_smem_raw);                                               // [T][CB]
     int16_t* sTap = reinterpret_cast<int16_t*>(conv_smem_raw + tap_offset(T, sizeof(T_)));       // [T][K]
     int* sPar = reinterpret_cast<int*>(conv_smem_raw + par_offset(T, sizeof(T_), K));            // [T]
+    float* sS = reinterpret_cast<float*>(conv_smem_raw + st_offset(T, sizeof(T_), K));          // [K-1][CB]
     const int b = blockIdx.y, cb0 = blockIdx.x * CB;
     const int ct = threadIdx.x % CT8, nl = threadIdx.x / CT8;  // channel thread, node lane
     const int c = cb0 + 8 * ct;                                // first of this thread's eight channels
     const bool live = c < C;                                   // all eight or none (C % 8 == 0)
+    // x rows four at a time, every load of a group issued before its stores
+    // (one memory round trip per group rather than per row)
+    constexpr int XG = 4;
+    constexpr int XW = 8 * int(sizeof(T_)) / 16;  // 16-byte words per eight channels
     if (live)
-        for (int r = nl; r < T; r += NL8) copy8c(sX + size_t(r) * CB + 8 * ct, x + (size_t(b) * T + r) * C + c);
+        for (int r0 = nl; r0 < T; r0 += XG * NL8) {
+            uint4 buf[XG][XW];
+#pragma unroll
+            for (int g = 0; g < XG; ++g)
+                if (r0 + g * NL8 < T)
+#pragma unroll
+                    for (int q = 0; q < XW; ++q)
+                        buf[g][q] = reinterpret_cast<const uint4*>(x + (size_t(b) * T + r0 + g * NL8) * C + c)[q];
+#pragma unroll
+            for (int g = 0; g < XG; ++g)
+                if (r0 + g * NL8 < T)
+#pragma unroll
+                    for (int q = 0; q < XW; ++q)
+                        reinterpret_cast<uint4*>(sX + size_t(r0 + g * NL8) * CB + 8 * ct)[q] = buf[g][q];
+        }
+    // the committed state of this CTA's channels (contiguous in [C][K-1]),
+    // transposed to one row per slot, so that no tap waits on global memory
+    {
+        constexpr int SG = (CB * (K - 1) + NT - 1) / NT;
+        float sv[SG];
+#pragma unroll
+        for (int g = 0; g < SG; ++g) {
+            const int e = threadIdx.x + g * NT;
+            if (e < CB * (K - 1) && cb0 + e / (K - 1) < C) sv[g] = state[(size_t(b) * C + cb0) * (K - 1) + e];
+        }
+#pragma unroll
+        for (int g = 0; g < SG; ++g) {
+            const int e = threadIdx.x + g * NT;
+            if (e < CB * (K - 1) && cb0 + e / (K - 1) < C) sS[(e % (K - 1)) * CB + e / (K - 1)] = sv[g];
+        }
+    }
     load_parents(parent, b, T, sPar, err, blockIdx.x == 0);
     // this thread's weights (w[c .. c+7][0 .. K-1], contiguous and 16-byte
     // aligned since c is a multiple of 8) and bias; the committed state is
@@ -248,9 +284,10 @@ __global__ void __launch_bounds__(NT, (K <= 4) ? 3 : 2) tree_conv8_kernel(const 
             if (t >= 0) {
                 load8c(sX + size_t(t) * CB + 8 * ct, v);
             } else {
-                const float* sp = state + (size_t(b) * C + c) * (K - 1) + (-1 - t);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __ldg(sp + e * (K - 1));
+                const float4* sp = reinterpret_cast<const float4*>(sS + (-1 - t) * CB + 8 * ct);
+                const float4 a0 = sp[0], a1 = sp[1];
+                v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+                v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = fmaf(wf[e * K + (K - 1 - m)], v[e], acc[e]);
