@@ -195,7 +195,7 @@ __host__ __device__ constexpr size_t conv8_smem(int T, int es, int K) { return s
 // newest first: tap m is the node m steps up the root path, or, once the
 // path (n nodes) has been passed, state slot K-2-(m-n), stored as -1 - slot.
 template <typename T_, int K>
-__global__ void __launch_bounds__(NT, (K <= 4) ? 3 : 2) tree_conv8_kernel(const T_* __restrict__ x, const float* __restrict__ state,
+__global__ void __launch_bounds__(NT, (K <= 4) ? 4 : 2) tree_conv8_kernel(const T_* __restrict__ x, const float* __restrict__ state,
                                                         const float* __restrict__ w, const float* __restrict__ bias,
                                                         const int32_t* __restrict__ parent, int T, int C, int silu,
                                                         T_* __restrict__ y, int32_t* err) {
