@@ -898,6 +898,8 @@ PROFILE_CASES = {
     "neumann64": ("neumann", 16, 64, "random_depth_4_20"),
     "neumann256": ("neumann", 16, 256, "random"),
     "neumann256_top8": ("neumann", 16, 256, "top8"),
+    "squaring256": ("squaring", 16, 256, "random"),
+    "squaring256_chain": ("squaring", 16, 256, "chain"),
     "split256": ("split", 16, 256, "random"),
     "commit64": ("commit", 16, 64, "random_depth_4_20"),
     "serial64": ("serial", 4, 64, "random_depth_4_20"),
@@ -942,7 +944,7 @@ def run_profile_case(args):
 
     if kind == "verify":
         fn = ver
-    elif kind in ("neumann", "split"):
+    elif kind in ("neumann", "squaring", "split"):
         def fn():
             ver(kind)
     elif kind == "path_replay":

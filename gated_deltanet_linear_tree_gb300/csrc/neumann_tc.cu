@@ -27,105 +27,17 @@
 // block w / 4.  Every mbarrier wait is bounded; a timeout sets
 // CANOPY_DEVERR_TIMEOUT, the later rounds are skipped, and the products in
 // flight are awaited (bounded) before tensor memory is freed.
-#include "common.cuh"
+#include "tc_tiles.cuh"
 
 namespace canopy {
 
 namespace ntc {
 
+using namespace tct;
+
 constexpr int NT = 512;
-constexpr int DV = 128;
-constexpr int BN = 64;                 // nodes per block
-constexpr int MAXNB = kMaxT / BN;      // blocks per tree at most
-constexpr int NTILE = MAXNB * (MAXNB + 1) / 2;
-constexpr int TILE = 16384;            // hi [64 rows][128 B] then lo
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t AY = 0;             // Y^T hi/lo: block s at 64 s (hi), 64 s + 32 (lo)
-constexpr uint32_t TD = 256;           // D: block r at 256 + 64 r
 constexpr int SMEM = NTILE * TILE + 128;
 static_assert(SMEM + 1024 <= 227 * 1024, "shared memory");
-
-__device__ inline int tile_index(int r, int s) { return r * (r + 1) / 2 + s; }
-
-// Two-part bf16 split with integer operations only: hi = x rounded half-up
-// to 8 significant bits, lo = the top 16 bits of x - hi.
-__device__ inline uint32_t hi_bits(float x) { return (__float_as_uint(x) + 0x8000u) & 0xFFFF0000u; }
-__device__ inline void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    const uint32_t h0 = hi_bits(x0), h1 = hi_bits(x1);
-    hi = __byte_perm(h0, h1, 0x7632);
-    lo = __byte_perm(__float_as_uint(x0 - __uint_as_float(h0)), __float_as_uint(x1 - __uint_as_float(h1)), 0x7632);
-}
-
-// Tiles (r, s <= r) of the [T][T] matrix m, times sign, as bf16 hi/lo B
-// operands (row rho = node 64 r + rho, K = node 64 s + j, 128-byte swizzle);
-// entries outside the tree read as zero.  nonzero[t] is set for every tile t
-// with an entry on a root path (the others contribute nothing and are
-// skipped); the caller clears it first.
-__device__ void stage_tiles(uint8_t* sm, const float* m, int T, int nb, float sign, int* nonzero) {
-    constexpr int PER_TILE = BN * 8;  // rows x 16-byte chunks
-    constexpr int BATCH = 5;          // chunks whose loads are in flight together
-    const int total = nb * (nb + 1) / 2 * PER_TILE;
-    for (int e0 = threadIdx.x; e0 < total; e0 += BATCH * NT) {
-        float x[BATCH][8];
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const int e = e0 + k * NT;
-            const int t = e / PER_TILE, rem = e - t * PER_TILE, rho = rem >> 3, c8 = rem & 7;
-            int r = 0;
-            while ((r + 1) * (r + 2) / 2 <= t) ++r;
-            const int s = t - r * (r + 1) / 2;
-            const int i = BN * r + rho, j0 = BN * s + 8 * c8;
-            if (e < total && i < T && j0 + 7 < T && (T & 3) == 0) {
-                const float4 a = *reinterpret_cast<const float4*>(m + size_t(i) * T + j0);
-                const float4 b = *reinterpret_cast<const float4*>(m + size_t(i) * T + j0 + 4);
-                x[k][0] = a.x; x[k][1] = a.y; x[k][2] = a.z; x[k][3] = a.w;
-                x[k][4] = b.x; x[k][5] = b.y; x[k][6] = b.z; x[k][7] = b.w;
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    x[k][u] = (e < total && i < T && j0 + u < T) ? m[size_t(i) * T + j0 + u] : 0.f;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const int e = e0 + k * NT;
-            if (e >= total) break;
-            const int t = e / PER_TILE, rem = e - t * PER_TILE, rho = rem >> 3, c8 = rem & 7;
-            bool nz = false;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) nz |= (x[k][u] != 0.f);
-            if (nz) nonzero[t] = 1;  // benign race: every writer stores 1
-            uint4 hv, lv;
-            split2(sign * x[k][0], sign * x[k][1], hv.x, lv.x);
-            split2(sign * x[k][2], sign * x[k][3], hv.y, lv.y);
-            split2(sign * x[k][4], sign * x[k][5], hv.z, lv.z);
-            split2(sign * x[k][6], sign * x[k][7], hv.w, lv.w);
-            uint8_t* base = sm + t * TILE + rho * 128 + ((c8 ^ (rho & 7)) << 4);
-            *reinterpret_cast<uint4*>(base) = hv;
-            *reinterpret_cast<uint4*>(base + TILE / 2) = lv;
-        }
-    }
-}
-
-// D_r += A_s B_rs^T for every block r < nb and s <= r whose tile has a
-// nonzero entry: three bf16 passes (A hi * B hi, A hi * B lo, A lo * B hi),
-// K = 64 nodes per tile.
-__device__ inline void issue_products(uint32_t tmem, const uint8_t* sm, int nb, const int* nonzero) {
-    for (int r = 0; r < nb; ++r)
-        for (int s = 0; s <= r; ++s) {
-            if (!nonzero[tile_index(r, s)]) continue;
-            const uint32_t bt = smem_u32(sm + tile_index(r, s) * TILE);
-#pragma unroll
-            for (int pass = 0; pass < 3; ++pass) {
-                const uint32_t acol = AY + 64 * s + (pass == 2 ? 32 : 0);
-                const uint32_t bb = bt + (pass == 1 ? TILE / 2 : 0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TD + 64 * r, tmem + acol + ks * 8, sdesc_sw128(bb + ks * 32),
-                                idesc_bf16(128, 64), 1);
-            }
-        }
-}
 
 // This thread's 64 nodes of a [B][T][H][DV] array (column c) into D.
 __device__ inline void load_into_d(uint32_t lane_base, const float* src, int b, int h, int T, int H, int n0, int c) {
@@ -177,7 +89,7 @@ __global__ void __launch_bounds__(NT, 1) neumann_tc_kernel(OutT* __restrict__ o,
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
     // the stream's depth d (tree prep's depths): G^(d+1) = 0
     for (int i = tid; i < T; i += NT) atomicMax(sDepth, ws.depth[size_t(b) * T + i]);
-    stage_tiles(sm, ws.gs + bh * T * T, T, nb, -1.f, sNz);
+    stage_tiles(sm, ws.gs + bh * T * T, T, nb, -1.f, sNz, NT);
     fence_proxy_async_smem();
     __syncthreads();
     const int d = min(max(*sDepth, 0), T - 1);
@@ -247,7 +159,7 @@ __global__ void __launch_bounds__(NT, 1) neumann_tc_kernel(OutT* __restrict__ o,
     if (!*sFlag) {
         if (tid < NTILE) sNz[tid] = 0;
         __syncthreads();
-        stage_tiles(sm, ws.cs + bh * T * T, T, nb, 1.f, sNz);
+        stage_tiles(sm, ws.cs + bh * T * T, T, nb, 1.f, sNz, NT);
         fence_proxy_async_smem();
         if (active) load_into_d(lane_base, ws.xq, b, h, T, H, n0, c);
         tc_fence_before();

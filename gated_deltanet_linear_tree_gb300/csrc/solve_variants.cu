@@ -14,18 +14,16 @@
 // paths), gamma X_Q and R as [B][T][H][dv]; like the blocked substitution
 // they write U = (I + G)^-1 R to the workspace (the commit reads it) and
 //     o = scale (gamma X_Q + C U).
-// The Neumann series beyond 64 nodes runs on tensor cores (neumann_tc.cu);
-// the two kernels here are fp32 on CUDA cores, 64 x 64 tiles through shared
-// memory:
-//   squaring_kernel one CTA per (stream, head): Z <- (I + P) Z with P = -G,
-//                   then P <- P^2 in place of G, k factors in all;
+// The Neumann series beyond 64 nodes and the squaring form run on tensor
+// cores (neumann_tc.cu, squaring_tc.cu); the split design's two kernels here
+// are fp32 on CUDA cores, 64 x 64 tiles through shared memory:
 //   invert_kernel   one CTA per (stream, head): W = (I + G)^-1 in place of G
 //                   (block row by block row) and M = C W in place of C;
 //   apply_kernel    one CTA per (stream, head, 64-node block, 64 value
 //                   columns): U_r = sum_s W_rs R_s, o_r = gamma X_Q,r +
 //                   sum_s M_rs R_s, with no dependence between CTAs.
-// The squaring and split kernels overwrite the G and C scratch, which
-// nothing reads after the verify.
+// The split kernels overwrite the G and C scratch (and the squaring form G),
+// which nothing reads after the verify.
 #include <algorithm>
 
 #include "common.cuh"
@@ -38,7 +36,6 @@ constexpr int BN = 64;    // nodes per tile
 constexpr int GS = 68;    // row stride of a staged tile (floats)
 constexpr int DV = 128;   // value columns (dk = dv = 128)
 constexpr int NT = 512;   // threads of the per-(stream, head) kernels
-constexpr int MAXNB = kMaxT / BN;
 constexpr int APPLY_NT = 256;
 
 // Tile (r, s) of a [T][T] matrix into a [BN][GS] staging tile; entries
@@ -101,153 +98,6 @@ __device__ __forceinline__ void mac(float (&acc)[MR][4], const float* a, const f
             }
         }
     }
-}
-
-// Rows of a [B][T][H][DV] array for (b, h) into shared [nb * BN][DV];
-// rows >= T read as zero.
-__device__ __forceinline__ void load_panel(float* dst, const float* src, int b, int h, int T, int H, int nb, int t) {
-    for (int e = t; e < nb * BN * (DV / 4); e += NT) {
-        const int i = e / (DV / 4), c4 = e % (DV / 4);
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < T) x = *reinterpret_cast<const float4*>(src + ((size_t(b) * T + i) * H + h) * DV + 4 * c4);
-        *reinterpret_cast<float4*>(dst + size_t(i) * DV + 4 * c4) = x;
-    }
-}
-
-// Deepest node of stream b (depths from tree prep), clamped to [0, T - 1].
-__device__ __forceinline__ int stream_depth(const Ws& ws, int b, int T, int t, int* sd) {
-    if (t == 0) *sd = 0;
-    __syncthreads();
-    for (int i = t; i < T; i += NT) atomicMax(sd, ws.depth[size_t(b) * T + i]);
-    __syncthreads();
-    return min(max(*sd, 0), T - 1);
-}
-
-// Z_r <- Z_r + sign * sum_{s <= r} P_rs Z_s for every 64-node block r, in
-// place: blocks from the last to the first, since block r reads only blocks
-// s <= r.  Z is [nb * BN][DV] in shared memory; P is a [T][T] matrix whose
-// tiles above the diagonal are never read.  With KEEP, Z_r is not added
-// (Z <- sign P Z), and the new Z_r is also added to u[r].
-template <bool SUB, bool KEEP>
-__device__ __forceinline__ void apply_panel(float* sZ, float* sA, const float* P, int T, int nb, int t,
-                                            float (&u)[MAXNB][4][4]) {
-    const int cg = t & 31, rg = t >> 5;
-#pragma unroll
-    for (int r = MAXNB - 1; r >= 0; --r) {
-        if (r >= nb) continue;
-        float acc[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                acc[q][cc] = KEEP ? 0.f : sZ[size_t(BN * r + 4 * rg + q) * DV + 4 * cg + cc];
-        for (int s = 0; s <= r; ++s) {
-            __syncthreads();  // the previous tile (and block r + 1's Z) is no longer read
-            load_tile(sA, P, T, r, s, t, NT);
-            __syncthreads();
-            mac<4, DV, SUB>(acc, sA + 4 * rg * GS, sZ + size_t(BN * s) * DV + 4 * cg);
-        }
-        __syncthreads();  // every thread has read Z_r
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            *reinterpret_cast<float4*>(sZ + size_t(BN * r + 4 * rg + q) * DV + 4 * cg) =
-                make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-            if (KEEP)
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) u[r][q][cc] += acc[q][cc];
-        }
-    }
-    __syncthreads();
-}
-
-// U (shared [nb * BN][DV]) to the workspace, then o = scale (gamma X_Q + C U).
-template <typename OutT>
-__device__ __forceinline__ void finish(OutT* o, const float* sU, float* sA, const float* C, const Ws& ws, int b,
-                                       int h, int T, int H, int nb, float scale, int t) {
-    const int cg = t & 31, rg = t >> 5;
-    for (int e = t; e < T * (DV / 4); e += NT) {
-        const int i = e / (DV / 4), c4 = e % (DV / 4);
-        *reinterpret_cast<float4*>(ws.U + ((size_t(b) * T + i) * H + h) * DV + 4 * c4) =
-            *reinterpret_cast<const float4*>(sU + size_t(i) * DV + 4 * c4);
-    }
-    for (int r = 0; r < nb; ++r) {
-        float acc[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = BN * r + 4 * rg + q;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < T) x = *reinterpret_cast<const float4*>(ws.xq + ((size_t(b) * T + i) * H + h) * DV + 4 * cg);
-            acc[q][0] = x.x; acc[q][1] = x.y; acc[q][2] = x.z; acc[q][3] = x.w;
-        }
-        for (int s = 0; s <= r; ++s) {
-            __syncthreads();
-            load_tile(sA, C, T, r, s, t, NT);
-            __syncthreads();
-            mac<4, DV, false>(acc, sA + 4 * rg * GS, sU + size_t(BN * s) * DV + 4 * cg);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = BN * r + 4 * rg + q;
-            if (i >= T) continue;
-            OutT* op = o + ((size_t(b) * T + i) * H + h) * DV + 4 * cg;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) store_out(op + cc, scale * acc[q][cc]);
-        }
-    }
-}
-
-// P <- P^2 in place for a [T][T] matrix with tiles on and below the
-// diagonal: (P^2)_rc = sum_{s=c..r} P_rs P_sc.  Block rows from the last to
-// the first, tiles of a row from left to right: the new tile (r, c) is
-// written only after every tile that still needs the old one has been
-// formed (rows above never read row r; later tiles of row r read only
-// columns >= c + 1 of it).  Each thread forms 2 x 4 entries of a tile.
-__device__ __forceinline__ void square_in_place(float* P, float* sA, float* sB, int T, int nb, int t) {
-    const int cg = t & 15, rg = t >> 4;
-    for (int r = nb - 1; r >= 0; --r) {
-        for (int c = 0; c <= r; ++c) {
-            float acc[2][4] = {};
-            for (int s = c; s <= r; ++s) {
-                __syncthreads();
-                load_tile(sA, P, T, r, s, t, NT);
-                load_tile(sB, P, T, s, c, t, NT);
-                __syncthreads();
-                mac<2, GS, false>(acc, sA + 2 * rg * GS, sB + 4 * cg);
-            }
-            store_tile_part<2>(P, T, r, c, 2 * rg, 4 * cg, acc);
-        }
-    }
-    __syncthreads();  // the squared matrix is visible to the whole block
-}
-
-// Squaring form: Z = R; Z <- (I - G) Z; then for f = 1..k-1:
-// P = G^(2^f) (squared in place of G), Z <- (I + P) Z; U = Z.
-template <typename OutT>
-__global__ void __launch_bounds__(NT, 1) squaring_kernel(OutT* __restrict__ o, int T, int H, Ws ws, float scale) {
-    extern __shared__ float smem[];
-    __shared__ int sDepth;
-    const int nb = (T + BN - 1) / BN;
-    float* sZ = smem;                          // [nb * BN][DV]
-    float* sA = sZ + size_t(nb) * BN * DV;     // [BN][GS]
-    float* sB = sA + BN * GS;                  // [BN][GS]
-    const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-    const size_t bh = size_t(b) * H + h;
-    const int d = stream_depth(ws, b, T, t, &sDepth);
-    int k = 0;
-    while ((1 << k) < d + 1) ++k;  // factors: 2^k >= d + 1 terms
-    load_panel(sZ, ws.rr, b, h, T, H, nb, t);
-    __syncthreads();
-    float* P = ws.gs + bh * T * T;
-    float unused[MAXNB][4][4];
-    for (int f = 0; f < k; ++f) {
-        if (f == 0) {
-            apply_panel<true, false>(sZ, sA, P, T, nb, t, unused);
-        } else {
-            square_in_place(P, sA, sB, T, nb, t);
-            apply_panel<false, false>(sZ, sA, P, T, nb, t, unused);
-        }
-    }
-    finish(o, sZ, sA, ws.cs + bh * T * T, ws, b, h, T, H, nb, scale, t);
 }
 
 // Split design, first kernel: W = (I + G)^-1 and M = C W per (stream,
@@ -397,9 +247,6 @@ __global__ void __launch_bounds__(APPLY_NT) apply_kernel(OutT* __restrict__ o, i
     }
 }
 
-__host__ __device__ constexpr size_t panel_smem(int T, int tiles) {
-    return size_t((T + BN - 1) / BN * BN) * DV * 4 + size_t(tiles) * BN * GS * 4;
-}
 constexpr size_t kInvertSmem = size_t(4) * BN * GS * 4 + size_t(BN) * BN;
 constexpr size_t kApplySmem = size_t(2) * BN * GS * 4 + size_t(BN) * BN * 4;
 
@@ -421,13 +268,6 @@ static cudaError_t launch_variant_typed(int variant, int T, int B, int H, OutT* 
                                         cudaStream_t st) {
     dim3 grid(H, B);
     cudaError_t e;
-    if (variant == 2) {
-        static bool attr = false;
-        e = set_smem_once(sv::squaring_kernel<OutT>, sv::panel_smem(kMaxT, 2), attr);
-        if (e != cudaSuccess) return e;
-        sv::squaring_kernel<OutT><<<grid, sv::NT, sv::panel_smem(T, 2), st>>>(o, T, H, ws, scale);
-        return cudaGetLastError();
-    }
     if (variant == 3) {
         static bool attr = false;
         e = set_smem_once(sv::invert_kernel, sv::kInvertSmem, attr);
@@ -446,13 +286,16 @@ static cudaError_t launch_variant_typed(int variant, int T, int B, int H, OutT* 
 }
 
 cudaError_t launch_neumann_tc(int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
+cudaError_t launch_squaring_tc(int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws, cudaStream_t st);
 
 // variant: 1 Neumann series (on tensor cores, neumann_tc.cu; T > 64), 2
-// squaring form, 3 split design (dk = dv = 128).
+// squaring form (on tensor cores, squaring_tc.cu), 3 split design (dk = dv =
+// 128).
 cudaError_t launch_solve_variant(int variant, int T, int B, int H, void* o, int o_bf16, float scale, const Ws& ws,
                                  cudaStream_t st) {
     if (T < 1 || T > kMaxT) return cudaErrorInvalidValue;
     if (variant == 1) return launch_neumann_tc(T, B, H, o, o_bf16, scale, ws, st);
+    if (variant == 2) return launch_squaring_tc(T, B, H, o, o_bf16, scale, ws, st);
     if (o_bf16)
         return launch_variant_typed(variant, T, B, H, static_cast<__nv_bfloat16*>(o), scale, ws, st);
     return launch_variant_typed(variant, T, B, H, static_cast<float*>(o), scale, ws, st);
