@@ -70,15 +70,17 @@ typedef enum { CANOPY_F32 = 0, CANOPY_BF16 = 1 } canopy_dtype;
  * The two series forms (NEUMANN, SQUARING) are accurate while the terms
  * (-G)^m R stay small: on deep paths whose keys are nearly aligned the terms
  * grow before they cancel and fp32 loses them (a 64-node chain of identical
- * keys gives errors of order 1); FWDSUB and SPLIT solve by substitution and
- * keep ~1e-6 at any depth. */
+ * keys gives errors of order 1); FWDSUB and SPLIT solve by substitution,
+ * whose accuracy does not depend on depth (about 1e-6 in fp32 arithmetic at
+ * any depth).  Every strategy multiplies on tcgen05 tensor cores with split
+ * bf16 operands (about 1e-4 max/rms on the pages' bf16 inputs). */
 typedef enum {
     CANOPY_SOLVE_FWDSUB = 0,   /* blocked forward substitution, 64-node blocks            */
     CANOPY_SOLVE_NEUMANN = 1,  /* finite Neumann series, d rounds (Bole's solve)          */
     CANOPY_SOLVE_SQUARING = 2, /* (I - G)(I + G^2)(I + G^4)..., ceil(log2(d + 1)) factors  */
-    CANOPY_SOLVE_SPLIT = 3     /* (I + G)^-1 once per (stream, value head) in the
-                                  workspace, then applied per 64-node block and 64 value
-                                  columns (two launches)                                  */
+    CANOPY_SOLVE_SPLIT = 3     /* (I + G)^-1 and C (I + G)^-1 once per (stream, value
+                                  head) in the workspace, then applied to R by a second
+                                  launch (all 128 value columns as one tile)              */
 } canopy_solve;
 
 /* Flags of canopy_tree_verify. */
