@@ -73,7 +73,7 @@ typedef enum { CANOPY_F32 = 0, CANOPY_BF16 = 1 } canopy_dtype;
  * keys gives errors of order 1); FWDSUB and SPLIT solve by substitution,
  * whose accuracy does not depend on depth (about 1e-6 in fp32 arithmetic at
  * any depth).  Every strategy multiplies on tcgen05 tensor cores with split
- * bf16 operands (about 1e-4 max/rms on the pages' bf16 inputs). */
+ * bf16 operands (1e-4 to 3e-4 max/rms on the pages' bf16 inputs). */
 typedef enum {
     CANOPY_SOLVE_FWDSUB = 0,   /* blocked forward substitution, 64-node blocks            */
     CANOPY_SOLVE_NEUMANN = 1,  /* finite Neumann series, d rounds (Bole's solve)          */
