@@ -13,17 +13,20 @@
 // 64 x 64 tiles, only the tiles on or below the diagonal, since ancestors
 // come first in a topological order).
 //
-// One CTA (256 threads) per (stream b, head h, 64-node row block r):
-//   - Q_r, K_r and the earlier K_s (s < r) come by TMA (128-byte swizzle);
-//     one thread issues [Q_r; K_r] K_s^T for s = 0..r (M = 128, N = 64) into
-//     tensor memory;
-//   - S0 (fp32) passes box by box through a two-slot staging area and is
-//     split into bf16 hi + lo pairs in tensor memory (the A operand);
-//     X^T = S0 [Q_r; K_r]^T (value columns on the lanes, two products);
-//   - warps 0-3 (a lane per row of [Q_r; K_r]) apply the path mask, the
-//     decay and beta to their row of every tile and write the C or G row
-//     segment; warps 4-7 (a lane per value column) write gamma X_Q and R for
-//     the block's nodes.  Every wait is bounded.
+// One CTA (256 threads) per (stream b, head h, 64-node row block r), in two
+// phases that share 256 tensor-memory columns and 84 KB of shared memory, so
+// that two CTAs fit on an SM:
+//   1. S0 (fp32) passes box by box through a two-slot staging area and is
+//      split into bf16 hi + lo pairs in tensor memory (the A operand); one
+//      thread issues X^T = S0 [Q_r; K_r]^T (value columns on the lanes, two
+//      products, Q_r and K_r by TMA with the 128-byte swizzle); warps 4-7 (a
+//      lane per value column) write gamma X_Q and R for the block's nodes;
+//   2. the earlier K_s (s < r) come by TMA into the freed staging area; one
+//      thread issues [Q_r; K_r] K_s^T for s = 0..r (M = 128, N = 64) into the
+//      freed columns; all eight warps (two per row of [Q_r; K_r], tiles
+//      shared between them) apply the path mask, the decay and beta and
+//      write the C or G row segments.
+// Every wait is bounded.
 #include "common.cuh"
 
 namespace canopy {
@@ -34,19 +37,19 @@ constexpr int DV = 128;   // value columns (dk = dv = 128)
 constexpr int TP = 64;    // nodes per block
 constexpr int NT = 256;   // threads per CTA
 constexpr int MAXB = kMaxT / TP;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TA = 0;     // S0 as A: hi [0,64), lo [64,128)
-constexpr uint32_t TX = 128;   // X^T: Q part [128,192), K part [192,256)
-constexpr uint32_t TG = 256;   // [Q_r; K_r] K_s^T: block s at [256 + 64 s, 320 + 64 s)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t TA = 0;     // phase 1: S0 as A: hi [0,64), lo [64,128)
+constexpr uint32_t TX = 128;   // phase 1: X^T: Q part [128,192), K part [192,256)
+constexpr uint32_t TG = 0;     // phase 2: [Q_r; K_r] K_s^T: block s at [64 s, 64 s + 64)
 
 struct Smem {
     static constexpr int QK = 0;                        // [Q_r; K_r] bf16: 2 key atoms x 128 rows x 128 B
-    static constexpr int KS = 32768;                    // K_s (s < r): per tile 2 key atoms x 64 rows x 128 B
-    static constexpr int KS_TILE = 16384;
-    static constexpr int S0S = KS + (MAXB - 1) * KS_TILE;   // S0 staging, two boxes of [128 rows][32 cols]
+    static constexpr int S0S = 32768;                   // phase 1: S0 staging, two boxes of [128 rows][32 cols]
     static constexpr int S0_BOX = 16384;
-    static constexpr int VT = S0S + 2 * S0_BOX;          // V_r bf16: 2 tiles [64 nodes][64 cols]
+    static constexpr int VT = S0S + 2 * S0_BOX;          // phase 1: V_r bf16: 2 tiles [64 nodes][64 cols]
     static constexpr int V_TILE = 8192;
+    static constexpr int KS = S0S;                      // phase 2: K_s (s < r), 2 key atoms x 64 rows x 128 B each
+    static constexpr int KS_TILE = 16384;
     static constexpr int LL = VT + 2 * V_TILE;           // float[kMaxT]: l of head h for every node
     static constexpr int BG = LL + kMaxT * 4;            // float2[64]: (beta, gamma) of block r's nodes
     static constexpr int MASKW = BG + TP * 8;            // u32[64][8]: strict-ancestor words of block r's nodes
@@ -55,6 +58,8 @@ struct Smem {
     static constexpr int FLAG = TMEMSLOT + 4;
     static constexpr int TOTAL = FLAG + 4;
     static_assert(S0S % 1024 == 0 && VT % 1024 == 0 && BAR % 8 == 0, "align");
+    static_assert(KS + (MAXB - 1) * KS_TILE <= LL, "the K_s tiles fit the phase-1 area");
+    static_assert(TOTAL + 1024 <= 113 * 1024, "two CTAs per SM");
 };
 
 enum { BAR_QK = 0, BAR_KS, BAR_V, BAR_S0, BAR_S0B, BAR_AC, BAR_X, NBAR };
@@ -70,7 +75,7 @@ __device__ inline void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
     lo = pack_top(__float_as_uint(x0 - __uint_as_float(h0)), __float_as_uint(x1 - __uint_as_float(h1)));
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT, 2)
     gram_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
                    const float* __restrict__ beta, int T, int H, int HK, Ws ws) {
@@ -100,13 +105,6 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_4d(sQK + 16384, &tmQ, &bars[BAR_QK], 64, hk, n0, b);
         tma_load_4d(sQK + 8192, &tmK, &bars[BAR_QK], 0, hk, n0, b);
         tma_load_4d(sQK + 24576, &tmK, &bars[BAR_QK], 64, hk, n0, b);
-        if (r > 0) {
-            mbar_expect_tx(&bars[BAR_KS], r * L::KS_TILE);
-            for (int s = 0; s < r; ++s) {
-                tma_load_4d(sm + L::KS + s * L::KS_TILE, &tmK, &bars[BAR_KS], 0, hk, TP * s, b);
-                tma_load_4d(sm + L::KS + s * L::KS_TILE + 8192, &tmK, &bars[BAR_KS], 64, hk, TP * s, b);
-            }
-        }
         for (int i = 0; i < 2; ++i) {
             mbar_expect_tx(&bars[BAR_S0 + i], L::S0_BOX);
             tma_load_4d(sm + L::S0S + i * L::S0_BOX, &tmS, &bars[BAR_S0 + i], 32 * i, 0, h, b);
@@ -139,71 +137,8 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t tmem = *sTmem;
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
 
-    if (warp < 4) {
-        // ---- [Q_r; K_r] K_s^T for s = 0..r, then C and G row segments ----------
-        if (tid == 0) {
-            bool ok = mbar_wait(&bars[BAR_QK], 0);
-            if (r > 0) ok = mbar_wait(&bars[BAR_KS], 0) && ok;
-            if (!ok) *sFlag = 1;
-            tc_fence_after();
-            const uint32_t aQK = smem_u32(sQK), aKS = smem_u32(sm + L::KS);
-            for (int s = 0; s <= r; ++s) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
-                    const uint64_t db = (s == r)
-                                            ? sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32)
-                                            : sdesc_sw128(aKS + s * L::KS_TILE + (ks >> 2) * 8192 + (ks & 3) * 32);
-                    mma_bf16_ss(tmem + TG + 64 * s, da, db, idesc_bf16(128, 64), ks != 0);
-                }
-            }
-            mma_commit(&bars[BAR_AC]);
-        }
-        __syncwarp();
-        if (!mbar_wait(&bars[BAR_AC], 0)) *sFlag = 1;
-        tc_fence_after();
-        const int rho = tid;                 // TMEM lane: Q row rho, or K row rho - 64
-        const bool qrow = rho < TP;
-        const int e = rho & (TP - 1), i = n0 + e;
-        const float li = sL[min(i, T - 1)];
-        const float sc = qrow ? 1.f : sBG[e].x;
-        float* dst = (qrow ? ws.cs : ws.gs) + ((size_t(b) * H + h) * T + i) * T;
-        const bool vec = (T & 3) == 0;
-        for (int s = 0; s <= r; ++s) {
-            uint32_t a[64];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                tmem_ld16(lane_base + TG + 64 * s + 16 * q4, *reinterpret_cast<uint32_t(*)[16]>(a + 16 * q4));
-            tmem_wait_ld();
-            if (i >= T) continue;
-            // path bits of row i among nodes 64 s .. 64 s + 63 (C: i included)
-            uint32_t m0 = sMask[e * 8 + 2 * s], m1 = sMask[e * 8 + 2 * s + 1];
-            if (qrow && s == r) {
-                if (e < 32) m0 |= 1u << e;
-                else m1 |= 1u << (e - 32);
-            }
-            float vals[64];
-#pragma unroll
-            for (int jj = 0; jj < 64; ++jj) {
-                const uint32_t bit = (jj < 32) ? ((m0 >> jj) & 1u) : ((m1 >> (jj - 32)) & 1u);
-                const int j = TP * s + jj;
-                vals[jj] = bit ? sc * expf(li - sL[min(j, T - 1)]) * __uint_as_float(a[jj]) : 0.f;
-            }
-            const int jn = min(64, T - TP * s);  // columns inside the tree
-            float* drow = dst + TP * s;
-            if (vec && jn == 64) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    *reinterpret_cast<float4*>(drow + 4 * q) =
-                        make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 64; ++jj)
-                    if (jj < jn) drow[jj] = vals[jj];
-            }
-        }
-    } else {
-        // ---- S0 -> bf16 hi/lo A operand; X^T; gamma X_Q and R --------------------
+    // ---- phase 1 (warps 4-7): S0 -> bf16 hi/lo A operand; X^T; gamma X_Q and R
+    if (warp >= 4) {
         const int c = quad * 32 + lane;  // value column (TMEM lane)
 #pragma unroll 1
         for (int bx = 0; bx < 4; ++bx) {
@@ -272,6 +207,87 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
     }
+    // the staging area, V and the tensor-memory columns are free
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- phase 2: [Q_r; K_r] K_s^T for s = 0..r, then C and G row segments --
+    if (tid == 0) {
+        tc_fence_after();
+        bool ok = !*sFlag;
+        const uint32_t aQK = smem_u32(sQK), aKS = smem_u32(sm + L::KS);
+        if (ok && r > 0) {
+            mbar_expect_tx(&bars[BAR_KS], r * L::KS_TILE);
+            for (int s = 0; s < r; ++s) {
+                tma_load_4d(sm + L::KS + s * L::KS_TILE, &tmK, &bars[BAR_KS], 0, hk, TP * s, b);
+                tma_load_4d(sm + L::KS + s * L::KS_TILE + 8192, &tmK, &bars[BAR_KS], 64, hk, TP * s, b);
+            }
+        }
+        // the diagonal tile first (K_r is at hand), then the earlier ones
+        for (int t = 0; t <= r; ++t) {
+            const int s = (t == 0) ? r : t - 1;
+            if (t == 1 && !mbar_wait(&bars[BAR_KS], 0)) {
+                *sFlag = 1;
+                ok = false;
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t da = sdesc_sw128(aQK + (ks >> 2) * 16384 + (ks & 3) * 32);
+                const uint64_t db = (s == r) ? sdesc_sw128(aQK + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32)
+                                             : sdesc_sw128(aKS + s * L::KS_TILE + (ks >> 2) * 8192 + (ks & 3) * 32);
+                mma_bf16_ss(tmem + TG + 64 * s, da, db, idesc_bf16(128, 64), ks != 0);
+            }
+        }
+        mma_commit(&bars[BAR_AC]);
+    }
+    __syncwarp();
+    if (!mbar_wait(&bars[BAR_AC], 0)) *sFlag = 1;
+    tc_fence_after();
+    {
+        const int rho = tid & 127;           // TMEM lane: Q row rho, or K row rho - 64
+        const bool qrow = rho < TP;
+        const int e = rho & (TP - 1), i = n0 + e;
+        const float li = sL[min(i, T - 1)];
+        const float sc = qrow ? 1.f : sBG[e].x;
+        float* dst = (qrow ? ws.cs : ws.gs) + ((size_t(b) * H + h) * T + min(i, T - 1)) * T;
+        const bool vec = (T & 3) == 0;
+        // warps w and w + 4 serve the same rows and take alternate tiles
+        for (int s = warp >> 2; s <= r && !*sFlag; s += 2) {
+            uint32_t m0 = sMask[e * 8 + 2 * s], m1 = sMask[e * 8 + 2 * s + 1];
+            if (qrow && s == r) {  // C: i on its own path
+                if (e < 32) m0 |= 1u << e;
+                else m1 |= 1u << (e - 32);
+            }
+            const int jn = min(64, T - TP * s);  // columns inside the tree
+            float* drow = dst + TP * s;
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t a[16];
+                tmem_ld16(lane_base + TG + 64 * s + 16 * q4, a);
+                tmem_wait_ld();
+                if (i >= T) continue;
+                float vals[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int jj = 16 * q4 + u;
+                    const uint32_t bit = (jj < 32) ? ((m0 >> jj) & 1u) : ((m1 >> (jj - 32)) & 1u);
+                    const int j = TP * s + jj;
+                    vals[u] = bit ? sc * expf(li - sL[min(j, T - 1)]) * __uint_as_float(a[u]) : 0.f;
+                }
+                if (vec && 16 * q4 + 16 <= jn) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4*>(drow + 16 * q4 + 4 * q) =
+                            make_float4(vals[4 * q], vals[4 * q + 1], vals[4 * q + 2], vals[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        if (16 * q4 + u < jn) drow[16 * q4 + u] = vals[u];
+                }
+            }
+        }
+    }
 
     tc_fence_before();
     __syncthreads();
@@ -279,7 +295,7 @@ __global__ void __launch_bounds__(NT, 1)
         // a wait gave up: let the copies in flight land before leaving
         raise_err(ws.err, CANOPY_DEVERR_TIMEOUT);
         mbar_wait(&bars[BAR_QK], 0);
-        if (r > 0) mbar_wait(&bars[BAR_KS], 0);
+        if (r > 0) mbar_wait(&bars[BAR_KS], 0);  // (bounded; it gives up if the copies were never issued)
         for (int i = 0; i < 4; ++i) mbar_wait(&bars[BAR_S0 + (i & 1)], uint32_t(i >> 1));
         mbar_wait(&bars[BAR_V], 0);
     }
