@@ -310,6 +310,19 @@ def run_canopy(args, world, rank, local):
             torch.cuda.synchronize()
             out.append(a.elapsed_time(b) / G)
     clk = clocks.stop()
+    # warm: the same input set at every launch, so its 46 MB stay in the
+    # 129 MB L2 (reported beside the cold, rotating figure)
+    g_warm = capture_graph(canopy, sets[:1], T, args.solve, G, "verify")
+    g_warm.replay()
+    torch.cuda.synchronize()
+    t_warm = []
+    for _ in range(args.kernel_reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g_warm.replay()
+        b.record()
+        torch.cuda.synchronize()
+        t_warm.append(a.elapsed_time(b) / G)
     total_ms = max_over_ranks(total_ms, world)
     vp_us, prod_us = verify_after_producer(canopy, sets, args.solve, G, args.kernel_reps)
     errs = [canopy.read_device_error(s["ws"]) for s in sets]
@@ -367,6 +380,10 @@ def run_canopy(args, world, rank, local):
             "frac_nominal": vb / (vp_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
             "setting": "each verify follows copy kernels that write its q, k and v (no overlap flags); "
                        f"time of (copies + verify) minus copies alone ({prod_us:.2f} us) per launch"},
+        "verify_warm_l2": {"us_per_launch": 1e3 * statistics.mean(t_warm),
+                           "algorithmic_GBps": vb / (1e3 * statistics.mean(t_warm) * 1e-6) / 1e9,
+                           "setting": "the same input set at every launch (back to back, overlap flags set): "
+                                      "its inputs and outputs stay in L2, so this is not an HBM figure"},
         "roofline_commit": {"bound": "hbm", "achieved": cb / (c_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
                             "frac": cb / (c_us * 1e-6) / 1e9 / peak,
                             "frac_nominal": cb / (c_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, "algorithmic_bytes": cb},
