@@ -19,8 +19,10 @@
 //   1. S0 (fp32) passes box by box through a two-slot staging area and is
 //      split into bf16 hi + lo pairs in tensor memory (the A operand); one
 //      thread issues X^T = S0 [Q_r; K_r]^T (value columns on the lanes, two
-//      products, Q_r and K_r by TMA with the 128-byte swizzle); warps 4-7 (a
-//      lane per value column) write gamma X_Q and R for the block's nodes;
+//      products, Q_r and K_r by TMA with the 128-byte swizzle); all eight
+//      warps (a lane per value column, two warps per lane, each with half of
+//      a box and then half of the nodes) convert S0 and write gamma X_Q and
+//      R for the block's nodes;
 //   2. the earlier K_s (s < r) come by TMA into the freed staging area; one
 //      thread issues [Q_r; K_r] K_s^T for s = 0..r (M = 128, N = 64) into the
 //      freed columns; all eight warps (two per row of [Q_r; K_r], tiles
@@ -137,26 +139,30 @@ __global__ void __launch_bounds__(NT, 2)
     const uint32_t tmem = *sTmem;
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
 
-    // ---- phase 1 (warps 4-7): S0 -> bf16 hi/lo A operand; X^T; gamma X_Q and R
-    if (warp >= 4) {
+    // ---- phase 1 (all eight warps; warps w and w + 4 serve the same TMEM
+    // lanes and split the work): S0 -> bf16 hi/lo A operand; X^T; gamma X_Q
+    // and R
+    {
         const int c = quad * 32 + lane;  // value column (TMEM lane)
+        const int grp = warp >> 2;       // which half of each box / of the nodes
 #pragma unroll 1
         for (int bx = 0; bx < 4; ++bx) {
             const int slot = bx & 1;
             if (!mbar_wait(&bars[BAR_S0 + slot], uint32_t(bx >> 1))) *sFlag = 1;
             const uint8_t* rowp = sm + L::S0S + slot * L::S0_BOX + c * 128;
-            uint32_t wh[16], wl[16];
+            uint32_t wh[8], wl[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * grp + jj;  // 16-byte chunk of the row: 4 keys
                 const float4 f = *reinterpret_cast<const float4*>(rowp + ((j ^ (c & 7)) << 4));
-                split2(f.x, f.y, wh[2 * j], wl[2 * j]);
-                split2(f.z, f.w, wh[2 * j + 1], wl[2 * j + 1]);
+                split2(f.x, f.y, wh[2 * jj], wl[2 * jj]);
+                split2(f.z, f.w, wh[2 * jj + 1], wl[2 * jj + 1]);
             }
-            tmem_st16(lane_base + TA + bx * 16, wh);
-            tmem_st16(lane_base + TA + 64 + bx * 16, wl);
+            tmem_st8(lane_base + TA + bx * 16 + 8 * grp, wh);
+            tmem_st8(lane_base + TA + 64 + bx * 16 + 8 * grp, wl);
             tmem_wait_st();
             tc_fence_before();
-            group_sync(2, 128);  // every thread has read (and stored) box bx
+            __syncthreads();  // every thread has read (and stored) box bx
             if (tid == 128) {
                 if (bx < 2) {
                     mbar_expect_tx(&bars[BAR_S0 + slot], L::S0_BOX);
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(NT, 2)
         const uint8_t* vt = sm + L::VT + (c >> 6) * L::V_TILE;
         const int cb = (c & 63) >> 3, cw = (c & 7) << 1;
 #pragma unroll 1
-        for (int nb = 0; nb < TP; nb += 16) {
+        for (int nb = 32 * grp; nb < 32 * grp + 32; nb += 16) {
             uint32_t xq[16], xk[16];
             tmem_ld16(lane_base + TX + nb, xq);
             tmem_ld16(lane_base + TX + 64 + nb, xk);
